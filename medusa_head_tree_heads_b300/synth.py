@@ -1,0 +1,236 @@
+"""Seeded synthetic inputs for one Medusa decode step.
+
+This module only draws random numbers and lays them out; it holds none of the
+step's arithmetic (no head FFN, no projection, no top-k, no tree, no
+attention, no acceptance).  Both the CUDA path (tests, benchmark) and the CPU
+oracle (tests) take their inputs from here.
+
+Workload shapes follow the method's description in "Medusa Heads"
+(ultralytics glossary): K heads read the final hidden state ``h``; each head
+is a residual SiLU feed-forward layer followed by a vocabulary projection
+that starts as a copy of ``lm_head`` ("Come le teste prevedono i token
+successivi").  The candidate tree is the Cartesian product of the per-depth
+top-k lists ("Attenzione sull'albero e accettazione").
+
+Distributions (``N(0, s)`` below gives the standard deviation):
+  lm_head  ~ N(0, 1/sqrt(H))        (variance 1/H, fan-in scale)
+  W2_k     = lm_head + N(0, 0.01)   (zero-init variant: an exact copy)
+  W1_k, b1 ~ N(0, 0.02)             (zero-init variant: zeros)
+  h, q, k, v (tree and cache) ~ N(0, 1)
+  root_token ~ uniform over the vocabulary
+Every tensor is drawn in fp32 from its own seeded ``torch.Generator`` and then
+rounded (RNE) to the workload's storage type.
+
+Planting.  A plant list ``[(node, token), ...]`` per sequence overwrites the
+tree q/k/v rows of those nodes so that the base model's top token at that
+node is ``token`` with a large margin: every q head of kv group g becomes
+``2*sqrt(Dh)*u_g`` and the node's own key ``15*u_g`` (self score 30 against
+cache scores of spread ~2), and the node's value for group g is
+``24 * M_g[token] / |M_g[token]|`` with ``M_g`` the sum of the lm_head column
+slices of the q heads in group g.  Which nodes and tokens to plant (and how
+many times to redraw ``h_b`` or a node's q row) is decided offline and stored
+with the tests; this module only applies it.
+"""
+from __future__ import annotations
+
+import dataclasses
+import json
+import math
+import os
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import torch
+
+PLANT_GAMMA_Q = 2.0  # q = PLANT_GAMMA_Q * sqrt(Dh) * u
+PLANT_GAMMA_K = 15.0  # k_self = PLANT_GAMMA_K * u
+PLANT_ALPHA_V = 24.0  # |v| = PLANT_ALPHA_V
+
+
+@dataclasses.dataclass(frozen=True)
+class Shape:
+    """One workload: sizes, storage type, acceptance rule and seed."""
+
+    name: str
+    dtype: str  # "f32" or "bf16"
+    hidden: int
+    vocab: int
+    n_heads: int
+    batch: int
+    topk: Tuple[int, ...]  # top-k per tree depth (depth = len(topk))
+    kv_len: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    accept: str  # "greedy" or "typical"
+    planted: Tuple  # ("fixed", d) or ("uniform", lo, hi)
+    seed: int
+    kv_capacity: int = 0  # cache rows per sequence; 0 means kv_len
+    temperature: float = 0.7
+    eps: float = 0.3
+    delta: float = 0.09
+    full_size: bool = False  # the oracle checks every node only when False
+
+    @property
+    def depth(self) -> int:
+        return len(self.topk)
+
+    @property
+    def n_nodes(self) -> int:
+        """Tree rows including the root (sizes of the level products, summed)."""
+        total, level = 1, 1
+        for k in self.topk:
+            level *= k
+            total += level
+        return total
+
+    @property
+    def cap(self) -> int:
+        return self.kv_capacity if self.kv_capacity else self.kv_len
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+# The five stated workloads, then reduced variants that keep every structural
+# feature (head count, tree shape, GQA ratio, acceptance rule) at sizes the
+# oracle finishes in seconds, with ragged vocabulary and cache lengths.
+SHAPES: Dict[str, Shape] = {}
+
+
+def _add(s: Shape) -> None:
+    SHAPES[s.name] = s
+
+
+_add(Shape("tiny-fp32", "f32", 256, 1000, 3, 1, (2, 3), 128, 4, 4, 64, "greedy", ("fixed", 2), 1000))
+_add(Shape("7b-bf16", "bf16", 4096, 32000, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3), 1001,
+           full_size=True))
+_add(Shape("13b-bf16", "bf16", 5120, 32000, 5, 8, (3, 2, 2, 1), 2048, 40, 40, 128, "greedy", ("uniform", 0, 4), 1002,
+           full_size=True))
+_add(Shape("gqa128k-bf16", "bf16", 4096, 128256, 4, 16, (4, 3, 2, 2), 4096, 32, 8, 128, "typical", ("uniform", 0, 4),
+           1003, full_size=True))
+_add(Shape("33b-bf16", "bf16", 6656, 32000, 5, 32, (4, 3, 2, 2, 2), 8192, 52, 52, 128, "greedy", ("uniform", 0, 5),
+           1004, full_size=True))
+# reduced variants
+_add(Shape("7b-mini", "bf16", 640, 3001, 5, 1, (4, 3, 2, 2, 1), 300, 5, 5, 128, "greedy", ("fixed", 3), 2001,
+           kv_capacity=333))
+_add(Shape("13b-mini", "bf16", 384, 2500, 5, 3, (3, 2, 2, 1), 200, 3, 3, 128, "greedy", ("uniform", 0, 4), 2002,
+           kv_capacity=211))
+_add(Shape("gqa-mini", "bf16", 512, 4099, 4, 2, (4, 3, 2, 2), 257, 4, 2, 128, "typical", ("uniform", 0, 4), 2003,
+           kv_capacity=260))
+_add(Shape("33b-mini", "bf16", 256, 1500, 5, 3, (4, 3, 2, 2, 2), 129, 2, 2, 128, "greedy", ("uniform", 0, 5), 2004))
+_add(Shape("tiny-fp32-gqa", "f32", 256, 777, 3, 2, (3, 2), 70, 4, 2, 64, "typical", ("uniform", 0, 2), 2005,
+           kv_capacity=75))
+
+# tensor tags for seed derivation
+_TAG = {"lm_head": 1, "W2": 2, "W1": 3, "b1": 4, "h": 5, "root": 6, "q": 7, "k_tree": 8, "v_tree": 9,
+        "k_cache": 10, "v_cache": 11, "u": 12, "q_redraw": 13}
+
+
+def seed_for(base: int, tag: str, index: int = 0, redraw: int = 0) -> int:
+    """Deterministic 63-bit seed for one tensor (or one row of one)."""
+    x = (base * 1_000_003 + _TAG[tag] * 7_919 + index * 104_729 + redraw * 15_485_863) & 0x7FFF_FFFF_FFFF_FFFF
+    return x
+
+
+def _randn(shape, seed: int) -> torch.Tensor:
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g, dtype=torch.float32)
+
+
+def _cast(x: torch.Tensor, s: Shape) -> torch.Tensor:
+    return x.to(s.torch_dtype)
+
+
+def draw_h_row(s: Shape, b: int, redraw: int = 0) -> torch.Tensor:
+    """Row b of the final hidden state, redraw number ``redraw`` (0 = first)."""
+    return _cast(_randn((s.hidden,), seed_for(s.seed, "h", b, redraw)), s)
+
+
+def draw_q_row(s: Shape, b: int, node: int, redraw: int) -> torch.Tensor:
+    """A fresh q row [Hq, Dh] for (b, node); redraw >= 1."""
+    return _cast(_randn((s.n_q_heads, s.head_dim), seed_for(s.seed, "q_redraw", b * s.n_nodes + node, redraw)), s)
+
+
+def make_weights(s: Shape, zero_init: bool = False) -> Dict[str, torch.Tensor]:
+    """lm_head [V,H], W1 [K,H,H] (out,in), b1 [K,H], W2 [K,V,H]."""
+    H, V, K = s.hidden, s.vocab, s.n_heads
+    lm = _cast(_randn((V, H), seed_for(s.seed, "lm_head")) * (1.0 / math.sqrt(H)), s)
+    W2 = torch.empty((K, V, H), dtype=s.torch_dtype)
+    W1 = torch.empty((K, H, H), dtype=s.torch_dtype)
+    b1 = torch.empty((K, H), dtype=s.torch_dtype)
+    lm32 = lm.to(torch.float32)
+    for k in range(K):
+        if zero_init:
+            W2[k] = lm
+            W1[k].zero_()
+            b1[k].zero_()
+        else:
+            W2[k] = _cast(lm32 + 0.01 * _randn((V, H), seed_for(s.seed, "W2", k)), s)
+            W1[k] = _cast(0.02 * _randn((H, H), seed_for(s.seed, "W1", k)), s)
+            b1[k] = _cast(0.02 * _randn((H,), seed_for(s.seed, "b1", k)), s)
+    del lm32
+    return {"lm_head": lm, "W1": W1, "b1": b1, "W2": W2}
+
+
+def make_activations(s: Shape, h_redraws: Optional[Sequence[int]] = None) -> Dict[str, torch.Tensor]:
+    """h [B,H], root_token [B] int32, tree q [B,T,Hq,Dh], k/v tree [B,T,Hkv,Dh],
+    k/v cache [B,cap,Hkv,Dh] (rows >= kv_len are filled too but never read)."""
+    B, T = s.batch, s.n_nodes
+    h = torch.stack([draw_h_row(s, b, (h_redraws[b] if h_redraws else 0)) for b in range(B)])
+    g = torch.Generator().manual_seed(seed_for(s.seed, "root"))
+    root = torch.randint(0, s.vocab, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    q = _cast(_randn((B, T, s.n_q_heads, s.head_dim), seed_for(s.seed, "q")), s)
+    kt = _cast(_randn((B, T, s.n_kv_heads, s.head_dim), seed_for(s.seed, "k_tree")), s)
+    vt = _cast(_randn((B, T, s.n_kv_heads, s.head_dim), seed_for(s.seed, "v_tree")), s)
+    kc = torch.empty((B, s.cap, s.n_kv_heads, s.head_dim), dtype=s.torch_dtype)
+    vc = torch.empty_like(kc)
+    for b in range(B):  # per sequence, to bound the fp32 temporary
+        kc[b] = _cast(_randn((s.cap, s.n_kv_heads, s.head_dim), seed_for(s.seed, "k_cache", b)), s)
+        vc[b] = _cast(_randn((s.cap, s.n_kv_heads, s.head_dim), seed_for(s.seed, "v_cache", b)), s)
+    return {"h": h, "root_token": root, "q": q, "k_tree": kt, "v_tree": vt, "k_cache": kc, "v_cache": vc}
+
+
+def plant(s: Shape, inputs: Dict[str, torch.Tensor], b: int, node: int, token: int) -> None:
+    """Overwrite the tree q/k/v rows of (b, node) so that the base model's top
+    token at that node is ``token`` (construction in the module docstring)."""
+    Dh, Hq, Hkv = s.head_dim, s.n_q_heads, s.n_kv_heads
+    G = Hq // Hkv
+    lm_row = inputs["lm_head"][token].to(torch.float64)  # [H]
+    for g in range(Hkv):
+        u = _randn((Dh,), seed_for(s.seed, "u", (b * s.n_nodes + node) * Hkv + g)).to(torch.float64)
+        u = u / u.norm()
+        m = torch.zeros(Dh, dtype=torch.float64)
+        for hh in range(g * G, (g + 1) * G):
+            m += lm_row[hh * Dh:(hh + 1) * Dh]
+        inputs["k_tree"][b, node, g] = (PLANT_GAMMA_K * u).to(s.torch_dtype)
+        inputs["v_tree"][b, node, g] = (PLANT_ALPHA_V * m / m.norm()).to(s.torch_dtype)
+        for hh in range(g * G, (g + 1) * G):
+            inputs["q"][b, node, hh] = (PLANT_GAMMA_Q * math.sqrt(Dh) * u).to(s.torch_dtype)
+
+
+def apply_plan(s: Shape, inputs: Dict[str, torch.Tensor], plan: dict) -> None:
+    """Apply a stored plan: q-row redraws, then the planted (node, token) pairs."""
+    for b, node, r in plan.get("q_redraws", []):
+        inputs["q"][b, node] = draw_q_row(s, b, node, r)
+    for b, seq in enumerate(plan["seqs"]):
+        for node, token in seq["plant"]:
+            plant(s, inputs, b, node, token)
+
+
+def make_inputs(s: Shape, plan: Optional[dict] = None, zero_init: bool = False) -> Dict[str, torch.Tensor]:
+    """All step inputs on the CPU; with ``plan`` the stored redraws and plants are applied."""
+    out = make_weights(s, zero_init=zero_init)
+    out.update(make_activations(s, plan.get("h_redraws") if plan else None))
+    if plan:
+        apply_plan(s, out, plan)
+    return out
+
+
+PLANS_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "tests", "golden",
+                          "plans.json")
+
+
+def load_plans(path: str = PLANS_PATH) -> dict:
+    with open(path) as f:
+        return json.load(f)

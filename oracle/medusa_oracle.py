@@ -1,0 +1,386 @@
+"""Plain CPU oracle for one Medusa speculative decode step.
+
+TEST INFRASTRUCTURE.  Only the test suite, the smoke check and the benchmark's
+CPU-baseline / reference arm may import this module; the CUDA library never
+does, and the two share no code.  It is deliberately slow and literal: every
+step is the definition written out in float64 (inputs decoded exactly from
+their stored fp32 or bf16 values), with a library matmul where the definition
+is a matrix product and plain loops elsewhere.
+
+Sources (page title -- section):
+  [P1] "Medusa Heads", ultralytics glossary (Italian):
+       "Come le teste prevedono i token successivi" -- head structure, the
+       zero-initialised head snippet and its printed result;
+       "Attenzione sull'albero e accettazione" -- Cartesian candidate tree,
+       ancestor-only mask, one verification pass, greedy and typical
+       acceptance.
+  [P2] "Tetes de decodage Medusa", aiunderstanding.org -- "Plongee profonde"
+       (tree attention mask, longest matching prefix, typical acceptance is
+       not distribution-exact).
+  [P3] "Medusa: Simple LLM Inference Acceleration Framework with Multiple
+       Decoding Heads", arXiv 2401.10774 -- abstract.
+
+Readings where the pages leave a step open (each is also listed with the
+design notes):
+  R1  head k (1-based) scores position t+k+1; the root of the tree is the base
+      model's token for t+1, given as input (P1 first section).
+  R2  "its own ancestors" includes the node itself, so a chain tree gives the
+      causal mask.
+  R3  attention scale 1/sqrt(Dh); no rotary embedding; q head h reads kv head
+      floor(h / (Hq/Hkv)).
+  R4  lm_head is applied directly to the concatenated attention output of a
+      node (there is no backbone block in this step).
+  R5  ties in top-k and argmax go to the lower token index.
+  R6  heads deeper than the tree still run; their top-1 is reported.
+  R7  typical acceptance: p = softmax(logits / temperature); entropy in nats;
+      threshold min(eps, delta * exp(-H)); a child is kept when p(token) is
+      strictly greater than the threshold; the longest accepted path wins,
+      ties to the lowest node index at the first divergence; the bonus token
+      is the argmax at the last accepted node.
+  R8  the attention output is rounded to its storage type (bf16 or fp32)
+      before the verification projection reads it.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+
+# ----------------------------------------------------------------- decoding --
+
+def decode(a: np.ndarray) -> np.ndarray:
+    """Exact float64 value of stored data.  uint16 arrays hold bf16 bit
+    patterns (the upper half of an fp32); float arrays are widened."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 (ties to even), returned as
+    float64.  bf16 keeps 8 exponent bits and 7 stored mantissa bits."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    ax = np.abs(x)
+    tiny = ax < 2.0 ** -126  # bf16 subnormal range: spacing 2^-133
+    q = x[tiny] / 2.0 ** -133
+    out[tiny] = np.round(q) * 2.0 ** -133  # np.round rounds halves to even
+    xn = x[~tiny]
+    bits = xn.view(np.uint64)
+    keep = (bits >> np.uint64(45)) & np.uint64(1)
+    bits = (bits + np.uint64((1 << 44) - 1) + keep) & ~np.uint64((1 << 45) - 1)
+    out[~tiny] = bits.view(np.float64)
+    return out
+
+
+def round_to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
+    """R8: the value the step stores for the attention output."""
+    if dtype == "bf16":
+        return round_to_bf16(x)
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- the heads --
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """SiLU(x) = x * sigmoid(x)  [P1, "Come le teste prevedono..."]."""
+    return x / (1.0 + np.exp(-x))
+
+
+def head_hidden(h, W1, b1) -> np.ndarray:
+    """z[b,k] = h[b] + SiLU(W1_k h[b] + b1_k): the residual SiLU feed-forward
+    layer of each Medusa head [P1, "Come le teste prevedono i token
+    successivi"].  h [B,H], W1 [K,H,H] (out, in), b1 [K,H] -> z [B,K,H]."""
+    h = decode(h)
+    K = W1.shape[0]
+    B, H = h.shape
+    z = np.empty((B, K, H))
+    for k in range(K):
+        Wk = decode(W1[k])
+        bk = decode(b1[k])
+        a = h @ Wk.T + bk  # [B,H]
+        z[:, k, :] = h + silu(a)
+    return z
+
+
+def head_logits(z: np.ndarray, W2, heads: Optional[Sequence[int]] = None) -> np.ndarray:
+    """logits[b,k,v] = W2_k[v] . z[b,k]: the vocabulary projection of each head
+    (no bias) [P1, same section].  z [B,K,H], W2 [K,V,H] -> [B,K,V]."""
+    B, K, H = z.shape
+    V = W2.shape[1]
+    ks = range(K) if heads is None else heads
+    out = np.full((B, K, V), np.nan)
+    for k in ks:
+        out[:, k, :] = z[:, k, :] @ decode(W2[k]).T
+    return out
+
+
+def base_logits(h, lm_head) -> np.ndarray:
+    """lm_head(h): the base model's next-token scores [P1, same section]."""
+    return decode(h) @ decode(lm_head).T
+
+
+def topk_lists(logits: np.ndarray, topk: Sequence[int]):
+    """Per-head top-k (R5, R6): head d (0-based) keeps topk[d] tokens when
+    d < depth, else 1; order is descending logit, ties to the lower index.
+    Returns idx int32 [B,K,kmax] (pad -1) and val float64 [B,K,kmax] (pad -inf)."""
+    B, K, V = logits.shape
+    kmax = max(topk)
+    idx = np.full((B, K, kmax), -1, dtype=np.int32)
+    val = np.full((B, K, kmax), -np.inf)
+    ids = np.arange(V)
+    for b in range(B):
+        for k in range(K):
+            n = topk[k] if k < len(topk) else 1
+            # library sort on the key (-logit, token id): primary key last
+            order = np.lexsort((ids, -logits[b, k]))[:n]
+            idx[b, k, :n] = order
+            val[b, k, :n] = logits[b, k, order]
+    return idx, val
+
+
+# ----------------------------------------------------------------- the tree --
+
+class Tree:
+    """Cartesian candidate tree [P1, "Attenzione sull'albero e accettazione"]:
+    the heads' top-k lists combined by Cartesian product, prefixes shared.
+    Nodes are numbered breadth-first: node 0 is the root; the nodes of depth d
+    follow those of depth d-1, ordered by parent, then by rank in the head-d
+    list.  Every branch at depth d takes the same head-d list."""
+
+    def __init__(self, topk: Sequence[int]):
+        self.topk = list(topk)
+        self.depth_max = len(self.topk)
+        parent, depth, rank = [-1], [0], [0]
+        level = [0]
+        for d in range(1, self.depth_max + 1):
+            nxt = []
+            for p in level:
+                for r in range(self.topk[d - 1]):
+                    parent.append(p)
+                    depth.append(d)
+                    rank.append(r)
+                    nxt.append(len(parent) - 1)
+            level = nxt
+        self.parent = np.array(parent, dtype=np.int32)
+        self.depth = np.array(depth, dtype=np.int32)
+        self.rank = np.array(rank, dtype=np.int32)
+        self.T = len(parent)
+        self.leaves = level
+        self.children: List[List[int]] = [[] for _ in range(self.T)]
+        for i in range(1, self.T):
+            self.children[parent[i]].append(i)
+        # R2: node i sees exactly the nodes on its chain to the root, itself included
+        self.mask = np.zeros((self.T, self.T), dtype=bool)
+        for i in range(self.T):
+            j = i
+            while j >= 0:
+                self.mask[i, j] = True
+                j = parent[j]
+        self.paths = np.array([self.chain(l) for l in self.leaves], dtype=np.int32)
+
+    def chain(self, i: int) -> List[int]:
+        """Nodes from the root down to i."""
+        out = []
+        while i >= 0:
+            out.append(i)
+            i = int(self.parent[i])
+        return out[::-1]
+
+    def tokens(self, topk_idx: np.ndarray, root_token: Sequence[int]) -> np.ndarray:
+        """token[b,0] = root token (R1); token[b,i] = head (depth_i)'s candidate
+        of rank rank_i."""
+        B = topk_idx.shape[0]
+        tok = np.zeros((B, self.T), dtype=np.int32)
+        for b in range(B):
+            tok[b, 0] = root_token[b]
+            for i in range(1, self.T):
+                tok[b, i] = topk_idx[b, self.depth[i] - 1, self.rank[i]]
+        return tok
+
+
+# --------------------------------------------------------- tree attention ---
+
+def tree_attention(q, k_tree, v_tree, k_cache, v_cache, kv_len: int, mask: np.ndarray,
+                   nodes: Optional[Sequence[int]] = None, batches: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Every tree node attends, in one pass, to the whole KV cache and to the
+    tree nodes its mask row allows [P1, "Attenzione sull'albero e
+    accettazione"; P2, "Plongee profonde"]:
+        o[b,i,h] = sum_j softmax_j(q[b,i,h] . k_j / sqrt(Dh)) v_j
+    over j in cache[0..kv_len) and {tree node j : mask[i,j]}, with kv head
+    floor(h/G) (R3).  Shapes: q [B,T,Hq,Dh], k/v tree [B,T,Hkv,Dh], k/v cache
+    [B,cap,Hkv,Dh].  Returns o [B,T,Hq*Dh] in float64; rows outside
+    ``nodes`` / ``batches`` are NaN."""
+    B, T, Hq, Dh = q.shape
+    Hkv = k_tree.shape[2]
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(Dh)
+    nodes = list(range(T)) if nodes is None else list(nodes)
+    batches = list(range(B)) if batches is None else list(batches)
+    o = np.full((B, T, Hq * Dh), np.nan)
+    for b in batches:
+        for g in range(Hkv):
+            Kc = decode(k_cache[b, :kv_len, g, :])
+            Vc = decode(v_cache[b, :kv_len, g, :])
+            Kt = decode(k_tree[b, :, g, :])
+            Vt = decode(v_tree[b, :, g, :])
+            for h in range(g * G, (g + 1) * G):
+                Q = decode(q[b, nodes, h, :])  # [n,Dh]
+                s_cache = (Q @ Kc.T) * scale  # [n,L]
+                s_tree = (Q @ Kt.T) * scale  # [n,T]
+                s_tree = np.where(mask[nodes, :], s_tree, -np.inf)
+                s = np.concatenate([s_cache, s_tree], axis=1)
+                s = s - s.max(axis=1, keepdims=True)
+                p = np.exp(s)
+                p = p / p.sum(axis=1, keepdims=True)
+                out = p[:, :kv_len] @ Vc + p[:, kv_len:] @ Vt
+                o[b, nodes, h * Dh:(h + 1) * Dh] = out
+    return o
+
+
+# -------------------------------------------------------------- verification -
+
+def verify_stats(o_stored: np.ndarray, lm_head, temperature: Optional[float] = None,
+                 rows: Optional[Sequence[int]] = None, chunk: int = 256) -> Dict[str, np.ndarray]:
+    """Base-model scores of every tree node, lm_head . o_i (R4), and their
+    summaries [P1, "Attenzione sull'albero e accettazione"]:
+      argmax (R5) and max logit, for greedy acceptance;
+      with a temperature: log-partition lse = log sum exp(logit/temp) and
+      entropy H = -sum p log p of p = softmax(logit/temp), for typical
+      acceptance;
+      'second', the runner-up score, used only to check input margins.
+    o_stored [N,H] (already rounded to storage, R8).  Returns float64 arrays of
+    length N (NaN / -1 outside ``rows``), plus 'logits' for the rows when N is
+    small enough to keep them."""
+    N = o_stored.shape[0]
+    rows = list(range(N)) if rows is None else list(rows)
+    W = decode(lm_head)
+    res = {"argmax": np.full(N, -1, dtype=np.int64), "maxlogit": np.full(N, np.nan),
+           "second": np.full(N, np.nan), "lse": np.full(N, np.nan), "entropy": np.full(N, np.nan)}
+    for c in range(0, len(rows), chunk):
+        rr = rows[c:c + chunk]
+        L = o_stored[rr] @ W.T  # [n,V]
+        res["argmax"][rr] = np.argmax(L, axis=1)  # first maximum = lowest index
+        res["maxlogit"][rr] = L.max(axis=1)
+        res["second"][rr] = np.sort(L, axis=1)[:, -2]  # runner-up score (margin checks)
+        if temperature is not None:
+            x = L / temperature
+            m = x.max(axis=1, keepdims=True)
+            e = np.exp(x - m)
+            Z = e.sum(axis=1, keepdims=True)
+            p = e / Z
+            res["lse"][rr] = (m + np.log(Z))[:, 0]
+            with np.errstate(divide="ignore", invalid="ignore"):
+                plogp = np.where(p > 0, p * np.log(p), 0.0)
+            res["entropy"][rr] = -plogp.sum(axis=1)
+    return res
+
+
+def token_logprob(o_stored_row: np.ndarray, lm_head, token: int, temperature: float, lse: float) -> float:
+    """log p(token) under softmax(lm_head . o / temperature)."""
+    return float(o_stored_row @ decode(lm_head[token])) / temperature - lse
+
+
+def typical_threshold(entropy: float, eps: float, delta: float) -> float:
+    """Entropy-tied acceptance threshold (R7): min(eps, delta * exp(-H))."""
+    return min(eps, delta * math.exp(-entropy))
+
+
+# ---------------------------------------------------------------- acceptance -
+
+def accept_greedy(tree: Tree, tokens_b: np.ndarray, argmax_b: np.ndarray):
+    """Greedy acceptance [P1, "Attenzione sull'albero e accettazione"]: a
+    candidate is kept when it equals the base model's top choice at its
+    parent; walk from the root while some child matches (tokens of one
+    top-k list are distinct, so at most one does).  Returns
+    (length, tokens, nodes incl. root, bonus = top choice at the last node)."""
+    cur, nodes, toks = 0, [0], []
+    for _ in range(tree.depth_max):
+        nxt = None
+        for c in tree.children[cur]:
+            if tokens_b[c] == argmax_b[cur]:
+                nxt = c
+                break
+        if nxt is None:
+            break
+        nodes.append(nxt)
+        toks.append(int(tokens_b[nxt]))
+        cur = nxt
+    return len(toks), toks, nodes, int(argmax_b[cur])
+
+
+def accept_typical(tree: Tree, tokens_b: np.ndarray, argmax_b: np.ndarray, keep_edge):
+    """Typical acceptance (R7): ``keep_edge(parent, child)`` says whether the
+    child's token clears its parent's entropy-tied threshold; the longest
+    chain of kept edges from the root wins, ties to the lowest node index at
+    the first divergence (a depth-first walk in node order keeps the first
+    longest chain it meets)."""
+    best = [0]
+
+    def walk(path):
+        nonlocal best
+        if len(path) > len(best):
+            best = list(path)
+        for c in tree.children[path[-1]]:
+            if keep_edge(path[-1], c):
+                walk(path + [c])
+
+    walk([0])
+    toks = [int(tokens_b[n]) for n in best[1:]]
+    return len(toks), toks, best, int(argmax_b[best[-1]])
+
+
+# -------------------------------------------------------------- whole step --
+
+def step(inp: Dict[str, np.ndarray], shape, nodes_only: Optional[Dict[int, Sequence[int]]] = None) -> Dict:
+    """One decode step, stages in order: heads, top-k, tree, tree attention,
+    verification, acceptance.  ``inp`` holds numpy arrays (bf16 as uint16
+    bit patterns); ``shape`` carries sizes and the acceptance rule.  With
+    ``nodes_only`` = {b: [nodes]} the attention and verification run only on
+    those nodes (acceptance then must not leave them)."""
+    topk = list(shape.topk)
+    z = head_hidden(inp["h"], inp["W1"], inp["b1"])
+    logits = head_logits(z, inp["W2"])
+    idx, val = topk_lists(logits, topk)
+    tree = Tree(topk)
+    tok = tree.tokens(idx, inp["root_token"])
+    B, T = tok.shape
+    H = shape.hidden
+    o = np.full((B, T, H), np.nan)
+    for b in range(B):
+        nb = None if nodes_only is None else nodes_only[b]
+        ob = tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"], inp["v_cache"],
+                            shape.kv_len, tree.mask, nodes=nb, batches=[b])
+        o[b] = ob[b]
+    o_st = round_to_storage(o, shape.dtype)
+    typical = shape.accept == "typical"
+    flat = o_st.reshape(B * T, H)
+    rows = None
+    if nodes_only is not None:
+        rows = [b * T + i for b in range(B) for i in nodes_only[b]]
+    stats = verify_stats(flat, inp["lm_head"], shape.temperature if typical else None, rows=rows)
+    argmax = stats["argmax"].reshape(B, T)
+    res = {"z": z, "head_logits": logits, "topk_idx": idx, "topk_val": val, "tree": tree, "tokens": tok,
+           "attn_out": o_st, "argmax": argmax, "maxlogit": stats["maxlogit"].reshape(B, T),
+           "second": stats["second"].reshape(B, T), "lse": stats["lse"].reshape(B, T), "entropy": stats["entropy"].reshape(B, T),
+           "accept_len": [], "acc_tokens": [], "acc_nodes": [], "bonus": []}
+    for b in range(B):
+        if typical:
+            def keep(p, c, b=b):
+                row = flat[b * T + p]
+                if np.isnan(row).any():
+                    return False
+                lp = token_logprob(row, inp["lm_head"], int(tok[b, c]), shape.temperature, stats["lse"][b * T + p])
+                thr = typical_threshold(stats["entropy"][b * T + p], shape.eps, shape.delta)
+                return math.exp(lp) > thr
+            n, tk, nd, bonus = accept_typical(tree, tok[b], argmax[b], keep)
+        else:
+            n, tk, nd, bonus = accept_greedy(tree, tok[b], argmax[b])
+        res["accept_len"].append(n)
+        res["acc_tokens"].append(tk)
+        res["acc_nodes"].append(nd)
+        res["bonus"].append(bonus)
+    return res

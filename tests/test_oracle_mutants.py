@@ -1,0 +1,145 @@
+"""Planted mistakes in a copy of the oracle (CPU only) must fail the pins:
+evidence that the pins would catch a dropped term, a wrong sign or index, or
+a transposed operand in the oracle itself."""
+from __future__ import annotations
+
+import math
+import types
+
+import numpy as np
+import pytest
+
+from oracle import medusa_oracle as O
+from tests import test_oracle_pins as P
+
+
+def mutant(**repl):
+    m = types.ModuleType("oracle_mutant")
+    m.__dict__.update({k: v for k, v in O.__dict__.items() if not k.startswith("__")})
+    m.__dict__.update(repl)
+    return m
+
+
+def _no_residual(h, W1, b1):
+    h = O.decode(h)
+    z = np.empty((h.shape[0], W1.shape[0], h.shape[1]))
+    for k in range(W1.shape[0]):
+        z[:, k] = O.silu(h @ O.decode(W1[k]).T + O.decode(b1[k]))
+    return z
+
+
+def _no_bias(h, W1, b1):
+    h = O.decode(h)
+    z = np.empty((h.shape[0], W1.shape[0], h.shape[1]))
+    for k in range(W1.shape[0]):
+        z[:, k] = h + O.silu(h @ O.decode(W1[k]).T)
+    return z
+
+
+def _transposed_w1(h, W1, b1):
+    h = O.decode(h)
+    z = np.empty((h.shape[0], W1.shape[0], h.shape[1]))
+    for k in range(W1.shape[0]):
+        z[:, k] = h + O.silu(h @ O.decode(W1[k]) + O.decode(b1[k]))
+    return z
+
+
+def _silu_sign(x):
+    return x / (1.0 + np.exp(x))
+
+
+def _topk_high_tie(logits, topk):
+    B, K, V = logits.shape
+    idx = np.full((B, K, max(topk)), -1, dtype=np.int32)
+    val = np.full((B, K, max(topk)), -np.inf)
+    for b in range(B):
+        for k in range(K):
+            n = topk[k] if k < len(topk) else 1
+            order = np.lexsort((-np.arange(V), -logits[b, k]))[:n]
+            idx[b, k, :n] = order
+            val[b, k, :n] = logits[b, k, order]
+    return idx, val
+
+
+class _DescTree(O.Tree):
+    """mask transposed: a node sees its descendants instead of its ancestors"""
+
+    def __init__(self, topk):
+        super().__init__(topk)
+        self.mask = self.mask.T.copy()
+
+
+class _NoSelfTree(O.Tree):
+    """mask without the node itself"""
+
+    def __init__(self, topk):
+        super().__init__(topk)
+        np.fill_diagonal(self.mask, False)
+        self.mask[0, 0] = True
+
+
+def _attn_scale_dh(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=None, batches=None):
+    Dh = q.shape[-1]
+    return O.tree_attention(q * (math.sqrt(Dh) / Dh), k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes, batches)
+
+
+def _attn_wrong_group(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=None, batches=None):
+    # q head h reads kv head h % Hkv instead of h // G
+    Hq, Hkv = q.shape[2], k_tree.shape[2]
+    G = Hq // Hkv
+    perm = [(h % Hkv) * G + h // Hkv for h in range(Hq)]
+    inv = np.argsort(perm)
+    o = O.tree_attention(q[:, :, perm], k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes, batches)
+    B, T, _ = o.shape
+    Dh = q.shape[3]
+    return o.reshape(B, T, Hq, Dh)[:, :, inv].reshape(B, T, Hq * Dh)
+
+
+def _greedy_child_argmax(tree, tokens_b, argmax_b):
+    cur, nodes, toks = 0, [0], []
+    for _ in range(tree.depth_max):
+        nxt = None
+        for c in tree.children[cur]:
+            if tokens_b[c] == argmax_b[c]:  # wrong index: the child's own choice
+                nxt = c
+                break
+        if nxt is None:
+            break
+        nodes.append(nxt)
+        toks.append(int(tokens_b[nxt]))
+        cur = nxt
+    return len(toks), toks, nodes, int(argmax_b[cur])
+
+
+def _argmax_last(o_stored, lm_head, temperature=None, rows=None, chunk=256):
+    res = O.verify_stats(o_stored, lm_head, temperature, rows, chunk)
+    L = o_stored @ O.decode(lm_head).T
+    res["argmax"] = L.shape[1] - 1 - np.argmax(L[:, ::-1], axis=1)
+    return res
+
+
+def _threshold_no_exp(entropy, eps, delta):
+    return min(eps, delta * entropy)
+
+
+MUTANTS = [
+    ("head drops the residual", dict(head_hidden=_no_residual), P.check_zero_init),
+    ("head drops the bias", dict(head_hidden=_no_bias), P.check_head_vs_torch),
+    ("head W1 transposed", dict(head_hidden=_transposed_w1), P.check_head_vs_torch),
+    ("SiLU sign flipped", dict(silu=_silu_sign), P.check_silu),
+    ("top-k ties to the higher index", dict(topk_lists=_topk_high_tie), P.check_topk),
+    ("mask sees descendants", dict(Tree=_DescTree), P.check_tree_2x3),
+    ("mask drops the node itself", dict(Tree=_NoSelfTree), P.check_attention_paths),
+    ("attention scale 1/Dh", dict(tree_attention=_attn_scale_dh), P.check_attention_paths),
+    ("GQA group index", dict(tree_attention=_attn_wrong_group), P.check_attention_paths),
+    ("greedy compares the child's own argmax", dict(accept_greedy=_greedy_child_argmax), P.check_greedy_lossless),
+    ("argmax ties to the last index", dict(verify_stats=_argmax_last), P.check_verify),
+    ("threshold without exp", dict(typical_threshold=_threshold_no_exp), P.check_verify),
+]
+
+
+@pytest.mark.parametrize("name,repl,check", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, repl, check):
+    m = mutant(**repl)
+    with pytest.raises(AssertionError):
+        check(m)
