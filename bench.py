@@ -1,0 +1,330 @@
+"""Benchmark of one Medusa decode step (heads + top-k, Cartesian tree, tree
+attention, verification, acceptance) on one B300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl medusa|reference]
+
+Prints one JSON line (rank 0).  A "step" is one medusa_step call over the
+whole batch of the workload; `value` is steps/s summed over ranks.  With N > 1
+(torchrun) every rank runs an independent replica of the workload: the step
+has no cross-sequence exchange at batch 1, so there is no collective on the
+data path (weak scaling).  `--impl reference` times the plain CPU oracle
+instead (the only reference implementation of this path), on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from medusa_head_tree_heads_b300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "7b-bf16"
+METRIC = "Medusa decode steps/s at 7B shape; achieved HBM GB/s vs B300 peak"
+
+
+def algorithmic_bytes(s) -> dict:
+    """Bytes each kernel must move at least once per step (weights and cache
+    read once, logits never materialised)."""
+    e = 2 if s.dtype == "bf16" else 4
+    B, H, V, K, T = s.batch, s.hidden, s.vocab, s.n_heads, s.n_nodes
+    kv = 2 * B * s.kv_len * s.n_kv_heads * s.head_dim * e
+    tree_qkv = B * T * (s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim * e
+    return {
+        "head_layer": (K * H * H + K * H + B * H) * e + B * K * H * 4,
+        "head_proj_topk": K * V * H * e + B * K * H * 4,
+        "tree_attn": kv + tree_qkv + B * T * H * e,
+        "verify_proj": V * H * e + B * T * H * e,
+        "step": (K * (H * H + H) + K * V * H + V * H + B * H) * e + kv + tree_qkv,
+    }
+
+
+def flops(s) -> dict:
+    B, H, V, K, T = s.batch, s.hidden, s.vocab, s.n_heads, s.n_nodes
+    return {"heads": 2 * B * K * (H * H + V * H), "verify": 2 * B * T * V * H,
+            "attn": 4 * B * T * s.n_q_heads * s.head_dim * (s.kv_len + s.depth + 1)}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "source": "fallback"}
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_inputs(inp):
+    import numpy as np
+    out = {}
+    for k, v in inp.items():
+        out[k] = v.view(torch.int16).numpy().view(np.uint16) if v.dtype == torch.bfloat16 else v.numpy()
+    return out
+
+
+def time_oracle(s, inp, budget_s: float = 20.0) -> dict:
+    """The oracle as it stands, on this host's cores: whole steps until the
+    time budget is used (at least one)."""
+    from oracle import medusa_oracle as O
+    n = oracle_inputs(inp)
+    times = []
+    t_all = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        O.step(n, s)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > budget_s:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": len(times) / sum(times), "unit": "steps/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(times)} whole step(s) of {s.name} (numpy float64, BLAS on all cores)",
+            "seconds": sum(times)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    s = synth.SHAPES[args.workload]
+    plan = synth.load_plans()[s.name]
+    inp = synth.make_inputs(s, plan)
+    # each timed "step" is one whole oracle step (bounded: a few minutes for K + W)
+    from oracle import medusa_oracle as O
+    n = oracle_inputs(inp)
+    for _ in range(args.warmup):
+        O.step(n, s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.step(n, s)
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": s.name, "batch": s.batch, "hidden": s.hidden, "vocab": s.vocab,
+                       "heads": s.n_heads, "topk": list(s.topk), "tree_nodes": s.n_nodes, "kv_len": s.kv_len},
+            "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} whole step(s) of {s.name} after {args.warmup} warm-up"},
+            "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_medusa(args, world, rank, local):
+    from medusa_head_tree_heads_b300 import medusa as M
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    s = synth.SHAPES[args.workload]
+    plan = synth.load_plans()[s.name]
+    inp = synth.make_inputs(s, plan)
+    dinp = {k: v.cuda() for k, v in inp.items()}
+    cfg = M.make_config(s)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_outputs(cfg)
+    io = M.step_io(dinp, out)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        M.medusa_step(cfg, io, ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert M.medusa_get_device_error(ws) == 0
+    # sanity: the planted acceptance
+    acc = out["accept_len"].cpu().tolist()
+    planted = [q["depth"] for q in plan["seqs"]]
+
+    # ---- timed region: K steps, inputs resident in HBM (1.7+ GB > L2)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = reduce_max(ms, world)
+    value = world * 1e3 / ms
+
+    # ---- per-kernel durations (same step with events around each kernel)
+    nk = len(M.STEP_KERNELS)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(args.steps)]
+    for row in evs:  # torch creates the CUDA event lazily, at its first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        M.medusa_step_profiled(cfg, io, ws, evs[i])
+    torch.cuda.synchronize()
+    per_kernel = {}
+    for k, name in enumerate(M.STEP_KERNELS):
+        per_kernel[name] = statistics.mean(evs[i][2 * k].elapsed_time(evs[i][2 * k + 1]) for i in range(args.steps))
+    byts = algorithmic_bytes(s)
+    peaks = measured_peaks()
+    dom = "head_proj_topk"
+    achieved = byts[dom] / (per_kernel[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": peaks["source"], "algorithmic_bytes": byts[dom],
+                "kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
+                "step_achieved_gbs": round(byts["step"] / (ms * 1e-3) / 1e9, 1),
+                "step_frac": round(byts["step"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+
+    # ---- end to end through the public API: per-step inputs from pinned host
+    # memory, results read back to the host every step
+    step_in = ["h", "root_token", "q", "k_tree", "v_tree"]
+    host_in = {k: inp[k].pin_memory() for k in step_in}
+    step_out = ["accept_len", "acc_tokens", "bonus"]
+    host_out = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory() for k in step_out}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def e2e_step():
+        for k in step_in:
+            dinp[k].copy_(host_in[k], non_blocking=True)
+        M.medusa_step(cfg, io, ws)
+        for k in step_out:
+            host_out[k].copy_(out[k], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_dt = reduce_max((time.perf_counter() - t0) / args.steps, world)
+    assert host_out["accept_len"].tolist() == planted
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
+            "config": {"workload": s.name, "batch": s.batch, "hidden": s.hidden, "vocab": s.vocab,
+                       "heads": s.n_heads, "topk": list(s.topk), "tree_nodes": s.n_nodes, "kv_len": s.kv_len,
+                       "q_heads": s.n_q_heads, "kv_heads": s.n_kv_heads, "head_dim": s.head_dim,
+                       "accept": s.accept, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (no flush)", "accept_len": acc},
+            "roofline": roofline,
+            "e2e": {"value": round(world / e2e_dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * nk, "clocks": clk.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(s, inp, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.SHAPES))
+    ap.add_argument("--impl", default="medusa", choices=["medusa", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        # each oracle step takes seconds: keep the whole run within a few minutes
+        args.steps, args.warmup = min(args.steps, 20), min(args.warmup, 2)
+        run_reference(args, world, rank)
+    else:
+        run_medusa(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

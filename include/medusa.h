@@ -1,0 +1,212 @@
+/*
+ * medusa.h -- C ABI of libmedusa.so: one Medusa speculative decode step on a
+ * B300 (sm_103a).
+ *
+ * The step (sources: "Medusa Heads", ultralytics glossary, sections "Come le
+ * teste prevedono i token successivi" and "Attenzione sull'albero e
+ * accettazione"; "Tetes de decodage Medusa", aiunderstanding.org, section
+ * "Plongee profonde"; arXiv 2401.10774, abstract):
+ *   1. K Medusa heads read the final hidden state h:
+ *        z_k = h + SiLU(W1_k h + b1_k),  logits_k = W2_k z_k
+ *      and each keeps its top-k tokens                    -> medusa_heads_topk
+ *   2. the per-depth top-k lists are combined by Cartesian product into a
+ *      prefix-sharing candidate tree whose attention mask lets a node see
+ *      only its ancestors (and itself)                    -> medusa_tree_build
+ *   3. all tree nodes attend, in one pass, to the KV cache and to their
+ *      ancestors                                           -> medusa_tree_attn
+ *   4. the base lm_head scores every node; the longest branch the base model
+ *      agrees with is kept (greedy: candidate == top choice; typical: the
+ *      candidate's probability exceeds an entropy-tied threshold)
+ *                                                          -> medusa_verify_accept
+ *   medusa_step runs 1-4 in order on one stream.
+ *
+ * Conventions
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *     caller allocates and owns all memory (inputs, outputs, the tree arrays
+ *     and the workspace).  The library allocates nothing per call.
+ *   - All tensors are dense row-major in the layouts given below; the
+ *     floating-point tensors use the config's dtype (fp32 or bf16) unless a
+ *     type is named; pointers to bf16/fp32 tensors must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  A non-zero return means nothing was enqueued (host
+ *     validation failed) or a launch failed.  Faults detected on the device
+ *     (an index out of range, a bounded wait that ran out) set an error word
+ *     in the workspace, read with medusa_get_device_error.
+ *   - The workspace (medusa_workspace_bytes) must be zero-filled once after
+ *     allocation; every call leaves it ready for the next one.  Calls that
+ *     share a workspace must not overlap on the GPU.
+ *
+ * Symbols: B batch, H hidden, V vocab, K heads, D tree depth, k_d top-k at
+ * depth d, T = 1 + sum_d prod_{j<=d} k_j tree nodes (root included),
+ * NL = prod_d k_d leaves, W = ceil(T/32) mask words per node, L kv_len,
+ * Lc kv_capacity, Hq/Hkv query/kv heads, Dh head dim (Hq*Dh == H).
+ */
+#ifndef MEDUSA_H
+#define MEDUSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MEDUSA_MAX_DEPTH 8   /* D <= 8 */
+#define MEDUSA_MAX_HEADS 8   /* K <= 8 */
+#define MEDUSA_MAX_TOPK 16   /* k_d <= 16 */
+#define MEDUSA_MAX_NODES 512 /* T <= 512 */
+
+typedef enum {
+  MEDUSA_OK = 0,
+  MEDUSA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, inconsistent sizes */
+  MEDUSA_ERR_UNSUPPORTED = -2, /* sizes outside the limits above */
+  MEDUSA_ERR_CUDA = -3,        /* a CUDA launch or runtime call failed */
+  MEDUSA_ERR_TIMEOUT = -4,     /* device: a bounded wait ran out */
+  MEDUSA_ERR_DEVICE = -5       /* device: an index check failed */
+} medusa_status_t;
+
+typedef enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 } medusa_dtype_t;
+typedef enum { MEDUSA_ACCEPT_GREEDY = 0, MEDUSA_ACCEPT_TYPICAL = 1 } medusa_accept_t;
+
+/* Sizes and options of one step (host memory, read during the call only). */
+typedef struct {
+  int32_t batch;                   /* B >= 1 */
+  int32_t hidden;                  /* H, a multiple of 64 */
+  int32_t vocab;                   /* V >= 2 */
+  int32_t n_heads;                 /* K, depth <= K <= 8 */
+  int32_t depth;                   /* D, 0 <= D <= 8 */
+  int32_t topk[MEDUSA_MAX_DEPTH];  /* k_1..k_D, 1 <= k_d <= 16, k_d <= V */
+  int32_t n_q_heads;               /* Hq */
+  int32_t n_kv_heads;              /* Hkv, Hq % Hkv == 0 */
+  int32_t head_dim;                /* Dh in {64, 128}; Hq*Dh == H */
+  int32_t kv_len;                  /* L >= 0 valid cache rows per sequence */
+  int32_t kv_capacity;             /* Lc >= L: cache rows allocated per sequence */
+  int32_t dtype;                   /* medusa_dtype_t of weights/activations */
+  int32_t accept_mode;             /* medusa_accept_t */
+  float temperature;               /* typical: softmax temperature (> 0) */
+  float eps;                       /* typical: threshold cap */
+  float delta;                     /* typical: threshold scale, thr = min(eps, delta*exp(-H)) */
+} medusa_config_t;
+
+/* Candidate tree, device arrays allocated by the caller (sizes from
+ * medusa_tree_size).  Nodes are numbered breadth first: node 0 is the root;
+ * depth-d nodes follow depth-(d-1) nodes, ordered by parent then by rank in
+ * the head-d list. */
+typedef struct {
+  int32_t* token;   /* [B][T] candidate token; token[b][0] = root_token[b] */
+  int32_t* parent;  /* [T] parent node, -1 for the root */
+  int32_t* depth;   /* [T] */
+  int32_t* rank;    /* [T] rank of the node's token in its head's list (root 0) */
+  uint32_t* mask;   /* [T][W] bit j of word j/32 set iff node j is node i or an ancestor */
+  int32_t* paths;   /* [NL][D+1] node ids from the root to each leaf */
+  int32_t* pos;     /* [T] position id kv_len + depth */
+} medusa_tree_t;
+
+/* All tensors of one fused step (device pointers). */
+typedef struct {
+  /* inputs */
+  const void* h;           /* [B][H] final hidden state */
+  const void* W1;          /* [K][H][H] head layer weight (out, in) */
+  const void* b1;          /* [K][H] head layer bias */
+  const void* W2;          /* [K][V][H] head vocabulary projection */
+  const void* lm_head;     /* [V][H] base model output layer */
+  const int32_t* root_token; /* [B] base model's token for the next position */
+  const void* q;           /* [B][T][Hq][Dh] tree queries */
+  const void* k_tree;      /* [B][T][Hkv][Dh] tree keys */
+  const void* v_tree;      /* [B][T][Hkv][Dh] tree values */
+  const void* k_cache;     /* [B][Lc][Hkv][Dh] cache keys (rows < L are read) */
+  const void* v_cache;     /* [B][Lc][Hkv][Dh] cache values */
+  /* outputs */
+  int32_t* topk_idx;       /* [B][K][kmax] see medusa_heads_topk */
+  float* topk_val;         /* [B][K][kmax] */
+  medusa_tree_t tree;      /* see medusa_tree_build */
+  void* attn_out;          /* [B][T][H] see medusa_tree_attn */
+  int32_t* node_argmax;    /* [B][T] see medusa_verify_accept */
+  float* node_maxlogit;    /* [B][T] */
+  float* node_lse;         /* [B][T] typical only (may be NULL for greedy) */
+  float* node_entropy;     /* [B][T] typical only (may be NULL for greedy) */
+  int32_t* accept_len;     /* [B] */
+  int32_t* acc_tokens;     /* [B][D] */
+  int32_t* acc_nodes;      /* [B][D+1] */
+  int32_t* bonus;          /* [B] */
+} medusa_step_io_t;
+
+/* Bytes of device workspace the calls below need for this config (0 on an
+ * invalid config).  Host-only. */
+size_t medusa_workspace_bytes(const medusa_config_t* cfg);
+
+/* Tree sizes for this config: T nodes, NL leaves, W mask words per node.
+ * Host-only; any output pointer may be NULL.  Returns a medusa_status_t. */
+int medusa_tree_size(const medusa_config_t* cfg, int32_t* n_nodes, int32_t* n_leaves, int32_t* mask_words);
+
+/* Heads and per-head top-k ("Medusa Heads", "Come le teste prevedono i token
+ * successivi": each head is a residual SiLU feed-forward layer followed by a
+ * vocabulary projection; "Attenzione sull'albero e accettazione": the best
+ * tokens of each head form the tree).
+ *   z_k = h + SiLU(W1_k h + b1_k) (fp32, in the workspace), logits_k = W2_k z_k.
+ *   topk_idx[b][k][r], topk_val[b][k][r]: rank r of head k, descending logit,
+ *   ties to the lower token id; kmax = max_d k_d; head k (0-based) keeps
+ *   k_{k+1} entries when k < D, else 1; unused entries are -1 / -inf.
+ * h [B][H], W1 [K][H][H], b1 [K][H], W2 [K][V][H]. */
+int medusa_heads_topk(const medusa_config_t* cfg, const void* h, const void* W1, const void* b1,
+                      const void* W2, int32_t* topk_idx, float* topk_val, void* workspace, void* stream);
+
+/* Cartesian candidate tree ("Attenzione sull'albero e accettazione": the
+ * product of the heads' lists, shared prefixes, ancestor-only mask).  Writes
+ * every array of *tree (the struct itself is host memory).  token[b][i] =
+ * topk_idx[b][depth_i - 1][rank_i]. */
+int medusa_tree_build(const medusa_config_t* cfg, const int32_t* topk_idx, const int32_t* root_token,
+                      const medusa_tree_t* tree, void* stream);
+
+/* Tree attention in one pass ("Attenzione sull'albero e accettazione"; "Plongee
+ * profonde"): for each b, q head h (kv head h / (Hq/Hkv)) and node i,
+ *   o = sum_j softmax_j(q.k_j / sqrt(Dh)) v_j
+ * over the L cache rows and the tree nodes j with mask[i] bit j.
+ * attn_out [B][T][H] holds o of q head h at columns h*Dh .. h*Dh+Dh-1, in the
+ * config's dtype.  Only tree->mask is read. */
+int medusa_tree_attn(const medusa_config_t* cfg, const void* q, const void* k_tree, const void* v_tree,
+                     const void* k_cache, const void* v_cache, const medusa_tree_t* tree, void* attn_out,
+                     void* workspace, void* stream);
+
+/* Verification and acceptance ("Attenzione sull'albero e accettazione").
+ * Scores s_i = lm_head . attn_out[b][i] (fp32 accumulation) for every node:
+ *   node_argmax (ties to the lower id), node_maxlogit; typical mode also
+ *   node_lse = log sum_v exp(s_v / temperature) and node_entropy = -sum p ln p
+ *   of p = softmax(s / temperature).
+ * Acceptance: an edge parent->c is kept when (greedy) token_c ==
+ * node_argmax[parent], or (typical) p_parent(token_c) > min(eps, delta *
+ * exp(-entropy_parent)).  The longest chain of kept edges from the root wins
+ * (ties: lowest node id at the first divergence).  accept_len[b] = its
+ * length n; acc_tokens[b][0..n) its tokens; acc_nodes[b][0..n] its nodes
+ * (root first); bonus[b] = node_argmax at its last node; unused entries -1.
+ * Reads tree->token, tree->parent, tree->paths. */
+int medusa_verify_accept(const medusa_config_t* cfg, const void* attn_out, const void* lm_head,
+                         const medusa_tree_t* tree, int32_t* node_argmax, float* node_maxlogit, float* node_lse,
+                         float* node_entropy, int32_t* accept_len, int32_t* acc_tokens, int32_t* acc_nodes,
+                         int32_t* bonus, void* workspace, void* stream);
+
+/* The whole step: heads_topk, tree_build, tree_attn, verify_accept, in order on
+ * `stream`.  io is host memory holding device pointers. */
+int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream);
+
+/* medusa_step with timing: the same launches, plus cudaEventRecord of
+ * events[2k] just before and events[2k+1] just after kernel k on the stream
+ * that kernel runs on (events: host array of n_events >= 2 *
+ * MEDUSA_STEP_KERNELS cudaEvent_t created by the caller).  Kernel order:
+ * 0 head layer, 1 head projection + top-k, 2 tree build, 3 tree attention,
+ * 4 verification projection, 5 acceptance. */
+#define MEDUSA_STEP_KERNELS 6
+int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
+                         void* const* events, int32_t n_events);
+
+/* Copies the device error word of `workspace` to *code (host pointer; 0 = no
+ * error, else a medusa_status_t) after synchronising `stream`, then clears it. */
+int medusa_get_device_error(void* workspace, int32_t* code, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* medusa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MEDUSA_H */

@@ -1,0 +1,304 @@
+// C ABI of libmedusa.so: argument validation, workspace layout, launch plan
+// and the entry points declared in include/medusa.h.
+#include <stdio.h>
+#include <string.h>
+
+#include "internal.cuh"
+
+namespace medusa {
+
+int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
+int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
+                     cudaStream_t st);
+int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+                       float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
+int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, const medusa_tree_t& t,
+                  const int32_t* node_argmax, const float* node_lse, const float* node_entropy, int32_t* accept_len,
+                  int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus, uint8_t* ws, cudaStream_t st);
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static int pick_nc(int H, int C) {
+  int nc = 8;
+  while (nc > 1 && ((size_t)nc * H * sizeof(float) > 64 * 1024 || nc / 2 >= C)) nc /= 2;
+  return nc;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+int make_plan(const medusa_config_t* c, Plan* p) {
+  if (!c || !p) return MEDUSA_ERR_INVALID_ARG;
+  memset(p, 0, sizeof(*p));
+  if (c->batch < 1 || c->hidden < 64 || c->vocab < 2 || c->n_heads < 1 || c->depth < 0) return MEDUSA_ERR_INVALID_ARG;
+  if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->kv_len < 0 || c->kv_capacity < c->kv_len)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (c->dtype != MEDUSA_F32 && c->dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
+  if (c->accept_mode != MEDUSA_ACCEPT_GREEDY && c->accept_mode != MEDUSA_ACCEPT_TYPICAL) return MEDUSA_ERR_INVALID_ARG;
+  if (c->n_heads > MEDUSA_MAX_HEADS || c->depth > MEDUSA_MAX_DEPTH || c->depth > c->n_heads)
+    return MEDUSA_ERR_UNSUPPORTED;
+  if (c->hidden % 64 != 0) return MEDUSA_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return MEDUSA_ERR_UNSUPPORTED;
+  if ((long long)c->n_q_heads * c->head_dim != c->hidden || c->n_q_heads % c->n_kv_heads != 0)
+    return MEDUSA_ERR_INVALID_ARG;
+  if ((long long)c->n_heads * c->vocab > (1LL << 30) || (long long)c->n_heads * c->hidden > (1LL << 30))
+    return MEDUSA_ERR_UNSUPPORTED;
+  if (c->accept_mode == MEDUSA_ACCEPT_TYPICAL && !(c->temperature > 0.f && c->eps > 0.f && c->delta >= 0.f))
+    return MEDUSA_ERR_INVALID_ARG;
+  p->B = c->batch;
+  p->H = c->hidden;
+  p->V = c->vocab;
+  p->K = c->n_heads;
+  p->D = c->depth;
+  p->Hq = c->n_q_heads;
+  p->Hkv = c->n_kv_heads;
+  p->G = c->n_q_heads / c->n_kv_heads;
+  p->Dh = c->head_dim;
+  p->L = c->kv_len;
+  p->Lc = c->kv_capacity;
+  p->bf16 = c->dtype == MEDUSA_BF16;
+  p->typical = c->accept_mode == MEDUSA_ACCEPT_TYPICAL;
+  p->temperature = c->temperature;
+  p->eps = c->eps;
+  p->delta = c->delta;
+  // tree sizes
+  TreeDims& td = p->tree;
+  td.D = p->D;
+  td.off[0] = 0;
+  long long level = 1, total = 1;
+  p->kmax = 1;
+  for (int d = 1; d <= p->D; ++d) {
+    const int k = c->topk[d - 1];
+    if (k < 1 || k > MEDUSA_MAX_TOPK || k > p->V) return MEDUSA_ERR_UNSUPPORTED;
+    td.k[d] = k;
+    if (k > p->kmax) p->kmax = k;
+    td.off[d] = (int)total;
+    level *= k;
+    total += level;
+    if (total > MEDUSA_MAX_NODES) return MEDUSA_ERR_UNSUPPORTED;
+  }
+  td.off[p->D + 1] = (int)total;
+  td.T = (int)total;
+  td.n_leaves = (int)level;
+  td.W = (td.T + 31) / 32;
+  p->T = td.T;
+  p->NL = td.n_leaves;
+  p->W = td.W;
+  for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) p->topk_n[k] = k < p->D ? c->topk[k] : 1;
+  if ((long long)p->B * p->T > (1LL << 24)) return MEDUSA_ERR_UNSUPPORTED;
+
+  // workspace (sized for the largest grids the launch plan can pick)
+  size_t o = 256;  // error word + tickets
+  p->off_z = o;
+  o = align_up(o + (size_t)p->B * p->K * p->H * sizeof(float), 256);
+  const size_t n_cand = (size_t)kMaxStreamCtas * kMaxPieces * p->B * p->kmax;
+  p->off_cand_val = o;
+  o = align_up(o + n_cand * sizeof(float), 256);
+  p->off_cand_idx = o;
+  o = align_up(o + n_cand * sizeof(int), 256);
+  p->off_cand_seg = o;
+  o = align_up(o + (size_t)kMaxStreamCtas * kMaxPieces * sizeof(int), 256);
+  const size_t n_vf = (size_t)kMaxStreamCtas * p->B * p->T;
+  p->off_vf_part = o;
+  o = align_up(o + n_vf * 3 * sizeof(float), 256);
+  p->off_vf_idx = o;
+  o = align_up(o + n_vf * sizeof(int), 256);
+  p->total = o;
+  return MEDUSA_OK;
+}
+
+// launch shapes need the device's SM count
+static void finish_plan(Plan* p) {
+  p->sm_count = sm_count();
+  p->fc_nc = pick_nc(p->H, p->B);
+  p->fc_ctiles = (p->B + p->fc_nc - 1) / p->fc_nc;
+  p->pj_nc = pick_nc(p->H, p->B);
+  p->pj_ctiles = (p->B + p->pj_nc - 1) / p->pj_nc;
+  p->vf_nc = pick_nc(p->H, p->B * p->T);
+  p->vf_ctiles = (p->B * p->T + p->vf_nc - 1) / p->vf_nc;
+}
+
+static bool aligned16(const void* x) { return x && ((uintptr_t)x & 15u) == 0; }
+
+static int cuda_status(int e) { return e == 0 ? MEDUSA_OK : MEDUSA_ERR_CUDA; }
+
+static int check_tree(const Plan& p, const medusa_tree_t* t) {
+  if (!t || !t->token || !t->parent || !t->depth || !t->rank || !t->mask || !t->paths || !t->pos)
+    return MEDUSA_ERR_INVALID_ARG;
+  return MEDUSA_OK;
+}
+
+}  // namespace medusa
+
+using namespace medusa;
+
+extern "C" {
+
+size_t medusa_workspace_bytes(const medusa_config_t* cfg) {
+  Plan p;
+  if (make_plan(cfg, &p) != MEDUSA_OK) return 0;
+  return p.total;
+}
+
+int medusa_tree_size(const medusa_config_t* cfg, int32_t* n_nodes, int32_t* n_leaves, int32_t* mask_words) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (n_nodes) *n_nodes = p.T;
+  if (n_leaves) *n_leaves = p.NL;
+  if (mask_words) *mask_words = p.W;
+  return MEDUSA_OK;
+}
+
+int medusa_heads_topk(const medusa_config_t* cfg, const void* h, const void* W1, const void* b1, const void* W2,
+                      int32_t* topk_idx, float* topk_val, void* workspace, void* stream) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!aligned16(h) || !aligned16(W1) || !aligned16(b1) || !aligned16(W2) || !topk_idx || !topk_val ||
+      !aligned16(workspace))
+    return MEDUSA_ERR_INVALID_ARG;
+  finish_plan(&p);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  int e = launch_fc(p, h, W1, b1, ws, st);
+  if (e) return cuda_status(e);
+  return cuda_status(launch_proj_topk(p, W2, topk_idx, topk_val, ws, st));
+}
+
+int medusa_tree_build(const medusa_config_t* cfg, const int32_t* topk_idx, const int32_t* root_token,
+                      const medusa_tree_t* tree, void* stream) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!topk_idx || !root_token) return MEDUSA_ERR_INVALID_ARG;
+  if ((s = check_tree(p, tree)) != MEDUSA_OK) return s;
+  return cuda_status(launch_tree_build(p, topk_idx, root_token, *tree, (cudaStream_t)stream));
+}
+
+int medusa_tree_attn(const medusa_config_t* cfg, const void* q, const void* k_tree, const void* v_tree,
+                     const void* k_cache, const void* v_cache, const medusa_tree_t* tree, void* attn_out,
+                     void* workspace, void* stream) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(attn_out) || !tree || !tree->mask ||
+      !aligned16(workspace))
+    return MEDUSA_ERR_INVALID_ARG;
+  if (p.L > 0 && (!aligned16(k_cache) || !aligned16(v_cache))) return MEDUSA_ERR_INVALID_ARG;
+  finish_plan(&p);
+  return cuda_status(launch_tree_attn(p, q, k_tree, v_tree, k_cache, v_cache, tree->mask, attn_out,
+                                      (uint8_t*)workspace, (cudaStream_t)stream));
+}
+
+int medusa_verify_accept(const medusa_config_t* cfg, const void* attn_out, const void* lm_head,
+                         const medusa_tree_t* tree, int32_t* node_argmax, float* node_maxlogit, float* node_lse,
+                         float* node_entropy, int32_t* accept_len, int32_t* acc_tokens, int32_t* acc_nodes,
+                         int32_t* bonus, void* workspace, void* stream) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!aligned16(attn_out) || !aligned16(lm_head) || !node_argmax || !node_maxlogit || !accept_len ||
+      !acc_tokens || !acc_nodes || !bonus || !aligned16(workspace))
+    return MEDUSA_ERR_INVALID_ARG;
+  if (p.typical && (!node_lse || !node_entropy)) return MEDUSA_ERR_INVALID_ARG;
+  if ((s = check_tree(p, tree)) != MEDUSA_OK) return s;
+  finish_plan(&p);
+  return cuda_status(launch_verify_accept(p, attn_out, lm_head, *tree, node_argmax, node_maxlogit, node_lse,
+                                          node_entropy, accept_len, acc_tokens, acc_nodes, bonus,
+                                          (uint8_t*)workspace, (cudaStream_t)stream));
+}
+
+}  // extern "C"
+
+namespace medusa {
+
+// Validates every argument of the step, then launches its kernels in order,
+// recording events[2k] / events[2k+1] around kernel k when events != NULL.
+static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
+                    void* const* events, int n_events) {
+  if (!io) return MEDUSA_ERR_INVALID_ARG;
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!aligned16(io->h) || !aligned16(io->W1) || !aligned16(io->b1) || !aligned16(io->W2) ||
+      !aligned16(io->lm_head) || !io->root_token || !aligned16(io->q) || !aligned16(io->k_tree) ||
+      !aligned16(io->v_tree) || !io->topk_idx || !io->topk_val || !aligned16(io->attn_out) || !io->node_argmax ||
+      !io->node_maxlogit || !io->accept_len || !io->acc_tokens || !io->acc_nodes || !io->bonus ||
+      !aligned16(workspace))
+    return MEDUSA_ERR_INVALID_ARG;
+  if (p.L > 0 && (!aligned16(io->k_cache) || !aligned16(io->v_cache))) return MEDUSA_ERR_INVALID_ARG;
+  if (p.typical && (!io->node_lse || !io->node_entropy)) return MEDUSA_ERR_INVALID_ARG;
+  if ((s = check_tree(p, &io->tree)) != MEDUSA_OK) return s;
+  if (events && n_events < 2 * MEDUSA_STEP_KERNELS) return MEDUSA_ERR_INVALID_ARG;
+  finish_plan(&p);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  int k = 0, e = 0;
+  auto rec = [&](int i) {
+    if (events && e == 0) e = (int)cudaEventRecord((cudaEvent_t)events[i], st);
+  };
+#define MEDUSA_STAGE(call)  \
+  rec(2 * k);               \
+  if (e == 0) e = (call);   \
+  rec(2 * k + 1);           \
+  ++k;                      \
+  if (e) return cuda_status(e);
+  MEDUSA_STAGE(launch_fc(p, io->h, io->W1, io->b1, ws, st))
+  MEDUSA_STAGE(launch_proj_topk(p, io->W2, io->topk_idx, io->topk_val, ws, st))
+  MEDUSA_STAGE(launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
+  MEDUSA_STAGE(launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->tree.mask,
+                                io->attn_out, ws, st))
+  MEDUSA_STAGE(launch_verify_rows(p, io->attn_out, io->lm_head, io->node_argmax, io->node_maxlogit, io->node_lse,
+                                  io->node_entropy, ws, st))
+  MEDUSA_STAGE(launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse,
+                             io->node_entropy, io->accept_len, io->acc_tokens, io->acc_nodes, io->bonus, ws, st))
+#undef MEDUSA_STAGE
+  return MEDUSA_OK;
+}
+
+}  // namespace medusa
+
+extern "C" {
+
+int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream) {
+  return run_step(cfg, io, workspace, stream, nullptr, 0);
+}
+
+int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
+                         void* const* events, int32_t n_events) {
+  if (!events) return MEDUSA_ERR_INVALID_ARG;
+  return run_step(cfg, io, workspace, stream, events, n_events);
+}
+
+int medusa_get_device_error(void* workspace, int32_t* code, void* stream) {
+  if (!workspace || !code) return MEDUSA_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  *code = v;
+  if (v != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  }
+  return MEDUSA_OK;
+}
+
+const char* medusa_status_string(int status) {
+  switch (status) {
+    case MEDUSA_OK: return "MEDUSA_OK";
+    case MEDUSA_ERR_INVALID_ARG: return "MEDUSA_ERR_INVALID_ARG";
+    case MEDUSA_ERR_UNSUPPORTED: return "MEDUSA_ERR_UNSUPPORTED";
+    case MEDUSA_ERR_CUDA: return "MEDUSA_ERR_CUDA";
+    case MEDUSA_ERR_TIMEOUT: return "MEDUSA_ERR_TIMEOUT";
+    case MEDUSA_ERR_DEVICE: return "MEDUSA_ERR_DEVICE";
+    default: return "MEDUSA_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

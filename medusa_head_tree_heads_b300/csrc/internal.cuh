@@ -1,0 +1,101 @@
+// Internal declarations shared by the translation units of libmedusa.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/medusa.h"
+
+namespace medusa {
+
+constexpr int kThreads = 256;   // threads per CTA of the streaming kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxPieces = 4;   // segments one streaming CTA may touch
+constexpr int kMaxStreamCtas = 1024;  // cap of the persistent streaming grids (workspace sizing)
+
+// ---------------------------------------------------------------- workspace --
+// [0, 256): int32 error word at 0, tickets from word 8 on.
+enum Ticket { TICKET_FC = 8, TICKET_PROJ = 9, TICKET_VERIFY = 10 };
+
+struct TreeDims {
+  int T, n_leaves, W, D;
+  int off[MEDUSA_MAX_DEPTH + 2];  // first node of depth d (off[D+1] = T)
+  int k[MEDUSA_MAX_DEPTH + 1];    // k[d] for d = 1..D
+};
+
+struct Plan {
+  // sizes
+  int B, H, V, K, D, kmax, T, NL, W, Hq, Hkv, G, Dh, L, Lc;
+  bool bf16, typical;
+  float temperature, eps, delta;
+  TreeDims tree;
+  int topk_n[MEDUSA_MAX_HEADS];  // entries kept per head
+  // streaming partitions
+  int sm_count;
+  int fc_nc, fc_ctiles, pj_nc, pj_ctiles, vf_nc, vf_ctiles;  // columns per CTA, column tiles
+  // workspace offsets (bytes)
+  size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, total;
+};
+
+int make_plan(const medusa_config_t* cfg, Plan* p);  // medusa_status_t
+
+// launchers (enqueue only; return cudaError_t as int)
+int launch_heads(const Plan& p, const void* h, const void* W1, const void* b1, const void* W2, int32_t* topk_idx,
+                 float* topk_val, uint8_t* ws, cudaStream_t st);
+int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* root, const medusa_tree_t& t,
+                      cudaStream_t st);
+int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
+                     const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st);
+int launch_verify_accept(const Plan& p, const void* attn_out, const void* lm_head, const medusa_tree_t& t,
+                         int32_t* node_argmax, float* node_maxlogit, float* node_lse, float* node_entropy,
+                         int32_t* accept_len, int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus, uint8_t* ws,
+                         cudaStream_t st);
+
+// ------------------------------------------------------------ device helpers --
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// streaming 16-byte load that bypasses L1 (weights are read exactly once)
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// first error wins
+__device__ __forceinline__ void set_error(uint8_t* ws, int code) {
+  atomicCAS(reinterpret_cast<int*>(ws), 0, code);
+}
+
+// (value desc, index asc) order used by every top-k / argmax
+__device__ __forceinline__ bool better(float v, int i, float w, int j) { return v > w || (v == w && i < j); }
+
+}  // namespace medusa

@@ -121,6 +121,14 @@ _add(Shape("gqa-mini", "bf16", 512, 4099, 4, 2, (4, 3, 2, 2), 257, 4, 2, 128, "t
 _add(Shape("33b-mini", "bf16", 256, 1500, 5, 3, (4, 3, 2, 2, 2), 129, 2, 2, 128, "greedy", ("uniform", 0, 5), 2004))
 _add(Shape("tiny-fp32-gqa", "f32", 256, 777, 3, 2, (3, 2), 70, 4, 2, 64, "typical", ("uniform", 0, 2), 2005,
            kv_capacity=75))
+# edge cases: a chain tree (the mask is causal), a root-only tree, an empty
+# cache, the widest tree under the 512-node limit, and the deepest tree
+_add(Shape("chain-bf16", "bf16", 256, 999, 3, 2, (1, 1, 1), 64, 2, 2, 128, "greedy", ("uniform", 0, 3), 3001))
+_add(Shape("rootonly-f32", "f32", 128, 500, 1, 2, (), 40, 2, 1, 64, "greedy", ("fixed", 0), 3002))
+_add(Shape("nocache-bf16", "bf16", 256, 700, 2, 2, (3, 2), 0, 2, 2, 128, "typical", ("uniform", 0, 2), 3003))
+_add(Shape("wide-bf16", "bf16", 256, 1200, 3, 1, (8, 8, 6), 100, 2, 1, 128, "greedy", ("fixed", 3), 3004))
+_add(Shape("deep-bf16", "bf16", 192, 600, 8, 2, (2, 2, 2, 2, 2, 2, 2, 2), 33, 3, 1, 64, "greedy", ("uniform", 0, 8),
+           3005))
 
 # tensor tags for seed derivation
 _TAG = {"lm_head": 1, "W2": 2, "W1": 3, "b1": 4, "h": 5, "root": 6, "q": 7, "k_tree": 8, "v_tree": 9,
@@ -183,11 +191,11 @@ def make_activations(s: Shape, h_redraws: Optional[Sequence[int]] = None) -> Dic
     q = _cast(_randn((B, T, s.n_q_heads, s.head_dim), seed_for(s.seed, "q")), s)
     kt = _cast(_randn((B, T, s.n_kv_heads, s.head_dim), seed_for(s.seed, "k_tree")), s)
     vt = _cast(_randn((B, T, s.n_kv_heads, s.head_dim), seed_for(s.seed, "v_tree")), s)
-    kc = torch.empty((B, s.cap, s.n_kv_heads, s.head_dim), dtype=s.torch_dtype)
+    kc = torch.empty((B, max(s.cap, 1), s.n_kv_heads, s.head_dim), dtype=s.torch_dtype)
     vc = torch.empty_like(kc)
     for b in range(B):  # per sequence, to bound the fp32 temporary
-        kc[b] = _cast(_randn((s.cap, s.n_kv_heads, s.head_dim), seed_for(s.seed, "k_cache", b)), s)
-        vc[b] = _cast(_randn((s.cap, s.n_kv_heads, s.head_dim), seed_for(s.seed, "v_cache", b)), s)
+        kc[b] = _cast(_randn((max(s.cap, 1), s.n_kv_heads, s.head_dim), seed_for(s.seed, "k_cache", b)), s)
+        vc[b] = _cast(_randn((max(s.cap, 1), s.n_kv_heads, s.head_dim), seed_for(s.seed, "v_cache", b)), s)
     return {"h": h, "root_token": root, "q": q, "k_tree": kt, "v_tree": vt, "k_cache": kc, "v_cache": vc}
 
 

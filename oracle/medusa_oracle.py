@@ -128,7 +128,7 @@ def topk_lists(logits: np.ndarray, topk: Sequence[int]):
     d < depth, else 1; order is descending logit, ties to the lower index.
     Returns idx int32 [B,K,kmax] (pad -1) and val float64 [B,K,kmax] (pad -inf)."""
     B, K, V = logits.shape
-    kmax = max(topk)
+    kmax = max(list(topk) + [1])
     idx = np.full((B, K, kmax), -1, dtype=np.int32)
     val = np.full((B, K, kmax), -np.inf)
     ids = np.arange(V)

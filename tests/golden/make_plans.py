@@ -72,7 +72,7 @@ def build_plan(s: synth.Shape, log=print) -> dict:
     # 1. h redraws until the head top-k boundaries have margins
     redraw = [0] * B
     pending = list(range(B))
-    topk_idx = np.zeros((B, s.n_heads, max(topk)), dtype=np.int32)
+    topk_idx = np.zeros((B, s.n_heads, max(topk + [1])), dtype=np.int32)
     while pending:
         hrows = torch.stack([synth.draw_h_row(s, b, redraw[b]) for b in pending])
         z = O.head_hidden(to_np(hrows), Wn["W1"], Wn["b1"])

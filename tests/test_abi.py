@@ -1,0 +1,101 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/medusa.h declares, sizes its workspace and tree, and rejects bad
+arguments on the host before any launch."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from medusa_head_tree_heads_b300 import build as B
+from medusa_head_tree_heads_b300 import medusa as M
+from medusa_head_tree_heads_b300 import synth
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "medusa.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not B.up_to_date():
+        B.build()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(medusa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_lists_the_binding_exports():
+    assert declared_functions() == sorted(M.EXPORTS)
+
+
+def test_library_exports_every_declared_function():
+    L = ctypes.CDLL(M.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+@pytest.mark.parametrize("name", sorted(synth.SHAPES))
+def test_tree_size_closed_form(name):
+    s = synth.SHAPES[name]
+    cfg = M.make_config(s)
+    T, NL, W = M.tree_size(cfg)
+    assert T == s.n_nodes
+    n = 1
+    for k in s.topk:
+        n *= k
+    assert NL == n
+    assert W == (T + 31) // 32
+    assert M.workspace_bytes(cfg) > 0
+
+
+def test_workspace_is_modest_at_full_size():
+    # the workspace holds partial results only (no weight-sized buffers)
+    for name in ("7b-bf16", "13b-bf16", "gqa128k-bf16", "33b-bf16"):
+        assert M.workspace_bytes(M.make_config(synth.SHAPES[name])) < 256 << 20
+
+
+BAD = [
+    (dict(batch=0), -1), (dict(hidden=100), -2), (dict(head_dim=96), -2), (dict(n_kv_heads=3), -1),
+    (dict(kv_capacity=10), -1), (dict(dtype=7), -1), (dict(accept_mode=5), -1), (dict(n_heads=9), -2),
+    (dict(depth=6), -2), (dict(temperature=0.0, accept_mode=1), -1),
+]
+
+
+@pytest.mark.parametrize("over,code", BAD)
+def test_invalid_configs_are_rejected_on_the_host(over, code):
+    cfg = M.make_config(synth.SHAPES["7b-mini"], **over)
+    assert M.workspace_bytes(cfg) == 0
+    r = M.lib().medusa_tree_size(ctypes.byref(cfg), None, None, None)
+    assert r == code, (over, r)
+
+
+def test_topk_and_node_limits():
+    cfg = M.make_config(synth.SHAPES["7b-mini"])
+    cfg.topk[0] = 17  # above the per-depth limit
+    assert M.lib().medusa_tree_size(ctypes.byref(cfg), None, None, None) == -2
+    cfg = M.make_config(synth.SHAPES["wide-bf16"])
+    cfg.topk[2] = 8  # 8 + 64 + 512 nodes: above 512
+    assert M.lib().medusa_tree_size(ctypes.byref(cfg), None, None, None) == -2
+
+
+def test_null_pointers_are_rejected_before_any_launch():
+    cfg = M.make_config(synth.SHAPES["tiny-fp32"])
+    L = M.lib()
+    assert L.medusa_heads_topk(ctypes.byref(cfg), None, None, None, None, None, None, None, None) == -1
+    assert L.medusa_tree_build(ctypes.byref(cfg), None, None, None, None) == -1
+    assert L.medusa_tree_attn(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None) == -1
+    assert L.medusa_verify_accept(ctypes.byref(cfg), None, None, None, *([None] * 10)) == -1
+    assert L.medusa_step(ctypes.byref(cfg), None, None, None) == -1
+    assert L.medusa_get_device_error(None, None, None) == -1
+    # misaligned (not 16-byte) pointers
+    assert L.medusa_heads_topk(ctypes.byref(cfg), 8, 16, 16, 16, 16, 16, 16, None) == -1
+
+
+def test_status_strings():
+    assert M.status_string(0) == "MEDUSA_OK"
+    assert M.status_string(-4) == "MEDUSA_ERR_TIMEOUT"
+    assert M.status_string(123) == "MEDUSA_ERR_UNKNOWN"

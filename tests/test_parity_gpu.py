@@ -1,0 +1,190 @@
+"""CUDA path vs the CPU oracle, through the C ABI (needs a B300).
+
+Reduced workloads: every output compared -- integers bit-exact, floats
+within the stated tolerance.  Full-size workloads (the launch shapes the
+benchmark times): all head top-k lists, the whole tree and the acceptance
+bit-exact, plus attention outputs and base-model choices at sampled nodes
+(every planted node and seeded random ones) computed by the oracle one by
+one."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from medusa_head_tree_heads_b300 import synth
+from oracle import medusa_oracle as O
+from tests import util as U
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [n for n, s in synth.SHAPES.items() if not s.full_size]
+FULL = [n for n, s in synth.SHAPES.items() if s.full_size]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for the gpu-marked tests")
+    from medusa_head_tree_heads_b300 import medusa as M
+    M.lib()  # fails loudly when the library is missing
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_step_matches_oracle(name):
+    s, inp = U.planned_inputs(name)
+    ref = O.step(U.np_inputs(inp), s)
+    res = U.gpu_step(s, U.to_device(inp))
+    U.compare_step(s, res, ref)
+    for b, sq in enumerate(U.plans()[name]["seqs"]):  # the planted acceptance
+        assert int(res["accept_len"][b]) == sq["depth"]
+        assert int(res["bonus"][b]) == sq["bonus"]
+
+
+@pytest.mark.parametrize("name", ["tiny-fp32", "gqa-mini", "33b-mini", "deep-bf16"])
+def test_stage_calls_equal_fused_step(name):
+    s, inp = U.planned_inputs(name)
+    d = U.to_device(inp)
+    a = U.gpu_step(s, d, fused=True)
+    b = U.gpu_step(s, d, fused=False)
+    for k in a:
+        if k == "tree":
+            for t in a[k]:
+                assert torch.equal(a[k][t], b[k][t]), t
+        else:
+            assert torch.equal(a[k].view(torch.int8) if a[k].dtype == torch.bfloat16 else a[k],
+                               b[k].view(torch.int8) if b[k].dtype == torch.bfloat16 else b[k]), k
+
+
+@pytest.mark.parametrize("name", ["7b-mini", "gqa-mini"])
+def test_repeated_steps_are_identical(name):
+    """The workspace tickets reset themselves: back-to-back steps agree bitwise."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs(name)
+    d = U.to_device(inp)
+    cfg = M.make_config(s)
+    ws = M.alloc_workspace(cfg)
+    outs = []
+    for _ in range(3):
+        out = M.alloc_outputs(cfg)
+        M.medusa_step(cfg, M.step_io(d, out), ws)
+        torch.cuda.synchronize()
+        outs.append(out)
+    for k in ("topk_idx", "node_argmax", "accept_len", "acc_nodes", "bonus", "node_maxlogit"):
+        assert torch.equal(outs[0][k], outs[1][k]) and torch.equal(outs[0][k], outs[2][k]), k
+
+
+@pytest.mark.parametrize("name", ["tiny-fp32", "7b-mini"])
+def test_zero_init_heads_reproduce_lm_head(name):
+    """"Medusa Heads", "Come le teste prevedono i token successivi": with the
+    head layer zeroed and the projection a copy of lm_head every head gives
+    lm_head's prediction; on the GPU every head's top-k (ids and values) is
+    bitwise the same, and equals the oracle's lm_head(h) top-k."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s = synth.SHAPES[name]
+    inp = synth.make_inputs(s, zero_init=True)
+    d = U.to_device(inp)
+    cfg = M.make_config(s)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_outputs(cfg)
+    M.medusa_heads_topk(cfg, d["h"], d["W1"], d["b1"], d["W2"], out["topk_idx"], out["topk_val"], ws)
+    torch.cuda.synchronize()
+    idx, val = out["topk_idx"].cpu(), out["topk_val"].cpu()
+    for k in range(1, s.n_heads):
+        m = min(s.topk[k] if k < s.depth else 1, s.topk[0])  # common prefix of the two lists
+        assert torch.equal(idx[:, k, :m], idx[:, 0, :m])
+        assert torch.equal(val[:, k, :m], val[:, 0, :m])
+    base = O.base_logits(U.to_np(inp["h"]), U.to_np(inp["lm_head"]))
+    ridx, _ = O.topk_lists(base[:, None, :], [s.topk[0]])
+    np.testing.assert_array_equal(idx[:, 0, :s.topk[0]].numpy(), ridx[:, 0, :s.topk[0]])
+
+
+def test_typical_delta_zero_accepts_full_depth():
+    """delta = 0 makes the threshold 0: every candidate is kept (full depth)."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs("gqa-mini")
+    d = U.to_device(inp)
+    cfg = M.make_config(s, delta=0.0)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_outputs(cfg)
+    M.medusa_step(cfg, M.step_io(d, out), ws)
+    torch.cuda.synchronize()
+    assert (out["accept_len"].cpu() == s.depth).all()
+    assert (out["acc_nodes"].cpu()[:, :] == torch.tensor([0, 1, 5, 17, 41], dtype=torch.int32)).all()
+
+
+def test_out_of_range_token_sets_device_error():
+    """A tree token outside the vocabulary is caught by the acceptance
+    kernel's own bounds check: the error word is set, nothing is read."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs("gqa-mini")
+    d = U.to_device(inp)
+    cfg = M.make_config(s)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_outputs(cfg)
+    M.medusa_step(cfg, M.step_io(d, out), ws)
+    torch.cuda.synchronize()
+    assert M.medusa_get_device_error(ws) == 0
+    out["tree"]["token"][0, 3] = s.vocab + 5
+    M.medusa_verify_accept(cfg, out["attn_out"], d["lm_head"], out["tree"], out, ws)
+    torch.cuda.synchronize()
+    assert M.medusa_get_device_error(ws) == -5
+    assert M.medusa_get_device_error(ws) == 0  # read clears it
+
+
+def _sample_nodes(s, plan, b, rng, extra=4):
+    planted = [p[0] for p in plan["seqs"][b]["plant"]]
+    rand = rng.choice(s.n_nodes, size=min(extra, s.n_nodes), replace=False).tolist()
+    return sorted(set(planted) | set(rand))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    s, inp = U.planned_inputs(name)
+    plan = U.plans()[name]
+    res = U.gpu_step(s, U.to_device(inp))
+    n = U.np_inputs(inp)
+    # heads and top-k: every sequence, every head
+    z = O.head_hidden(n["h"], n["W1"], n["b1"])
+    idx, val = O.topk_lists(O.head_logits(z, n["W2"]), list(s.topk))
+    np.testing.assert_array_equal(res["topk_idx"].numpy(), idx)
+    live = idx >= 0
+    U.assert_close(res["topk_val"].numpy()[live], val[live], s.dtype, "topk_val")
+    # the tree: everything
+    tree = O.Tree(s.topk)
+    np.testing.assert_array_equal(res["tree"]["token"].numpy(), tree.tokens(idx, n["root_token"]))
+    np.testing.assert_array_equal(res["tree"]["parent"].numpy(), tree.parent)
+    np.testing.assert_array_equal(res["tree"]["mask"].numpy().view(np.uint32), U.pack_mask(tree.mask))
+    np.testing.assert_array_equal(res["tree"]["paths"].numpy(), tree.paths)
+    # acceptance: the planted result, bit-exact
+    for b, sq in enumerate(plan["seqs"]):
+        assert int(res["accept_len"][b]) == sq["depth"], b
+        assert res["acc_tokens"][b, :sq["depth"]].tolist() == sq["tokens"], b
+        assert res["acc_nodes"][b, :sq["depth"] + 1].tolist() == sq["nodes"], b
+        assert int(res["bonus"][b]) == sq["bonus"], b
+    # sampled nodes: attention output and the base model's choice
+    rng = np.random.default_rng(s.seed)
+    bs = sorted({0, s.batch - 1} | set(rng.choice(s.batch, size=min(2, s.batch), replace=False).tolist()))
+    typical = s.accept == "typical"
+    for b in bs:
+        nodes = _sample_nodes(s, plan, b, rng)
+        o = O.tree_attention(n["q"], n["k_tree"], n["v_tree"], n["k_cache"], n["v_cache"], s.kv_len, tree.mask,
+                             nodes=nodes, batches=[b])
+        o_st = O.round_to_storage(o[b, nodes], s.dtype)
+        got = res["attn_out"][b, nodes].float().numpy()
+        U.assert_close(got, o_st, s.dtype, f"attn_out b={b}")
+        st = O.verify_stats(o_st, n["lm_head"], s.temperature if typical else None)
+        U.assert_close(res["node_maxlogit"][b, nodes].numpy(), st["maxlogit"], s.dtype, "maxlogit")
+        planted = {p[0] for p in plan["seqs"][b]["plant"]}
+        lm = n["lm_head"]
+        for j, i in enumerate(nodes):
+            g = int(res["node_argmax"][b, i])
+            r = int(st["argmax"][j])
+            if i in planted or g == r:
+                assert g == r, (b, i)
+            else:  # an unplanted node: the GPU's choice must tie the best within rounding
+                lg = float(o_st[j] @ O.decode(lm[g]))
+                assert st["maxlogit"][j] - lg <= 2e-3 * abs(st["maxlogit"][j]), (b, i, g, r)
+        if typical:
+            U.assert_close(res["node_lse"][b, nodes].numpy(), st["lse"], s.dtype, "lse")
+            U.assert_close(res["node_entropy"][b, nodes].numpy(), st["entropy"], s.dtype, "entropy")
