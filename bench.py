@@ -216,6 +216,14 @@ def run_medusa(args, world, rank, local):
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
+    if not args.no_graph:  # one CUDA graph per step: no host launch gaps between the kernels
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            M.medusa_step(cfg, io, ws)
+        step = graph.replay
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
     assert M.medusa_get_device_error(ws) == 0
     # sanity: the planted acceptance
     acc = out["accept_len"].cpu().tolist()
@@ -243,8 +251,15 @@ def run_medusa(args, world, rank, local):
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        M.medusa_step_profiled(cfg, io, ws, evs[i])
+    if args.no_graph:
+        for i in range(args.steps):
+            M.medusa_step_profiled(cfg, io, ws, evs[i])
+    else:  # the same graph shape as the timed steps, one capture per event set
+        for i in range(args.steps):
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp):
+                M.medusa_step_profiled(cfg, io, ws, evs[i])
+            gp.replay()
     torch.cuda.synchronize()
     per_kernel = {}
     for k, name in enumerate(M.STEP_KERNELS):
@@ -293,7 +308,8 @@ def run_medusa(args, world, rank, local):
                        "heads": s.n_heads, "topk": list(s.topk), "tree_nodes": s.n_nodes, "kv_len": s.kv_len,
                        "q_heads": s.n_q_heads, "kv_heads": s.n_kv_heads, "head_dim": s.head_dim,
                        "accept": s.accept, "parallelism": f"replicas{world}",
-                       "l2": "inputs larger than L2 (no flush)", "accept_len": acc},
+                       "l2": "inputs larger than L2 (no flush)", "accept_len": acc,
+                       "launch": "eager" if args.no_graph else "cuda_graph"},
             "roofline": roofline,
             "e2e": {"value": round(world / e2e_dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
@@ -313,6 +329,7 @@ def main():
     ap.add_argument("--impl", default="medusa", choices=["medusa", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -12,6 +12,8 @@ int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* to
                      cudaStream_t st);
 int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
                        float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
+int launch_verify(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+                  float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, const medusa_tree_t& t,
                   const int32_t* node_argmax, const float* node_lse, const float* node_entropy, int32_t* accept_len,
                   int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus, uint8_t* ws, cudaStream_t st);
@@ -107,6 +109,8 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   o = align_up(o + n_vf * 3 * sizeof(float), 256);
   p->off_vf_idx = o;
   o = align_up(o + n_vf * sizeof(int), 256);
+  p->off_vtc_part = o;
+  if (p->bf16) o = align_up(o + verify_tc_part_bytes(p->V, p->B * p->T), 256);
   p->total = o;
   return MEDUSA_OK;
 }
@@ -253,8 +257,8 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   MEDUSA_STAGE(launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
   MEDUSA_STAGE(launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->tree.mask,
                                 io->attn_out, ws, st))
-  MEDUSA_STAGE(launch_verify_rows(p, io->attn_out, io->lm_head, io->node_argmax, io->node_maxlogit, io->node_lse,
-                                  io->node_entropy, ws, st))
+  MEDUSA_STAGE(launch_verify(p, io->attn_out, io->lm_head, io->node_argmax, io->node_maxlogit, io->node_lse,
+                             io->node_entropy, ws, st))
   MEDUSA_STAGE(launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse,
                              io->node_entropy, io->accept_len, io->acc_tokens, io->acc_nodes, io->bonus, ws, st))
 #undef MEDUSA_STAGE

@@ -138,11 +138,18 @@ int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, cons
   return (int)cudaGetLastError();
 }
 
+// bf16: tensor-core projection; fp32 (no TF32 anywhere): the CUDA-core stream kernel
+int launch_verify(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+                  float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st) {
+  if (p.bf16) return launch_verify_tc(p, attn_out, lm_head, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
+  return launch_verify_rows(p, attn_out, lm_head, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
+}
+
 int launch_verify_accept(const Plan& p, const void* attn_out, const void* lm_head, const medusa_tree_t& t,
                          int32_t* node_argmax, float* node_maxlogit, float* node_lse, float* node_entropy,
                          int32_t* accept_len, int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus, uint8_t* ws,
                          cudaStream_t st) {
-  int e = launch_verify_rows(p, attn_out, lm_head, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
+  int e = launch_verify(p, attn_out, lm_head, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
   if (e) return e;
   return launch_accept(p, attn_out, lm_head, t, node_argmax, node_lse, node_entropy, accept_len, acc_tokens,
                        acc_nodes, bonus, ws, st);

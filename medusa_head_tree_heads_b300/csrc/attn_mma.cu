@@ -1,0 +1,289 @@
+// Tree attention on tensor cores (bf16), flash-style ("Medusa Heads",
+// "Attenzione sull'albero e accettazione": all candidates in one pass, each
+// seeing only its ancestors; "Tetes de decodage Medusa", "Plongee profonde").
+//
+//   o[b][i][h] = sum_j softmax_j(q . k_j / sqrt(Dh)) v_j
+//   over cache rows j < L, then tree nodes j allowed by the node's mask row.
+//
+// A CTA owns 16*NW query rows of one (sequence b, kv head g); query row r is
+// (node r / G, q head g*G + r % G).  Each warp holds 16 rows: their Q
+// fragments stay in registers for the whole pass, S = Q K^T and O += P V are
+// m16n8k16 bf16 MMAs with fp32 accumulation, the online softmax keeps its
+// running max and sum per row in registers, and P is repacked from the S
+// accumulators straight into A fragments.  K/V blocks of 64 keys are
+// double-buffered in shared memory with cp.async (rows padded to break bank
+// conflicts); cache blocks need no mask, tree blocks test one mask bit per
+// (row, key).  The key range is not split, so there is no combine step.
+#include "internal.cuh"
+
+namespace medusa {
+
+constexpr int AM_KB = 64;  // keys per block
+
+struct AmArgs {
+  const __nv_bfloat16 *q, *kt, *vt, *kc, *vc;
+  const uint32_t* mask;
+  __nv_bfloat16* out;
+  int B, T, W, Hq, Hkv, G, L, Lc, H;
+  float qscale;  // log2(e) / sqrt(Dh)
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  const int n = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int DH, int NW>
+__global__ void __launch_bounds__(NW * 32) tree_attn_mma_kernel(AmArgs a) {
+  constexpr int LD = DH + 8;  // padded smem row (elements)
+  constexpr int NT = NW * 32;
+  constexpr int KS = DH / 16;  // k-steps of Q K^T
+  constexpr int ND = DH / 8;   // n-tiles of O
+  extern __shared__ float4 am_smem[];
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(am_smem);  // [2][AM_KB][LD]
+  __nv_bfloat16* Vs = Ks + 2 * AM_KB * LD;                          // [2][AM_KB][LD]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;  // mma group / thread-in-group
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int nrows = a.T * a.G;
+  const int rbase = blockIdx.x * 16 * NW + warp * 16;
+  const size_t kv_row = (size_t)a.Hkv * DH;  // elements between consecutive keys
+
+  // ---- Q fragments (rows gq and gq+8 of this warp), scale folded in later
+  uint32_t qf[KS][4];
+  int node[2];
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int r = rbase + gq + hr * 8;
+    const bool ok = r < nrows;
+    const int i = ok ? r / a.G : 0;
+    node[hr] = ok ? i : -1;
+    const int h = g * a.G + (ok ? r - i * a.G : 0);
+    const __nv_bfloat16* qp = a.q + (((size_t)b * a.T + i) * a.Hq + h) * DH;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const uint32_t lo = ok ? *reinterpret_cast<const uint32_t*>(qp + kk * 16 + 2 * tq) : 0u;
+      const uint32_t hi = ok ? *reinterpret_cast<const uint32_t*>(qp + kk * 16 + 8 + 2 * tq) : 0u;
+      qf[kk][hr] = lo;       // a0 (row gq) / a1 (row gq+8)
+      qf[kk][hr + 2] = hi;   // a2 / a3
+    }
+  }
+
+  float o[ND][4];
+#pragma unroll
+  for (int j = 0; j < ND; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+  const int nb_cache = (a.L + AM_KB - 1) / AM_KB;
+  const int nb_tree = (a.T + AM_KB - 1) / AM_KB;
+  const int nb = nb_cache + nb_tree;
+
+  auto load_block = [&](int blk, int buf) {
+    const bool tree = blk >= nb_cache;
+    const int k0 = tree ? (blk - nb_cache) * AM_KB : blk * AM_KB;
+    const int nk = tree ? min(AM_KB, a.T - k0) : min(AM_KB, a.L - k0);
+    const __nv_bfloat16* kb = tree ? a.kt + ((size_t)b * a.T) * kv_row : a.kc + ((size_t)b * a.Lc) * kv_row;
+    const __nv_bfloat16* vb = tree ? a.vt + ((size_t)b * a.T) * kv_row : a.vc + ((size_t)b * a.Lc) * kv_row;
+    constexpr int CH = DH / 8;  // 16-byte chunks per row
+    for (int c = threadIdx.x; c < AM_KB * CH; c += NT) {
+      const int j = c / CH, x = (c - j * CH) * 8;
+      const bool ok = j < nk;
+      const size_t src = ((size_t)(ok ? k0 + j : k0)) * kv_row + (size_t)g * DH + x;
+      cp_async16(Ks + ((size_t)buf * AM_KB + j) * LD + x, kb + src, ok);
+      cp_async16(Vs + ((size_t)buf * AM_KB + j) * LD + x, vb + src, ok);
+    }
+    cp_async_commit();
+  };
+
+  load_block(0, 0);
+  for (int blk = 0; blk < nb; ++blk) {
+    const int buf = blk & 1;
+    if (blk + 1 < nb) {
+      load_block(blk + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+
+    const bool tree = blk >= nb_cache;
+    const int k0 = tree ? (blk - nb_cache) * AM_KB : blk * AM_KB;
+    const int nk = tree ? min(AM_KB, a.T - k0) : min(AM_KB, a.L - k0);
+    const __nv_bfloat16* Kb = Ks + (size_t)buf * AM_KB * LD;
+    const __nv_bfloat16* Vb = Vs + (size_t)buf * AM_KB * LD;
+
+    // ---- S = Q K^T for 64 keys: 8 n-tiles of 8 keys
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int kk = 0; kk < KS; kk += 2) {
+        uint32_t bf[4];  // b0,b1 of k-step kk and kk+1
+        const int mi = lane >> 3, ri = lane & 7;
+        ldsm_x4(bf, Kb + (size_t)(nt * 8 + ri) * LD + kk * 16 + mi * 8);
+        mma16816(s[nt], qf[kk], bf[0], bf[1]);
+        mma16816(s[nt], qf[kk + 1], bf[2], bf[3]);
+      }
+    }
+    // ---- mask, scale, online softmax (rows gq and gq+8)
+    uint32_t mw[2][2] = {{0u, 0u}, {0u, 0u}};
+    if (tree) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+        if (node[hr] >= 0) {
+          const int w0 = k0 >> 5;
+          mw[hr][0] = a.mask[(size_t)node[hr] * a.W + w0];
+          mw[hr][1] = (w0 + 1 < a.W) ? a.mask[(size_t)node[hr] * a.W + w0 + 1] : 0u;
+        }
+    }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int hr = e >> 1;
+        const int kl = nt * 8 + 2 * tq + (e & 1);  // key within the block
+        bool ok = kl < nk;
+        if (tree) ok = ok && ((mw[hr][kl >> 5] >> (kl & 31)) & 1u);
+        const float v = ok ? s[nt][e] * a.qscale : -INFINITY;
+        s[nt][e] = v;
+        mx[hr] = fmaxf(mx[hr], v);
+      }
+    float corr[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+      const float mn = fmaxf(mrow[hr], mx[hr]);
+      // mn == -inf: nothing visible yet for this row; keep everything at zero
+      corr[hr] = (mn == -INFINITY) ? 1.f : exp2f(mrow[hr] - mn);
+      mrow[hr] = mn;
+    }
+    float ls[2] = {0.f, 0.f};
+    uint32_t pf[4][4];  // A fragments of P for the 4 k-steps of P V
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      float p[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int hr = e >> 1;
+        p[e] = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - mrow[hr]);
+        ls[hr] += p[e];
+      }
+      const int kk2 = nt >> 1, half = nt & 1;
+      pf[kk2][half * 2 + 0] = pack_bf16(p[0], p[1]);  // row gq
+      pf[kk2][half * 2 + 1] = pack_bf16(p[2], p[3]);  // row gq+8
+    }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      ls[hr] += __shfl_xor_sync(0xffffffffu, ls[hr], 1);
+      ls[hr] += __shfl_xor_sync(0xffffffffu, ls[hr], 2);
+      lrow[hr] = lrow[hr] * corr[hr] + ls[hr];
+    }
+#pragma unroll
+    for (int j = 0; j < ND; ++j) {
+      o[j][0] *= corr[0];
+      o[j][1] *= corr[0];
+      o[j][2] *= corr[1];
+      o[j][3] *= corr[1];
+    }
+    // ---- O += P V: 4 k-steps of 16 keys, ND n-tiles of 8 dims
+#pragma unroll
+    for (int kk2 = 0; kk2 < 4; ++kk2) {
+      // A fragment order: a0 (row gq, keys 0-7 of the step), a1 (row gq+8, 0-7), a2 (row gq, 8-15), a3 (gq+8, 8-15)
+      const uint32_t af[4] = {pf[kk2][0], pf[kk2][1], pf[kk2][2], pf[kk2][3]};
+#pragma unroll
+      for (int j = 0; j < ND; j += 2) {
+        uint32_t bf[4];  // (keys 0-7, dims j), (keys 8-15, dims j), (keys 0-7, dims j+1), (keys 8-15, dims j+1)
+        const int mi = lane >> 3, ri = lane & 7;
+        const int key = kk2 * 16 + (mi & 1) * 8 + ri;
+        const int dim = (j + (mi >> 1)) * 8;
+        ldsm_x4_t(bf, Vb + (size_t)key * LD + dim);
+        mma16816(o[j], af, bf[0], bf[1]);
+        mma16816(o[j + 1], af, bf[2], bf[3]);
+      }
+    }
+    __syncthreads();  // this buffer is refilled two blocks later
+  }
+
+  // ---- normalise and store (bf16)
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int r = rbase + gq + hr * 8;
+    if (r >= nrows) continue;
+    const int i = r / a.G, h = g * a.G + (r - (r / a.G) * a.G);
+    const float inv = 1.f / lrow[hr];
+    __nv_bfloat16* op = a.out + ((size_t)b * a.T + i) * a.H + (size_t)h * DH;
+#pragma unroll
+    for (int j = 0; j < ND; ++j)
+      *reinterpret_cast<uint32_t*>(op + j * 8 + 2 * tq) = pack_bf16(o[j][hr * 2] * inv, o[j][hr * 2 + 1] * inv);
+  }
+}
+
+int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
+                         const uint32_t* mask, void* out, cudaStream_t st) {
+  AmArgs a;
+  a.q = (const __nv_bfloat16*)q;
+  a.kt = (const __nv_bfloat16*)kt;
+  a.vt = (const __nv_bfloat16*)vt;
+  a.kc = (const __nv_bfloat16*)(kc ? kc : kt);
+  a.vc = (const __nv_bfloat16*)(vc ? vc : vt);
+  a.mask = mask;
+  a.out = (__nv_bfloat16*)out;
+  a.B = p.B;
+  a.T = p.T;
+  a.W = p.W;
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.G = p.G;
+  a.L = p.L;
+  a.Lc = p.Lc;
+  a.H = p.H;
+  a.qscale = 1.4426950408889634f / sqrtf((float)p.Dh);
+  const int rows = p.T * p.G;
+  // four warps per CTA when that still gives two CTAs per SM, else two
+  const int ctas4 = (rows + 63) / 64 * p.Hkv * p.B;
+  const int nw = ctas4 >= 2 * p.sm_count ? 4 : 2;
+  dim3 grid((rows + 16 * nw - 1) / (16 * nw), p.Hkv, p.B);
+  const size_t smem = (size_t)4 * AM_KB * (p.Dh + 8) * sizeof(__nv_bfloat16);
+  void (*k)(AmArgs);
+  if (p.Dh == 128) k = nw == 4 ? tree_attn_mma_kernel<128, 4> : tree_attn_mma_kernel<128, 2>;
+  else k = nw == 4 ? tree_attn_mma_kernel<64, 4> : tree_attn_mma_kernel<64, 2>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  k<<<grid, nw * 32, smem, st>>>(a);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace medusa

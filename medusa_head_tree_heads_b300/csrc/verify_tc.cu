@@ -1,0 +1,409 @@
+// Verification projection on the 5th-generation tensor cores ("Medusa Heads",
+// "Attenzione sull'albero e accettazione": the base model scores every tree
+// node; greedy acceptance needs its top choice, typical acceptance the
+// entropy of its distribution).
+//
+//   logits[n][v] = o[n] . lm_head[v]   for every node n < N = B*T, token v < V,
+//   reduced over v on the fly: argmax (ties to the lower id), max, and with a
+//   temperature the softmax log-partition and entropy.  Logits never reach
+//   global memory.
+//
+// Mapping (swap-AB): MMA M = 128 vocabulary rows of lm_head (A, K-major), MMA
+// N = BN <= 256 nodes (B = attention output rows, K-major), K = H in blocks
+// of 64 (one 128-byte swizzled TMA box per operand and stage).  Accumulators
+// live in TMEM (two 256-column buffers, so the epilogue of one tile overlaps
+// the MMAs of the next).  Warp roles in a persistent CTA (one per SM):
+//   warp 0      TMA producer (one thread), S-stage smem ring
+//   warp 1      TMEM allocator + MMA issuer (one thread)
+//   warps 2..5  epilogue: tcgen05.ld 16 columns at a time; per column a
+//               butterfly "transpose-reduce" across the 32 rows of the warp
+//               (16 exchange rounds per 16 columns instead of 5 per column),
+//               then the 4 warps combine in shared memory and write one
+//               partial (max, sum e, sum e*t, argmax) per (vocab tile, node).
+// The last CTA to finish (atomic ticket) merges the vocab-tile partials.
+// Every wait is bounded; on a timeout the kernel sets MEDUSA_ERR_TIMEOUT,
+// drains its own copies and MMAs, frees TMEM and returns.
+#include <limits.h>
+
+#include "internal.cuh"
+#include "tc.cuh"
+
+namespace medusa {
+
+constexpr int VT_M = 128;       // vocab rows per tile (MMA M)
+constexpr int VT_BK = 64;       // K elements per stage (128 bytes of bf16)
+constexpr int VT_THREADS = 192; // 6 warps
+constexpr uint32_t VT_TMEM_COLS = 512;
+constexpr uint64_t VT_WAIT_NS = 20ull * 1000 * 1000;  // 20 ms per wait
+
+struct VtcArgs {
+  int V, N, H, BN, n_vt, n_nt, n_tiles, nk, stages;
+  uint32_t idesc;
+  int typical;
+  float inv_temp;
+  float4* part;  // [n_vt][N]: (max, sum e, sum e*t, argmax bits)
+  int* ticket;
+  int32_t* node_argmax;
+  float* node_maxlogit;
+  float* node_lse;
+  float* node_entropy;
+  uint8_t* ws;
+};
+
+struct Soft {
+  float m, z, s;
+  int i;
+};
+
+__device__ __forceinline__ Soft soft_empty() {
+  Soft r;
+  r.m = -INFINITY;
+  r.z = 0.f;
+  r.s = 0.f;
+  r.i = INT_MAX;
+  return r;
+}
+
+// merge of two column states; z == 0 is empty
+__device__ __forceinline__ Soft soft_join(const Soft& a, const Soft& b, bool typical, float it) {
+  if (a.z == 0.f) return b;
+  if (b.z == 0.f) return a;
+  Soft r;
+  const bool af = better(a.m, a.i, b.m, b.i);
+  r.m = af ? a.m : b.m;
+  r.i = af ? a.i : b.i;
+  if (typical) {
+    const float da = (a.m - r.m) * it, db = (b.m - r.m) * it;
+    const float ea = expf(da), eb = expf(db);
+    r.z = a.z * ea + b.z * eb;
+    r.s = ea * (a.s + a.z * da) + eb * (b.s + b.z * db);
+  } else {
+    r.z = a.z + b.z;
+    r.s = 0.f;
+  }
+  return r;
+}
+
+__device__ __forceinline__ Soft shfl_soft(const Soft& a, int o) {
+  Soft r;
+  r.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+  r.z = __shfl_xor_sync(0xffffffffu, a.z, o);
+  r.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+  r.i = __shfl_xor_sync(0xffffffffu, a.i, o);
+  return r;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint8_t* ws) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::globaltimer_ns();
+  while (!tc::mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (tc::globaltimer_ns() - t0 > VT_WAIT_NS) {
+      set_error(ws, MEDUSA_ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(VT_THREADS, 1)
+    verify_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, VtcArgs a) {
+  extern __shared__ uint8_t vt_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(vt_smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.stages;
+  const uint32_t bytesA = VT_M * VT_BK * 2, bytesB = (uint32_t)a.BN * VT_BK * 2;
+  const uint32_t stage_bytes = bytesA + bytesB;
+  Soft* red = reinterpret_cast<Soft*>(smem + (size_t)S * stage_bytes);  // [4][BN]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 4 * a.BN);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
+  volatile int* ep_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool typical = a.typical != 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], 4);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tmA);
+    tc::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, VT_TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x) {
+        const int vt = t / a.n_nt, nt = t - vt * a.n_nt;
+        for (int kb = 0; kb < a.nk; ++kb, ++g) {
+          const int s = g % S;
+          const uint32_t ph = (g / S) & 1u;
+          if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.ws)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + (size_t)s * stage_bytes;
+          tc::mbar_arrive_expect_tx(&full[s], stage_bytes);
+          tc::tma_load_2d(sa, &tmA, &full[s], kb * VT_BK, vt * VT_M);
+          tc::tma_load_2d(sa + bytesA, &tmB, &full[s], kb * VT_BK, nt * a.BN);
+        }
+      }
+      if (!ok) {  // drain the copies this thread issued before leaving
+        const uint32_t first = g > (uint32_t)S ? g - S : 0;
+        for (uint32_t gi = first; gi < g; ++gi) {
+          uint64_t* b = &full[gi % S];
+          const uint64_t t0 = tc::globaltimer_ns();
+          while (!tc::mbar_try_wait(b, (gi / S) & 1u) && tc::globaltimer_ns() - t0 < VT_WAIT_NS) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      uint32_t g = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x, ++tl) {
+        const int acc = tl & 1;
+        const uint32_t aph = (tl >> 1) & 1u;
+        if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort_flag, a.ws)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t d = tmem + acc * 256;
+        for (int kb = 0; kb < a.nk; ++kb, ++g) {
+          const int s = g % S;
+          const uint32_t ph = (g / S) & 1u;
+          if (!wait_or_abort(&full[s], ph, abort_flag, a.ws)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t sa = tc::smem_u32(smem + (size_t)s * stage_bytes);
+          const uint64_t da = tc::sw128_desc(sa), db = tc::sw128_desc(sa + bytesA);
+#pragma unroll
+          for (int j = 0; j < VT_BK / 16; ++j)  // K = 16 per MMA: +32 bytes in the swizzled row
+            tc::mma_bf16(d, da + 2 * j, db + 2 * j, a.idesc, (kb | j) != 0);
+          tc::mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
+        }
+        if (!ok) break;
+        tc::mma_commit(&tfull[acc]);
+      }
+      // every MMA issued by this thread completes before TMEM is freed
+      tc::mma_commit(drain);
+      const uint64_t t0 = tc::globaltimer_ns();
+      while (!tc::mbar_try_wait(drain, 0) && tc::globaltimer_ns() - t0 < VT_WAIT_NS) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may read
+    const int etid = threadIdx.x - 64;
+    uint32_t tl = 0;
+    for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++tl) {
+      const int vt = t / a.n_nt, nt = t - vt * a.n_nt;
+      const int acc = tl & 1;
+      const uint32_t aph = (tl >> 1) & 1u;
+      // one thread waits, the named barrier hands its verdict to all 128
+      if (etid == 0) *ep_ok = wait_or_abort(&tfull[acc], aph, abort_flag, a.ws) ? 1 : 0;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (!*ep_ok) break;
+      tc::fence_after_sync();
+      const int row = vt * VT_M + q * 32 + lane;
+      const bool row_ok = row < a.V;
+      const uint32_t tbase = tmem + acc * 256 + ((uint32_t)(q * 32) << 16);
+      for (int ch = 0; ch < a.BN / 16; ++ch) {
+        float v[16];
+        tc::tmem_ld16(tbase + ch * 16, v);
+        Soft st[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          st[j] = soft_empty();
+          if (row_ok) {
+            st[j].m = v[j];
+            st[j].z = 1.f;
+            st[j].i = row;
+          }
+        }
+        // butterfly transpose-reduce: after it lane l holds column l >> 1
+#pragma unroll
+        for (int step = 0; step < 4; ++step) {
+          const int o = 16 >> step, half = 8 >> step;
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const Soft send = up ? st[i] : st[i + half];
+            const Soft keep = up ? st[i + half] : st[i];
+            st[i] = soft_join(keep, shfl_soft(send, o), typical, a.inv_temp);
+          }
+        }
+        st[0] = soft_join(st[0], shfl_soft(st[0], 1), typical, a.inv_temp);
+        if ((lane & 1) == 0) red[q * a.BN + ch * 16 + (lane >> 1)] = st[0];
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty[acc]);  // this warp is done with the accumulator
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      for (int col = etid; col < a.BN; col += 128) {
+        const int n = nt * a.BN + col;
+        if (n < a.N) {
+          Soft m = red[col];
+          for (int w = 1; w < 4; ++w) m = soft_join(m, red[w * a.BN + col], typical, a.inv_temp);
+          a.part[(size_t)vt * a.N + n] = make_float4(m.m, m.z, m.s, __int_as_float(m.i));
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, VT_TMEM_COLS);
+  }
+  __threadfence();  // this CTA's partials are visible before its ticket
+  __syncthreads();
+  if (threadIdx.x == 0) *s_last = (atomicAdd(a.ticket, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  const int nw = VT_THREADS / 32;
+  for (int n = warp; n < a.N; n += nw) {
+    Soft m = soft_empty();
+    for (int vt = lane; vt < a.n_vt; vt += 32) {
+      const float4 p = a.part[(size_t)vt * a.N + n];
+      Soft o;
+      o.m = p.x;
+      o.z = p.y;
+      o.s = p.z;
+      o.i = __float_as_int(p.w);
+      m = soft_join(m, o, typical, a.inv_temp);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = soft_join(m, shfl_soft(m, o), typical, a.inv_temp);
+    if (lane == 0) {
+      a.node_argmax[n] = m.i;
+      a.node_maxlogit[n] = m.m;
+      if (typical) {
+        const float lz = logf(m.z);
+        a.node_lse[n] = m.m * a.inv_temp + lz;
+        a.node_entropy[n] = lz - m.s / m.z;
+      }
+    }
+  }
+  if (threadIdx.x == 0) *a.ticket = 0;
+}
+
+// ------------------------------------------------------------------- host --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 [rows][cols] row-major, box of (64 columns x box_rows rows), 128-byte swizzle
+int make_tmap_bf16(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return (int)cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)VT_BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
+void verify_tc_shape(int N, int* BN, int* n_nt) {
+  int nt = (N + 255) / 256;
+  int bn = (N + nt - 1) / nt;
+  bn = (bn + 15) / 16 * 16;
+  if (bn < 16) bn = 16;
+  *BN = bn;
+  *n_nt = nt;
+}
+
+size_t verify_tc_part_bytes(int V, int N) { return (size_t)((V + VT_M - 1) / VT_M) * N * sizeof(float4); }
+
+int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+                     float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st) {
+  VtcArgs a;
+  a.V = p.V;
+  a.N = p.B * p.T;
+  a.H = p.H;
+  verify_tc_shape(a.N, &a.BN, &a.n_nt);
+  a.n_vt = (p.V + VT_M - 1) / VT_M;
+  a.n_tiles = a.n_vt * a.n_nt;
+  a.nk = p.H / VT_BK;
+  a.idesc = tc::idesc_bf16_f32(VT_M, a.BN);
+  a.typical = p.typical ? 1 : 0;
+  a.inv_temp = p.typical ? 1.f / p.temperature : 1.f;
+  a.part = reinterpret_cast<float4*>(ws + p.off_vtc_part);
+  a.ticket = reinterpret_cast<int*>(ws) + TICKET_VERIFY;
+  a.node_argmax = node_argmax;
+  a.node_maxlogit = node_maxlogit;
+  a.node_lse = node_lse;
+  a.node_entropy = node_entropy;
+  a.ws = ws;
+  const size_t stage = (size_t)(VT_M + a.BN) * VT_BK * 2;
+  const size_t fixed = 1024 + (size_t)4 * a.BN * sizeof(Soft) + 256;
+  const size_t budget = 227 * 1024;
+  int S = (int)((budget - fixed) / stage);
+  if (S > 8) S = 8;
+  if (S < 2) return (int)cudaErrorInvalidConfiguration;
+  a.stages = S;
+  const size_t smem = fixed + (size_t)S * stage;
+  CUtensorMap tA, tB;
+  int e = make_tmap_bf16(&tA, lm_head, p.V, p.H, VT_M);
+  if (e) return e;
+  e = make_tmap_bf16(&tB, attn_out, a.N, p.H, a.BN);
+  if (e) return e;
+  cudaError_t ce = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (ce != cudaSuccess) return (int)ce;
+  const int grid = a.n_tiles < p.sm_count ? a.n_tiles : p.sm_count;
+  verify_tc_kernel<<<grid, VT_THREADS, smem, st>>>(tA, tB, a);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace medusa

@@ -121,6 +121,10 @@ _add(Shape("gqa-mini", "bf16", 512, 4099, 4, 2, (4, 3, 2, 2), 257, 4, 2, 128, "t
 _add(Shape("33b-mini", "bf16", 256, 1500, 5, 3, (4, 3, 2, 2, 2), 129, 2, 2, 128, "greedy", ("uniform", 0, 5), 2004))
 _add(Shape("tiny-fp32-gqa", "f32", 256, 777, 3, 2, (3, 2), 70, 4, 2, 64, "typical", ("uniform", 0, 2), 2005,
            kv_capacity=75))
+# profiling case: the 7B shapes with a quarter-sized vocabulary (still far
+# larger than L2) so that counter replays stay small
+_add(Shape("7b-prof", "bf16", 4096, 8192, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3), 4001,
+           full_size=True))
 # edge cases: a chain tree (the mask is causal), a root-only tree, an empty
 # cache, the widest tree under the 512-node limit, and the deepest tree
 _add(Shape("chain-bf16", "bf16", 256, 999, 3, 2, (1, 1, 1), 64, 2, 2, 128, "greedy", ("uniform", 0, 3), 3001))
