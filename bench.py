@@ -251,15 +251,9 @@ def run_medusa(args, world, rank, local):
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
-    if args.no_graph:
-        for i in range(args.steps):
-            M.medusa_step_profiled(cfg, io, ws, evs[i])
-    else:  # the same graph shape as the timed steps, one capture per event set
-        for i in range(args.steps):
-            gp = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gp):
-                M.medusa_step_profiled(cfg, io, ws, evs[i])
-            gp.replay()
+    # (eager launches: an event recorded during graph capture is only an edge, not a timestamp)
+    for i in range(args.steps):
+        M.medusa_step_profiled(cfg, io, ws, evs[i])
     torch.cuda.synchronize()
     per_kernel = {}
     for k, name in enumerate(M.STEP_KERNELS):

@@ -111,6 +111,8 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   o = align_up(o + n_vf * sizeof(int), 256);
   p->off_vtc_part = o;
   if (p->bf16) o = align_up(o + verify_tc_part_bytes(p->V, p->B * p->T), 256);
+  p->off_attn_part = o;
+  if (p->bf16) o = align_up(o + attn_part_bytes(p->B, p->T, p->G, p->Hkv, p->L, p->Dh), 256);
   p->total = o;
   return MEDUSA_OK;
 }

@@ -137,13 +137,13 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
 }
 
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                         const uint32_t* mask, void* out, cudaStream_t st);
+                         const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st);
 
 // bf16: tensor-core kernel (attn_mma.cu); fp32: this CUDA-core kernel (no TF32)
 int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
                      const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st) {
   (void)ws;
-  if (p.bf16) return launch_tree_attn_mma(p, q, kt, vt, kc, vc, mask, out, st);
+  if (p.bf16) return launch_tree_attn_mma(p, q, kt, vt, kc, vc, mask, out, ws, st);
   AttnArgs a;
   a.q = q;
   a.kt = kt;

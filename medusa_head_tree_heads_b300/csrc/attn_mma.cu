@@ -13,7 +13,11 @@
 // accumulators straight into A fragments.  K/V blocks of 64 keys are
 // double-buffered in shared memory with cp.async (rows padded to break bank
 // conflicts); cache blocks need no mask, tree blocks test one mask bit per
-// (row, key).  The key range is not split, so there is no combine step.
+// (row, key).  When (rows / 32) * Hkv * B is too small to fill the GPU the key
+// range is split (flash-decoding): a few cache chunks plus one tree chunk per
+// (b, g, row block), each writing an unnormalised partial (o, max, sum) that
+// a small combine kernel merges; otherwise one CTA covers all keys and
+// writes the output directly.
 #include "internal.cuh"
 
 namespace medusa {
@@ -25,7 +29,11 @@ struct AmArgs {
   const uint32_t* mask;
   __nv_bfloat16* out;
   int B, T, W, Hq, Hkv, G, L, Lc, H;
-  float qscale;  // log2(e) / sqrt(Dh)
+  int NS;          // key splits per (b, g): 1 = no split, else NS-1 cache chunks + the tree
+  int chunk_blks;  // cache key blocks per cache chunk
+  float* part_o;   // [B][Hq][T][NS][Dh] unnormalised partial outputs (split mode)
+  float2* part_ml; // [B][Hq][T][NS] (running max in log2 units, sum)
+  float qscale;    // log2(e) / sqrt(Dh)
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -73,7 +81,7 @@ __global__ void __launch_bounds__(NW * 32) tree_attn_mma_kernel(AmArgs a) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;  // mma group / thread-in-group
-  const int g = blockIdx.y, b = blockIdx.z;
+  const int g = blockIdx.y / a.NS, sp = blockIdx.y - g * a.NS, b = blockIdx.z;
   const int nrows = a.T * a.G;
   const int rbase = blockIdx.x * 16 * NW + warp * 16;
   const size_t kv_row = (size_t)a.Hkv * DH;  // elements between consecutive keys
@@ -105,7 +113,16 @@ __global__ void __launch_bounds__(NW * 32) tree_attn_mma_kernel(AmArgs a) {
 
   const int nb_cache = (a.L + AM_KB - 1) / AM_KB;
   const int nb_tree = (a.T + AM_KB - 1) / AM_KB;
-  const int nb = nb_cache + nb_tree;
+  // this CTA's key blocks [blk_lo, blk_hi) of (cache blocks, then tree blocks)
+  int blk_lo = 0, blk_hi = nb_cache + nb_tree;
+  if (a.NS > 1) {
+    if (sp < a.NS - 1) {
+      blk_lo = min(nb_cache, sp * a.chunk_blks);
+      blk_hi = min(nb_cache, (sp + 1) * a.chunk_blks);
+    } else {
+      blk_lo = nb_cache;
+    }
+  }
 
   auto load_block = [&](int blk, int buf) {
     const bool tree = blk >= nb_cache;
@@ -124,10 +141,10 @@ __global__ void __launch_bounds__(NW * 32) tree_attn_mma_kernel(AmArgs a) {
     cp_async_commit();
   };
 
-  load_block(0, 0);
-  for (int blk = 0; blk < nb; ++blk) {
-    const int buf = blk & 1;
-    if (blk + 1 < nb) {
+  if (blk_lo < blk_hi) load_block(blk_lo, 0);
+  for (int blk = blk_lo; blk < blk_hi; ++blk) {
+    const int buf = (blk - blk_lo) & 1;
+    if (blk + 1 < blk_hi) {
       load_block(blk + 1, buf ^ 1);
       cp_async_wait<1>();
     } else {
@@ -237,7 +254,22 @@ __global__ void __launch_bounds__(NW * 32) tree_attn_mma_kernel(AmArgs a) {
     __syncthreads();  // this buffer is refilled two blocks later
   }
 
-  // ---- normalise and store (bf16)
+  // ---- split mode: unnormalised partial; else normalise and store (bf16)
+  if (a.NS > 1) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = rbase + gq + hr * 8;
+      if (r >= nrows) continue;
+      const int i = r / a.G, h = g * a.G + (r - (r / a.G) * a.G);
+      const size_t pr = (((size_t)b * a.Hq + h) * a.T + i) * a.NS + sp;
+      float* po = a.part_o + pr * DH;
+#pragma unroll
+      for (int j = 0; j < ND; ++j)
+        *reinterpret_cast<float2*>(po + j * 8 + 2 * tq) = make_float2(o[j][hr * 2], o[j][hr * 2 + 1]);
+      if (tq == 0) a.part_ml[pr] = make_float2(mrow[hr], lrow[hr]);
+    }
+    return;
+  }
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
     const int r = rbase + gq + hr * 8;
@@ -251,8 +283,61 @@ __global__ void __launch_bounds__(NW * 32) tree_attn_mma_kernel(AmArgs a) {
   }
 }
 
+// Merges the NS partials of every (b, q head, node): one warp per row.
+template <int DH>
+__global__ void __launch_bounds__(256) tree_attn_combine_kernel(AmArgs a) {
+  const int lane = threadIdx.x & 31;
+  const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h, i) flattened
+  if (row >= (size_t)a.B * a.Hq * a.T) return;
+  const int i = (int)(row % a.T);
+  const int h = (int)((row / a.T) % a.Hq);
+  const int b = (int)(row / ((size_t)a.T * a.Hq));
+  float mx = -INFINITY;
+  for (int s = 0; s < a.NS; ++s) mx = fmaxf(mx, a.part_ml[row * a.NS + s].x);
+  float acc[DH / 32], l = 0.f;
+#pragma unroll
+  for (int t = 0; t < DH / 32; ++t) acc[t] = 0.f;
+  for (int s = 0; s < a.NS; ++s) {
+    const float2 ml = a.part_ml[row * a.NS + s];
+    const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - mx);
+    l += w * ml.y;
+    const float* po = a.part_o + (row * a.NS + s) * DH;
+#pragma unroll
+    for (int t = 0; t < DH / 32; ++t) acc[t] += w * po[lane + 32 * t];
+  }
+  const float inv = 1.f / l;
+  __nv_bfloat16* op = a.out + ((size_t)b * a.T + i) * a.H + (size_t)h * DH;
+#pragma unroll
+  for (int t = 0; t < DH / 32; ++t) op[lane + 32 * t] = __float2bfloat16_rn(acc[t] * inv);
+}
+
+// Key splits for a shape (device independent, so the workspace can be sized
+// from the config alone): split when fewer than ~2 waves of 2-warp CTAs exist.
+void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks) {
+  const int row_blocks = (T * G + 31) / 32;
+  const int base = row_blocks * Hkv * B;
+  const int nbc = (L + AM_KB - 1) / AM_KB;
+  *NS = 1;
+  *chunk_blks = nbc;
+  if (base >= 296 || nbc == 0) return;
+  int ncs = (600 + base - 1) / base - 1;
+  if (ncs < 1) ncs = 1;
+  if (ncs > nbc) ncs = nbc;
+  const int cb = (nbc + ncs - 1) / ncs;
+  *chunk_blks = cb;
+  *NS = (nbc + cb - 1) / cb + 1;
+}
+
+size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh) {
+  int NS, cb;
+  attn_split_shape(B, T, G, Hkv, L, &NS, &cb);
+  if (NS == 1) return 0;
+  const size_t rows = (size_t)B * Hkv * G * T * NS;
+  return rows * Dh * sizeof(float) + rows * sizeof(float2) + 256;
+}
+
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                         const uint32_t* mask, void* out, cudaStream_t st) {
+                         const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st) {
   AmArgs a;
   a.q = (const __nv_bfloat16*)q;
   a.kt = (const __nv_bfloat16*)kt;
@@ -271,11 +356,15 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   a.Lc = p.Lc;
   a.H = p.H;
   a.qscale = 1.4426950408889634f / sqrtf((float)p.Dh);
+  attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &a.NS, &a.chunk_blks);
+  const size_t rows_all = (size_t)p.B * p.Hq * p.T * a.NS;
+  a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);
+  a.part_ml = reinterpret_cast<float2*>(ws + p.off_attn_part + rows_all * p.Dh * sizeof(float));
   const int rows = p.T * p.G;
   // four warps per CTA when that still gives two CTAs per SM, else two
-  const int ctas4 = (rows + 63) / 64 * p.Hkv * p.B;
+  const int ctas4 = (rows + 63) / 64 * p.Hkv * p.B * a.NS;
   const int nw = ctas4 >= 2 * p.sm_count ? 4 : 2;
-  dim3 grid((rows + 16 * nw - 1) / (16 * nw), p.Hkv, p.B);
+  dim3 grid((rows + 16 * nw - 1) / (16 * nw), p.Hkv * a.NS, p.B);
   const size_t smem = (size_t)4 * AM_KB * (p.Dh + 8) * sizeof(__nv_bfloat16);
   void (*k)(AmArgs);
   if (p.Dh == 128) k = nw == 4 ? tree_attn_mma_kernel<128, 4> : tree_attn_mma_kernel<128, 2>;
@@ -283,6 +372,12 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   k<<<grid, nw * 32, smem, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.NS == 1) return (int)e;
+  const size_t nrow = (size_t)p.B * p.Hq * p.T;
+  const unsigned cgrid = (unsigned)((nrow + 7) / 8);
+  if (p.Dh == 128) tree_attn_combine_kernel<128><<<cgrid, 256, 0, st>>>(a);
+  else tree_attn_combine_kernel<64><<<cgrid, 256, 0, st>>>(a);
   return (int)cudaGetLastError();
 }
 

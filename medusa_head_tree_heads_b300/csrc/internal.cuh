@@ -35,11 +35,12 @@ struct Plan {
   int sm_count;
   int fc_nc, fc_ctiles, pj_nc, pj_ctiles, vf_nc, vf_ctiles;  // columns per CTA, column tiles
   // workspace offsets (bytes)
-  size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, off_vtc_part, total;
+  size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, off_vtc_part, off_attn_part, total;
 };
 
 int make_plan(const medusa_config_t* cfg, Plan* p);  // medusa_status_t
 size_t verify_tc_part_bytes(int V, int N);
+size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh);
 int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
                      float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 

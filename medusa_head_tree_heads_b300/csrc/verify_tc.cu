@@ -8,11 +8,13 @@
 //   temperature the softmax log-partition and entropy.  Logits never reach
 //   global memory.
 //
-// Mapping (swap-AB): MMA M = 128 vocabulary rows of lm_head (A, K-major), MMA
-// N = BN <= 256 nodes (B = attention output rows, K-major), K = H in blocks
-// of 64 (one 128-byte swizzled TMA box per operand and stage).  Accumulators
-// live in TMEM (two 256-column buffers, so the epilogue of one tile overlaps
-// the MMAs of the next).  Warp roles in a persistent CTA (one per SM):
+// Mapping (swap-AB): a tile is 256 vocabulary rows of lm_head, as two MMA
+// M = 128 halves (A, K-major) that share every stage of the node operand (MMA
+// N = BN <= 256 attention-output rows, K-major) -- the node operand is
+// re-read from L2 once per tile, so a taller tile halves that traffic; K = H
+// in blocks of 64 (one 128-byte swizzled TMA box per operand and stage).  The
+// two accumulators fill the 512 TMEM columns.  Warp roles in a persistent CTA
+// (one per SM):
 //   warp 0      TMA producer (one thread), S-stage smem ring
 //   warp 1      TMEM allocator + MMA issuer (one thread)
 //   warps 2..5  epilogue: tcgen05.ld 16 columns at a time; per column a
@@ -30,7 +32,8 @@
 
 namespace medusa {
 
-constexpr int VT_M = 128;       // vocab rows per tile (MMA M)
+constexpr int VT_M = 128;       // vocab rows per MMA (M)
+constexpr int VT_SUB = 2;       // MMA halves per tile: a tile is VT_SUB * VT_M vocab rows
 constexpr int VT_BK = 64;       // K elements per stage (128 bytes of bf16)
 constexpr int VT_THREADS = 192; // 6 warps
 constexpr uint32_t VT_TMEM_COLS = 512;
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
   extern __shared__ uint8_t vt_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(vt_smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
-  const uint32_t bytesA = VT_M * VT_BK * 2, bytesB = (uint32_t)a.BN * VT_BK * 2;
+  const uint32_t bytesA1 = VT_M * VT_BK * 2, bytesA = VT_SUB * bytesA1, bytesB = (uint32_t)a.BN * VT_BK * 2;
   const uint32_t stage_bytes = bytesA + bytesB;
   Soft* red = reinterpret_cast<Soft*>(smem + (size_t)S * stage_bytes);  // [4][BN]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red + 4 * a.BN);
@@ -135,10 +138,8 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], 4);
-    }
+    tc::mbar_init(&tfull[0], 1);
+    tc::mbar_init(&tempty[0], 4);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -170,7 +171,9 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
           }
           uint8_t* sa = smem + (size_t)s * stage_bytes;
           tc::mbar_arrive_expect_tx(&full[s], stage_bytes);
-          tc::tma_load_2d(sa, &tmA, &full[s], kb * VT_BK, vt * VT_M);
+#pragma unroll
+          for (int h = 0; h < VT_SUB; ++h)
+            tc::tma_load_2d(sa + h * bytesA1, &tmA, &full[s], kb * VT_BK, (vt * VT_SUB + h) * VT_M);
           tc::tma_load_2d(sa + bytesA, &tmB, &full[s], kb * VT_BK, nt * a.BN);
         }
       }
@@ -190,14 +193,12 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       uint32_t g = 0, tl = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x, ++tl) {
-        const int acc = tl & 1;
-        const uint32_t aph = (tl >> 1) & 1u;
-        if (!wait_or_abort(&tempty[acc], aph ^ 1u, abort_flag, a.ws)) {
+        const uint32_t aph = tl & 1u;  // one accumulator set (both halves), reused per tile
+        if (!wait_or_abort(&tempty[0], aph ^ 1u, abort_flag, a.ws)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t d = tmem + acc * 256;
         for (int kb = 0; kb < a.nk; ++kb, ++g) {
           const int s = g % S;
           const uint32_t ph = (g / S) & 1u;
@@ -207,14 +208,18 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
           }
           tc::fence_after_sync();
           const uint32_t sa = tc::smem_u32(smem + (size_t)s * stage_bytes);
-          const uint64_t da = tc::sw128_desc(sa), db = tc::sw128_desc(sa + bytesA);
+          const uint64_t db = tc::sw128_desc(sa + bytesA);
 #pragma unroll
-          for (int j = 0; j < VT_BK / 16; ++j)  // K = 16 per MMA: +32 bytes in the swizzled row
-            tc::mma_bf16(d, da + 2 * j, db + 2 * j, a.idesc, (kb | j) != 0);
+          for (int h = 0; h < VT_SUB; ++h) {
+            const uint64_t da = tc::sw128_desc(sa + h * bytesA1);
+#pragma unroll
+            for (int j = 0; j < VT_BK / 16; ++j)  // K = 16 per MMA: +32 bytes in the swizzled row
+              tc::mma_bf16(tmem + h * 256, da + 2 * j, db + 2 * j, a.idesc, (kb | j) != 0);
+          }
           tc::mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
         }
         if (!ok) break;
-        tc::mma_commit(&tfull[acc]);
+        tc::mma_commit(&tfull[0]);
       }
       // every MMA issued by this thread completes before TMEM is freed
       tc::mma_commit(drain);
@@ -229,47 +234,50 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
     uint32_t tl = 0;
     for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++tl) {
       const int vt = t / a.n_nt, nt = t - vt * a.n_nt;
-      const int acc = tl & 1;
-      const uint32_t aph = (tl >> 1) & 1u;
+      const uint32_t aph = tl & 1u;
       // one thread waits, the named barrier hands its verdict to all 128
-      if (etid == 0) *ep_ok = wait_or_abort(&tfull[acc], aph, abort_flag, a.ws) ? 1 : 0;
+      if (etid == 0) *ep_ok = wait_or_abort(&tfull[0], aph, abort_flag, a.ws) ? 1 : 0;
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (!*ep_ok) break;
       tc::fence_after_sync();
-      const int row = vt * VT_M + q * 32 + lane;
-      const bool row_ok = row < a.V;
-      const uint32_t tbase = tmem + acc * 256 + ((uint32_t)(q * 32) << 16);
       for (int ch = 0; ch < a.BN / 16; ++ch) {
-        float v[16];
-        tc::tmem_ld16(tbase + ch * 16, v);
-        Soft st[16];
+        Soft col = soft_empty();  // this lane's column (lane >> 1) of the chunk, over both halves
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          st[j] = soft_empty();
-          if (row_ok) {
-            st[j].m = v[j];
-            st[j].z = 1.f;
-            st[j].i = row;
+        for (int h = 0; h < VT_SUB; ++h) {
+          const int row = (vt * VT_SUB + h) * VT_M + q * 32 + lane;
+          const bool row_ok = row < a.V;
+          float v[16];
+          tc::tmem_ld16(tmem + h * 256 + ((uint32_t)(q * 32) << 16) + ch * 16, v);
+          Soft st[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            st[j] = soft_empty();
+            if (row_ok) {
+              st[j].m = v[j];
+              st[j].z = 1.f;
+              st[j].i = row;
+            }
           }
-        }
-        // butterfly transpose-reduce: after it lane l holds column l >> 1
+          // butterfly transpose-reduce: after it lane l holds column l >> 1
 #pragma unroll
-        for (int step = 0; step < 4; ++step) {
-          const int o = 16 >> step, half = 8 >> step;
-          const bool up = (lane & o) != 0;
+          for (int step = 0; step < 4; ++step) {
+            const int o = 16 >> step, half = 8 >> step;
+            const bool up = (lane & o) != 0;
 #pragma unroll
-          for (int i = 0; i < half; ++i) {
-            const Soft send = up ? st[i] : st[i + half];
-            const Soft keep = up ? st[i + half] : st[i];
-            st[i] = soft_join(keep, shfl_soft(send, o), typical, a.inv_temp);
+            for (int i = 0; i < half; ++i) {
+              const Soft send = up ? st[i] : st[i + half];
+              const Soft keep = up ? st[i + half] : st[i];
+              st[i] = soft_join(keep, shfl_soft(send, o), typical, a.inv_temp);
+            }
           }
+          st[0] = soft_join(st[0], shfl_soft(st[0], 1), typical, a.inv_temp);
+          col = soft_join(col, st[0], typical, a.inv_temp);
         }
-        st[0] = soft_join(st[0], shfl_soft(st[0], 1), typical, a.inv_temp);
-        if ((lane & 1) == 0) red[q * a.BN + ch * 16 + (lane >> 1)] = st[0];
+        if ((lane & 1) == 0) red[q * a.BN + ch * 16 + (lane >> 1)] = col;
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tempty[acc]);  // this warp is done with the accumulator
+      if (lane == 0) tc::mbar_arrive(&tempty[0]);  // this warp is done with the accumulators
       asm volatile("bar.sync 1, 128;" ::: "memory");
       for (int col = etid; col < a.BN; col += 128) {
         const int n = nt * a.BN + col;
@@ -364,7 +372,9 @@ void verify_tc_shape(int N, int* BN, int* n_nt) {
   *n_nt = nt;
 }
 
-size_t verify_tc_part_bytes(int V, int N) { return (size_t)((V + VT_M - 1) / VT_M) * N * sizeof(float4); }
+size_t verify_tc_part_bytes(int V, int N) {
+  return (size_t)((V + VT_SUB * VT_M - 1) / (VT_SUB * VT_M)) * N * sizeof(float4);
+}
 
 int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
                      float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st) {
@@ -373,7 +383,7 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, i
   a.N = p.B * p.T;
   a.H = p.H;
   verify_tc_shape(a.N, &a.BN, &a.n_nt);
-  a.n_vt = (p.V + VT_M - 1) / VT_M;
+  a.n_vt = (p.V + VT_SUB * VT_M - 1) / (VT_SUB * VT_M);
   a.n_tiles = a.n_vt * a.n_nt;
   a.nk = p.H / VT_BK;
   a.idesc = tc::idesc_bf16_f32(VT_M, a.BN);
@@ -386,7 +396,7 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, i
   a.node_lse = node_lse;
   a.node_entropy = node_entropy;
   a.ws = ws;
-  const size_t stage = (size_t)(VT_M + a.BN) * VT_BK * 2;
+  const size_t stage = (size_t)(VT_SUB * VT_M + a.BN) * VT_BK * 2;
   const size_t fixed = 1024 + (size_t)4 * a.BN * sizeof(Soft) + 256;
   const size_t budget = 227 * 1024;
   int S = (int)((budget - fixed) / stage);
