@@ -251,9 +251,19 @@ def run_medusa(args, world, rank, local):
         for e in row:
             e.record(stream)
     torch.cuda.synchronize()
-    # (eager launches: an event recorded during graph capture is only an edge, not a timestamp)
-    for i in range(args.steps):
-        M.medusa_step_profiled(cfg, io, ws, evs[i])
+    if args.no_graph:
+        for i in range(args.steps):
+            M.medusa_step_profiled(cfg, io, ws, evs[i])
+    else:  # one capture per event set, replayed like the timed steps
+        graphs = []
+        for i in range(args.steps):
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp):
+                M.medusa_step_profiled(cfg, io, ws, evs[i])
+            graphs.append(gp)
+        torch.cuda.synchronize()
+        for gp in graphs:
+            gp.replay()
     torch.cuda.synchronize()
     per_kernel = {}
     for k, name in enumerate(M.STEP_KERNELS):

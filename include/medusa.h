@@ -189,12 +189,14 @@ int medusa_verify_accept(const medusa_config_t* cfg, const void* attn_out, const
  * `stream`.  io is host memory holding device pointers. */
 int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream);
 
-/* medusa_step with timing: the same launches, plus cudaEventRecord of
- * events[2k] just before and events[2k+1] just after kernel k on the stream
- * that kernel runs on (events: host array of n_events >= 2 *
- * MEDUSA_STEP_KERNELS cudaEvent_t created by the caller).  Kernel order:
- * 0 head layer, 1 head projection + top-k, 2 tree build, 3 tree attention,
- * 4 verification projection, 5 acceptance. */
+/* medusa_step with timing: the same launches, plus an external event record
+ * (cudaEventRecordExternal, so it also times correctly inside a captured CUDA
+ * graph) of events[2k] just before and events[2k+1] just after stage k
+ * (events: host array of n_events >= 2 * MEDUSA_STEP_KERNELS cudaEvent_t
+ * created by the caller).  Stages, each one or two kernel launches: 0 head
+ * layer, 1 head projection + top-k (stream kernel, candidate merge), 2 tree
+ * build, 3 tree attention (+ split combine), 4 verification projection
+ * (+ partial merge), 5 acceptance. */
 #define MEDUSA_STEP_KERNELS 6
 int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
                          void* const* events, int32_t n_events);

@@ -8,8 +8,23 @@
 namespace medusa {
 
 int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
+bool gemv_tma_supported(const Plan& p);
+int launch_fc_tma(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
+int launch_proj_tma(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
+                    cudaStream_t st);
+
+// head layer / head projection: the TMA-fed small-batch kernel where it
+// applies (bf16, batch <= 4), else the general streaming kernel
+static int launch_head_layer(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws,
+                             cudaStream_t st) {
+  if (gemv_tma_supported(p)) return launch_fc_tma(p, h, W1, b1, ws, st);
+  return launch_fc(p, h, W1, b1, ws, st);
+}
 int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                      cudaStream_t st);
+static int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
+                            cudaStream_t st);
+
 int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
                        float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 int launch_verify(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
@@ -128,6 +143,12 @@ static void finish_plan(Plan* p) {
   p->vf_ctiles = (p->B * p->T + p->vf_nc - 1) / p->vf_nc;
 }
 
+static int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
+                            cudaStream_t st) {
+  if (gemv_tma_supported(p)) return launch_proj_tma(p, W2, topk_idx, topk_val, ws, st);
+  return launch_proj_topk(p, W2, topk_idx, topk_val, ws, st);
+}
+
 static bool aligned16(const void* x) { return x && ((uintptr_t)x & 15u) == 0; }
 
 static int cuda_status(int e) { return e == 0 ? MEDUSA_OK : MEDUSA_ERR_CUDA; }
@@ -171,9 +192,9 @@ int medusa_heads_topk(const medusa_config_t* cfg, const void* h, const void* W1,
   finish_plan(&p);
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = (uint8_t*)workspace;
-  int e = launch_fc(p, h, W1, b1, ws, st);
+  int e = launch_head_layer(p, h, W1, b1, ws, st);
   if (e) return cuda_status(e);
-  return cuda_status(launch_proj_topk(p, W2, topk_idx, topk_val, ws, st));
+  return cuda_status(launch_head_proj(p, W2, topk_idx, topk_val, ws, st));
 }
 
 int medusa_tree_build(const medusa_config_t* cfg, const int32_t* topk_idx, const int32_t* root_token,
@@ -245,8 +266,8 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = (uint8_t*)workspace;
   int k = 0, e = 0;
-  auto rec = [&](int i) {
-    if (events && e == 0) e = (int)cudaEventRecord((cudaEvent_t)events[i], st);
+  auto rec = [&](int i) {  // external records also time correctly inside a captured CUDA graph
+    if (events && e == 0) e = (int)cudaEventRecordWithFlags((cudaEvent_t)events[i], st, cudaEventRecordExternal);
   };
 #define MEDUSA_STAGE(call)  \
   rec(2 * k);               \
@@ -254,8 +275,8 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   rec(2 * k + 1);           \
   ++k;                      \
   if (e) return cuda_status(e);
-  MEDUSA_STAGE(launch_fc(p, io->h, io->W1, io->b1, ws, st))
-  MEDUSA_STAGE(launch_proj_topk(p, io->W2, io->topk_idx, io->topk_val, ws, st))
+  MEDUSA_STAGE(launch_head_layer(p, io->h, io->W1, io->b1, ws, st))
+  MEDUSA_STAGE(launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
   MEDUSA_STAGE(launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
   MEDUSA_STAGE(launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->tree.mask,
                                 io->attn_out, ws, st))

@@ -28,7 +28,7 @@
 namespace medusa {
 
 enum Epi { EPI_FC = 0, EPI_TOPK = 1, EPI_VERIFY = 2 };
-constexpr int KM = MEDUSA_MAX_TOPK;  // compile-time bound of a top-k list
+constexpr int KMAX = MEDUSA_MAX_TOPK;  // compile-time bound of a top-k list
 constexpr int UNROLL = 16;           // 16-byte loads in flight per lane
 constexpr int kRowBuf = 2048;        // EPI_TOPK: rows a CTA may own (row results kept in shared memory)
 
@@ -74,6 +74,7 @@ __device__ __forceinline__ int kept_of(const RowArgs& a, int seg) {
 
 // insert (v, id) into a best-first list of n live entries (n <= KM): one
 // compare-and-swap pass, branch-free so the list stays in registers
+template <int KM>
 __device__ __forceinline__ void list_insert(float (&lv)[KM], int (&li)[KM], int n, float v, int id) {
   float tv = lv[0];
   int ti = li[0];
@@ -96,6 +97,7 @@ __device__ __forceinline__ void list_insert(float (&lv)[KM], int (&li)[KM], int 
   }
 }
 
+template <int KM>
 __device__ __forceinline__ void list_reset(float (&lv)[KM], int (&li)[KM]) {
 #pragma unroll
   for (int i = 0; i < KM; ++i) {
@@ -107,6 +109,7 @@ __device__ __forceinline__ void list_reset(float (&lv)[KM], int (&li)[KM]) {
 // Warp-wide top-n of the union of the lanes' best-first lists: n rounds of
 // "the best list head wins, its owner pops".  Lane 0 writes n_out entries
 // (ranks >= n, or missing ones, get -inf and pad_idx).
+template <int KM>
 __device__ __forceinline__ void warp_select(float (&lv)[KM], int (&li)[KM], int n, int n_out, float* out_val,
                                             int* out_idx, int pad_idx) {
   const int lane = threadIdx.x & 31;
@@ -303,8 +306,8 @@ __global__ void __launch_bounds__(kThreads, 2) stream_rows_kernel(RowArgs a) {
       __syncthreads();
       if (warp < NC && c0 + warp < a.C) {
         const int c = warp;
-        float lv[KM];
-        int li[KM];
+        float lv[KMAX];
+        int li[KMAX];
         list_reset(lv, li);
         for (int e = lane; e < r1 - r0; e += 32) list_insert(lv, li, kn, rowbuf[c * kRowBuf + e], r0 + e - seg * a.S);
         const size_t base = ((size_t)(cta * kMaxPieces + piece) * a.C + (c0 + c)) * a.kmax;
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_rows_kernel(RowArgs a) {
       a.part_idx[pi] = m.mi;
     }
   }
-  if (EPI == EPI_FC) return;
+  if (EPI != EPI_VERIFY) return;  // top-k candidates are merged by topk_merge_kernel
 
   // ---- last CTA merges every CTA's partial result
   __threadfence();
@@ -344,27 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_rows_kernel(RowArgs a) {
   __threadfence();
   const int nctas = gridDim.x;
 
-  if (EPI == EPI_TOPK) {
-    for (int pair = warp; pair < a.nseg * a.C; pair += kWarps) {
-      const int seg = pair / a.C, c = pair - seg * a.C;
-      const int kn = kept_of(a, seg);
-      const int b_lo = (int)(((long long)seg * a.S) / a.rpc);
-      const int b_hi = min(nctas - 1, (int)(((long long)(seg + 1) * a.S - 1) / a.rpc));
-      float lv[KM];
-      int li[KM];
-      list_reset(lv, li);
-      const int n_ent = (b_hi - b_lo + 1) * kMaxPieces * kn;
-      for (int e = lane; e < n_ent; e += 32) {
-        const int i = e % kn, bp = e / kn;
-        const int blk = b_lo + bp / kMaxPieces, p = bp % kMaxPieces;
-        if (a.cand_seg[blk * kMaxPieces + p] != seg) continue;
-        const size_t base = ((size_t)(blk * kMaxPieces + p) * a.C + c) * a.kmax;
-        list_insert(lv, li, kn, a.cand_val[base + i], a.cand_idx[base + i]);
-      }
-      const size_t o = ((size_t)c * a.nseg + seg) * a.kmax;
-      warp_select(lv, li, kn, a.kmax, a.out_val + o, a.out_idx + o, -1);
-    }
-  } else {  // EPI_VERIFY
+  if (EPI == EPI_VERIFY) {
     for (int c = warp; c < a.C; c += kWarps) {
       SoftState m;
       m.m = -INFINITY;
@@ -403,6 +386,32 @@ __global__ void __launch_bounds__(kThreads, 2) stream_rows_kernel(RowArgs a) {
   if (threadIdx.x == 0) *a.ticket = 0;  // ready for the next call
 }
 
+// Final per-head top-k: one warp per (segment, column) folds the candidate
+// lists of the CTAs whose row range touched the segment (loads spread over the
+// lanes), then picks the best kn with warp_select.
+template <int KM>
+__global__ void __launch_bounds__(256) topk_merge_kernel(RowArgs a, int nctas) {
+  const int lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (pair >= a.nseg * a.C) return;
+  const int seg = pair / a.C, c = pair - seg * a.C;
+  const int kn = kept_of(a, seg);
+  const int b_lo = (int)(((long long)seg * a.S) / a.rpc);
+  const int b_hi = min(nctas - 1, (int)(((long long)(seg + 1) * a.S - 1) / a.rpc));
+  float lv[KM];
+  int li[KM];
+  list_reset(lv, li);
+  const int n_slots = (b_hi - b_lo + 1) * kMaxPieces;
+  for (int sl = lane; sl < n_slots; sl += 32) {
+    const int blk = b_lo + sl / kMaxPieces, p = sl % kMaxPieces;
+    if (a.cand_seg[blk * kMaxPieces + p] != seg) continue;
+    const size_t base = ((size_t)(blk * kMaxPieces + p) * a.C + c) * a.kmax;
+    for (int i = 0; i < kn; ++i) list_insert(lv, li, kn, a.cand_val[base + i], a.cand_idx[base + i]);
+  }
+  const size_t o = ((size_t)c * a.nseg + seg) * a.kmax;
+  warp_select(lv, li, kn, a.kmax, a.out_val + o, a.out_idx + o, -1);
+}
+
 // --------------------------------------------------------------- launchers --
 // rows per CTA so that a grid of `want` CTAs covers R rows with no CTA
 // spanning more than kMaxPieces segments of S rows
@@ -436,6 +445,12 @@ static int launch_nc(RowArgs a, int sm_count, int nc, int ctiles, cudaStream_t s
       if (ctas > kMaxStreamCtas) return (int)cudaErrorInvalidConfiguration;                                 \
       k<<<dim3(ctas, ctiles), kThreads, smem, st>>>(a);                                                     \
       e = cudaGetLastError();                                                                               \
+      if (e == cudaSuccess && EPI == EPI_TOPK) {                                                            \
+        const unsigned mg = (unsigned)((a.nseg * a.C + 7) / 8);                                             \
+        if (a.kmax <= 4) topk_merge_kernel<4><<<mg, 256, 0, st>>>(a, ctas);                                 \
+        else topk_merge_kernel<KMAX><<<mg, 256, 0, st>>>(a, ctas);                                          \
+        e = cudaGetLastError();                                                                             \
+      }                                                                                                     \
     }                                                                                                       \
     break;                                                                                                  \
   }
@@ -449,6 +464,29 @@ static int launch_nc(RowArgs a, int sm_count, int nc, int ctiles, cudaStream_t s
   }
 #undef MEDUSA_LAUNCH_NC
   return (int)e;
+}
+
+// Final top-k merge for candidates written by any streaming kernel.
+int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc,
+                      cudaStream_t st) {
+  RowArgs a{};
+  a.R = p.K * p.V;
+  a.S = p.V;
+  a.H = p.H;
+  a.C = p.B;
+  a.rpc = rpc;
+  a.nseg = p.K;
+  a.kmax = p.kmax;
+  for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) a.topk_n[k] = p.topk_n[k];
+  a.cand_val = reinterpret_cast<float*>(ws + p.off_cand_val);
+  a.cand_idx = reinterpret_cast<int*>(ws + p.off_cand_idx);
+  a.cand_seg = reinterpret_cast<int*>(ws + p.off_cand_seg);
+  a.out_idx = topk_idx;
+  a.out_val = topk_val;
+  const unsigned mg = (unsigned)((a.nseg * a.C + 7) / 8);
+  if (a.kmax <= 4) topk_merge_kernel<4><<<mg, 256, 0, st>>>(a, ctas);
+  else topk_merge_kernel<KMAX><<<mg, 256, 0, st>>>(a, ctas);
+  return (int)cudaGetLastError();
 }
 
 int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st) {

@@ -22,7 +22,7 @@
 //               (16 exchange rounds per 16 columns instead of 5 per column),
 //               then the 4 warps combine in shared memory and write one
 //               partial (max, sum e, sum e*t, argmax) per (vocab tile, node).
-// The last CTA to finish (atomic ticket) merges the vocab-tile partials.
+// A second small kernel merges the vocab-tile partials, one warp per node.
 // Every wait is bounded; on a timeout the kernel sets MEDUSA_ERR_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <limits.h>
@@ -45,7 +45,6 @@ struct VtcArgs {
   int typical;
   float inv_temp;
   float4* part;  // [n_vt][N]: (max, sum e, sum e*t, argmax bits)
-  int* ticket;
   int32_t* node_argmax;
   float* node_maxlogit;
   float* node_lse;
@@ -96,6 +95,55 @@ __device__ __forceinline__ Soft shfl_soft(const Soft& a, int o) {
   return r;
 }
 
+// Reduces 16 columns over the 32 rows held by the warp's lanes (one row per
+// lane): a butterfly "transpose-reduce" in which every exchange round halves
+// the number of columns a lane carries, so 16 columns cost 16 rounds instead
+// of 5 per column.  Afterwards lane l holds column l >> 1.
+template <bool TYPICAL>
+__device__ __forceinline__ Soft column_reduce(const float (&v)[16], int row, bool row_ok, int lane, float it) {
+  Soft st[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    st[j].m = row_ok ? v[j] : -INFINITY;
+    st[j].z = row_ok ? 1.f : 0.f;
+    st[j].s = 0.f;
+    st[j].i = row_ok ? row : INT_MAX;
+  }
+#pragma unroll
+  for (int step = 0; step < 4; ++step) {
+    const int o = 16 >> step, half = 8 >> step;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const Soft send = up ? st[i] : st[i + half];
+      const Soft keep = up ? st[i + half] : st[i];
+      if (TYPICAL) {
+        st[i] = soft_join(keep, shfl_soft(send, o), true, it);
+      } else {  // greedy: only (max, argmax) travel
+        Soft r;
+        r.m = __shfl_xor_sync(0xffffffffu, send.m, o);
+        r.i = __shfl_xor_sync(0xffffffffu, send.i, o);
+        const bool tk = better(r.m, r.i, keep.m, keep.i);
+        st[i].m = tk ? r.m : keep.m;
+        st[i].i = tk ? r.i : keep.i;
+        st[i].z = 1.f;
+        st[i].s = 0.f;
+      }
+    }
+  }
+  if (TYPICAL) return soft_join(st[0], shfl_soft(st[0], 1), true, it);
+  Soft r;
+  r.m = __shfl_xor_sync(0xffffffffu, st[0].m, 1);
+  r.i = __shfl_xor_sync(0xffffffffu, st[0].i, 1);
+  const bool tk = better(r.m, r.i, st[0].m, st[0].i);
+  Soft o;
+  o.m = tk ? r.m : st[0].m;
+  o.i = tk ? r.i : st[0].i;
+  o.z = (o.i == INT_MAX) ? 0.f : 1.f;
+  o.s = 0.f;
+  return o;
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               uint8_t* ws) {
   if (tc::mbar_try_wait(bar, parity)) return true;
@@ -127,7 +175,6 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
   volatile int* ep_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -240,40 +287,35 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       asm volatile("bar.sync 1, 128;" ::: "memory");
       if (!*ep_ok) break;
       tc::fence_after_sync();
-      for (int ch = 0; ch < a.BN / 16; ++ch) {
-        Soft col = soft_empty();  // this lane's column (lane >> 1) of the chunk, over both halves
+      for (int ch0 = 0; ch0 < a.BN / 16; ch0 += 4) {
+        const int nch = min(4, a.BN / 16 - ch0);
+        Soft col[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) col[c] = soft_empty();
 #pragma unroll
         for (int h = 0; h < VT_SUB; ++h) {
           const int row = (vt * VT_SUB + h) * VT_M + q * 32 + lane;
           const bool row_ok = row < a.V;
-          float v[16];
-          tc::tmem_ld16(tmem + h * 256 + ((uint32_t)(q * 32) << 16) + ch * 16, v);
-          Soft st[16];
+          float v[4][16];
+          const uint32_t tb = tmem + h * 256 + ((uint32_t)(q * 32) << 16) + ch0 * 16;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            st[j] = soft_empty();
-            if (row_ok) {
-              st[j].m = v[j];
-              st[j].z = 1.f;
-              st[j].i = row;
-            }
+          for (int c = 0; c < 4; ++c)
+            if (c < nch) tc::tmem_ld16_nowait(tb + c * 16, v[c]);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc::tmem_regs_ready(v[c]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (c >= nch) break;
+            Soft r;
+            if (typical) r = column_reduce<true>(v[c], row, row_ok, lane, a.inv_temp);
+            else r = column_reduce<false>(v[c], row, row_ok, lane, a.inv_temp);
+            col[c] = soft_join(col[c], r, typical, a.inv_temp);
           }
-          // butterfly transpose-reduce: after it lane l holds column l >> 1
-#pragma unroll
-          for (int step = 0; step < 4; ++step) {
-            const int o = 16 >> step, half = 8 >> step;
-            const bool up = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < half; ++i) {
-              const Soft send = up ? st[i] : st[i + half];
-              const Soft keep = up ? st[i + half] : st[i];
-              st[i] = soft_join(keep, shfl_soft(send, o), typical, a.inv_temp);
-            }
-          }
-          st[0] = soft_join(st[0], shfl_soft(st[0], 1), typical, a.inv_temp);
-          col = soft_join(col, st[0], typical, a.inv_temp);
         }
-        if ((lane & 1) == 0) red[q * a.BN + ch * 16 + (lane >> 1)] = col;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (c < nch && (lane & 1) == 0) red[q * a.BN + (ch0 + c) * 16 + (lane >> 1)] = col[c];
       }
       tc::fence_before_sync();
       __syncwarp();
@@ -298,37 +340,45 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, VT_TMEM_COLS);
   }
-  __threadfence();  // this CTA's partials are visible before its ticket
-  __syncthreads();
-  if (threadIdx.x == 0) *s_last = (atomicAdd(a.ticket, 1) == (int)gridDim.x - 1);
-  __syncthreads();
-  if (!*s_last) return;
-  __threadfence();
-  const int nw = VT_THREADS / 32;
-  for (int n = warp; n < a.N; n += nw) {
-    Soft m = soft_empty();
-    for (int vt = lane; vt < a.n_vt; vt += 32) {
-      const float4 p = a.part[(size_t)vt * a.N + n];
-      Soft o;
-      o.m = p.x;
-      o.z = p.y;
-      o.s = p.z;
-      o.i = __float_as_int(p.w);
-      m = soft_join(m, o, typical, a.inv_temp);
+}
+
+// Merges the per-tile partials of every node: one warp per node, each lane
+// folds a strided subset of the vocab tiles (loads issued back to back), then
+// a butterfly joins the 32 lane states.
+template <bool TYPICAL>
+__global__ void __launch_bounds__(256) verify_merge_kernel(VtcArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (n >= a.N) return;
+  Soft m = soft_empty();
+  for (int vt0 = 0; vt0 < a.n_vt; vt0 += 128) {
+    float4 p[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int vt = vt0 + u * 32 + lane;
+      p[u] = vt < a.n_vt ? a.part[(size_t)vt * a.N + n] : make_float4(-INFINITY, 0.f, 0.f, __int_as_float(INT_MAX));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = soft_join(m, shfl_soft(m, o), typical, a.inv_temp);
-    if (lane == 0) {
-      a.node_argmax[n] = m.i;
-      a.node_maxlogit[n] = m.m;
-      if (typical) {
-        const float lz = logf(m.z);
-        a.node_lse[n] = m.m * a.inv_temp + lz;
-        a.node_entropy[n] = lz - m.s / m.z;
-      }
+    for (int u = 0; u < 4; ++u) {
+      Soft o;
+      o.m = p[u].x;
+      o.z = p[u].y;
+      o.s = p[u].z;
+      o.i = __float_as_int(p[u].w);
+      m = soft_join(m, o, TYPICAL, a.inv_temp);
     }
   }
-  if (threadIdx.x == 0) *a.ticket = 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = soft_join(m, shfl_soft(m, o), TYPICAL, a.inv_temp);
+  if (lane == 0) {
+    a.node_argmax[n] = m.i;
+    a.node_maxlogit[n] = m.m;
+    if (TYPICAL) {
+      const float lz = logf(m.z);
+      a.node_lse[n] = m.m * a.inv_temp + lz;
+      a.node_entropy[n] = lz - m.s / m.z;
+    }
+  }
 }
 
 // ------------------------------------------------------------------- host --
@@ -390,7 +440,6 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, i
   a.typical = p.typical ? 1 : 0;
   a.inv_temp = p.typical ? 1.f / p.temperature : 1.f;
   a.part = reinterpret_cast<float4*>(ws + p.off_vtc_part);
-  a.ticket = reinterpret_cast<int*>(ws) + TICKET_VERIFY;
   a.node_argmax = node_argmax;
   a.node_maxlogit = node_maxlogit;
   a.node_lse = node_lse;
@@ -413,6 +462,11 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, i
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.n_tiles < p.sm_count ? a.n_tiles : p.sm_count;
   verify_tc_kernel<<<grid, VT_THREADS, smem, st>>>(tA, tB, a);
+  ce = cudaGetLastError();
+  if (ce != cudaSuccess) return (int)ce;
+  const unsigned mgrid = (unsigned)((a.N + 7) / 8);
+  if (a.typical) verify_merge_kernel<true><<<mgrid, 256, 0, st>>>(a);
+  else verify_merge_kernel<false><<<mgrid, 256, 0, st>>>(a);
   return (int)cudaGetLastError();
 }
 
