@@ -266,8 +266,13 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = (uint8_t*)workspace;
   int k = 0, e = 0;
-  auto rec = [&](int i) {  // external records also time correctly inside a captured CUDA graph
-    if (events && e == 0) e = (int)cudaEventRecordWithFlags((cudaEvent_t)events[i], st, cudaEventRecordExternal);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (events && cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MEDUSA_ERR_CUDA;
+  auto rec = [&](int i) {  // inside a capture only external records keep their timestamps
+    if (!events || e != 0) return;
+    e = cap == cudaStreamCaptureStatusActive
+            ? (int)cudaEventRecordWithFlags((cudaEvent_t)events[i], st, cudaEventRecordExternal)
+            : (int)cudaEventRecord((cudaEvent_t)events[i], st);
   };
 #define MEDUSA_STAGE(call)  \
   rec(2 * k);               \

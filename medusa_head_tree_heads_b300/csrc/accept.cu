@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(256) accept_kernel(AcceptArgs a) {
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* tok = a.token + (size_t)b * a.T;
+  pdl_trigger();
+  pdl_wait();
 
   if (!a.typical) {
     for (int c = 1 + threadIdx.x; c < a.T; c += blockDim.x)
@@ -133,9 +135,8 @@ int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, cons
   a.acc_nodes = acc_nodes;
   a.bonus = bonus;
   a.ws = ws;
-  if (p.bf16) accept_kernel<__nv_bfloat16><<<p.B, 256, 0, st>>>(a);
-  else accept_kernel<float><<<p.B, 256, 0, st>>>(a);
-  return (int)cudaGetLastError();
+  if (p.bf16) return (int)launch_k(accept_kernel<__nv_bfloat16>, dim3(p.B), dim3(256), 0, st, true, a);
+  return (int)launch_k(accept_kernel<float>, dim3(p.B), dim3(256), 0, st, true, a);
 }
 
 // bf16: tensor-core projection; fp32 (no TF32 anywhere): the CUDA-core stream kernel

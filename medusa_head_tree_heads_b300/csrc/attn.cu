@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
   const int row0 = blockIdx.x * AT_ROWS;
   const int nrows = a.T * a.G;
   const TT* Q = reinterpret_cast<const TT*>(a.q);
+  pdl_trigger();
+  pdl_wait();
 
   // queries of this CTA, pre-scaled so that exp2 gives the softmax weights
   for (int e = threadIdx.x; e < AT_ROWS * DH; e += blockDim.x) {
@@ -169,8 +171,7 @@ int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* v
   else k = p.Dh == 128 ? tree_attn_kernel<float, 128> : tree_attn_kernel<float, 64>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  k<<<grid, 256, smem, st>>>(a);
-  return (int)cudaGetLastError();
+  return (int)launch_k(k, grid, dim3(256), smem, st, true, a);
 }
 
 }  // namespace medusa

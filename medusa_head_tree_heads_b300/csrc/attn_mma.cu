@@ -70,7 +70,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 template <int DH, int NW>
-__global__ void __launch_bounds__(NW * 32) tree_attn_mma_kernel(AmArgs a) {
+__global__ void __launch_bounds__(NW * 32, 12 / NW) tree_attn_mma_kernel(AmArgs a) {
   constexpr int LD = DH + 8;  // padded smem row (elements)
   constexpr int NT = NW * 32;
   constexpr int KS = DH / 16;  // k-steps of Q K^T
@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(NW * 32) tree_attn_mma_kernel(AmArgs a) {
   const int nrows = a.T * a.G;
   const int rbase = blockIdx.x * 16 * NW + warp * 16;
   const size_t kv_row = (size_t)a.Hkv * DH;  // elements between consecutive keys
+  pdl_trigger();
+  pdl_wait();
 
   // ---- Q fragments (rows gq and gq+8 of this warp), scale folded in later
   uint32_t qf[KS][4];
@@ -288,6 +290,8 @@ template <int DH>
 __global__ void __launch_bounds__(256) tree_attn_combine_kernel(AmArgs a) {
   const int lane = threadIdx.x & 31;
   const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h, i) flattened
+  pdl_trigger();
+  pdl_wait();
   if (row >= (size_t)a.B * a.Hq * a.T) return;
   const int i = (int)(row % a.T);
   const int h = (int)((row / a.T) % a.Hq);
@@ -314,13 +318,14 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(AmArgs a) {
 // Key splits for a shape (device independent, so the workspace can be sized
 // from the config alone): split when fewer than ~2 waves of 2-warp CTAs exist.
 void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks) {
-  const int row_blocks = (T * G + 31) / 32;
+  constexpr int kSlots = 444;  // ~3 resident 4-warp CTAs on each of 148 SMs
+  const int row_blocks = (T * G + 63) / 64;
   const int base = row_blocks * Hkv * B;
   const int nbc = (L + AM_KB - 1) / AM_KB;
   *NS = 1;
   *chunk_blks = nbc;
-  if (base >= 296 || nbc == 0) return;
-  int ncs = (600 + base - 1) / base - 1;
+  if (2 * base > kSlots || nbc == 0) return;
+  int ncs = kSlots / base - 1;  // cache chunks; the tree is one more split
   if (ncs < 1) ncs = 1;
   if (ncs > nbc) ncs = nbc;
   const int cb = (nbc + ncs - 1) / ncs;
@@ -361,9 +366,7 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);
   a.part_ml = reinterpret_cast<float2*>(ws + p.off_attn_part + rows_all * p.Dh * sizeof(float));
   const int rows = p.T * p.G;
-  // four warps per CTA when that still gives two CTAs per SM, else two
-  const int ctas4 = (rows + 63) / 64 * p.Hkv * p.B * a.NS;
-  const int nw = ctas4 >= 2 * p.sm_count ? 4 : 2;
+  const int nw = 4;  // 64 query rows per CTA; three CTAs fit an SM (registers and shared memory)
   dim3 grid((rows + 16 * nw - 1) / (16 * nw), p.Hkv * a.NS, p.B);
   const size_t smem = (size_t)4 * AM_KB * (p.Dh + 8) * sizeof(__nv_bfloat16);
   void (*k)(AmArgs);
@@ -371,14 +374,12 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   else k = nw == 4 ? tree_attn_mma_kernel<64, 4> : tree_attn_mma_kernel<64, 2>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  k<<<grid, nw * 32, smem, st>>>(a);
-  e = cudaGetLastError();
+  e = launch_k(k, grid, dim3(nw * 32), smem, st, true, a);
   if (e != cudaSuccess || a.NS == 1) return (int)e;
   const size_t nrow = (size_t)p.B * p.Hq * p.T;
   const unsigned cgrid = (unsigned)((nrow + 7) / 8);
-  if (p.Dh == 128) tree_attn_combine_kernel<128><<<cgrid, 256, 0, st>>>(a);
-  else tree_attn_combine_kernel<64><<<cgrid, 256, 0, st>>>(a);
-  return (int)cudaGetLastError();
+  if (p.Dh == 128) return (int)launch_k(tree_attn_combine_kernel<128>, dim3(cgrid), dim3(256), 0, st, true, a);
+  return (int)launch_k(tree_attn_combine_kernel<64>, dim3(cgrid), dim3(256), 0, st, true, a);
 }
 
 }  // namespace medusa

@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(GtArgs a) {
     tc::fence_mbar_init();
   }
   __syncthreads();
+  pdl_trigger();
 
   if (warp == 8) {
     // ---------------------------------------------------------------- producer
@@ -166,6 +167,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(GtArgs a) {
   }
 
   // ------------------------------------------------------------------ consumers
+  // (the producer streams weights, which no kernel writes, before the
+  // preceding kernel has finished; x, z and the outputs wait for it)
+  pdl_wait();
   const int nvec = a.H / 8;
   float xr[NC][VPL][8];
   int cur_seg = -1;
@@ -411,9 +415,8 @@ static int gemv_tma_launch(GtArgs a, int sm_count, int nc, cudaStream_t st, int*
   if (!k) return (int)cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  k<<<ctas, GT_THREADS, smem, st>>>(a);
   if (ctas_out) *ctas_out = ctas;
-  return (int)cudaGetLastError();
+  return (int)launch_k(k, dim3(ctas), dim3(GT_THREADS), smem, st, EPI == 1, a);
 }
 
 static int gt_nc(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : 4); }

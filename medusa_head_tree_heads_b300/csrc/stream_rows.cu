@@ -214,6 +214,8 @@ __global__ void __launch_bounds__(kThreads, 2) stream_rows_kernel(RowArgs a) {
   const int nvec = a.H / EPV;
   const bool typical = a.typical != 0;
 
+  pdl_trigger();
+  pdl_wait();
   SoftState soft;
   soft.m = -INFINITY;
   soft.z = 0.f;
@@ -393,6 +395,8 @@ template <int KM>
 __global__ void __launch_bounds__(256) topk_merge_kernel(RowArgs a, int nctas) {
   const int lane = threadIdx.x & 31;
   const int pair = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_trigger();
+  pdl_wait();
   if (pair >= a.nseg * a.C) return;
   const int seg = pair / a.C, c = pair - seg * a.C;
   const int kn = kept_of(a, seg);
@@ -443,13 +447,11 @@ static int launch_nc(RowArgs a, int sm_count, int nc, int ctiles, cudaStream_t s
       int ctas = 0;                                                                                         \
       partition(a.R, a.S, sm_count * (occ > 0 ? occ : 1), EPI == EPI_TOPK ? kRowBuf : (1 << 30), &ctas, &a.rpc); \
       if (ctas > kMaxStreamCtas) return (int)cudaErrorInvalidConfiguration;                                 \
-      k<<<dim3(ctas, ctiles), kThreads, smem, st>>>(a);                                                     \
-      e = cudaGetLastError();                                                                               \
+      e = launch_k(k, dim3(ctas, ctiles), dim3(kThreads), smem, st, EPI != EPI_FC, a);                      \
       if (e == cudaSuccess && EPI == EPI_TOPK) {                                                            \
         const unsigned mg = (unsigned)((a.nseg * a.C + 7) / 8);                                             \
-        if (a.kmax <= 4) topk_merge_kernel<4><<<mg, 256, 0, st>>>(a, ctas);                                 \
-        else topk_merge_kernel<KMAX><<<mg, 256, 0, st>>>(a, ctas);                                          \
-        e = cudaGetLastError();                                                                             \
+        if (a.kmax <= 4) e = launch_k(topk_merge_kernel<4>, dim3(mg), dim3(256), 0, st, true, a, ctas);     \
+        else e = launch_k(topk_merge_kernel<KMAX>, dim3(mg), dim3(256), 0, st, true, a, ctas);              \
       }                                                                                                     \
     }                                                                                                       \
     break;                                                                                                  \
@@ -484,9 +486,8 @@ int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t
   a.out_idx = topk_idx;
   a.out_val = topk_val;
   const unsigned mg = (unsigned)((a.nseg * a.C + 7) / 8);
-  if (a.kmax <= 4) topk_merge_kernel<4><<<mg, 256, 0, st>>>(a, ctas);
-  else topk_merge_kernel<KMAX><<<mg, 256, 0, st>>>(a, ctas);
-  return (int)cudaGetLastError();
+  if (a.kmax <= 4) return (int)launch_k(topk_merge_kernel<4>, dim3(mg), dim3(256), 0, st, true, a, ctas);
+  return (int)launch_k(topk_merge_kernel<KMAX>, dim3(mg), dim3(256), 0, st, true, a, ctas);
 }
 
 int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st) {

@@ -38,6 +38,8 @@ __global__ void tree_build_kernel(TreeArgs a) {
   const TreeDims& td = a.td;
   const int gid = blockIdx.x * blockDim.x + threadIdx.x;
   const int T = td.T;
+  pdl_trigger();
+  pdl_wait();
   if (gid < a.B * T) {
     const int b = gid / T, i = gid - b * T;
     const int d = node_depth(td, i);
@@ -94,8 +96,7 @@ int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* roo
   if (p.T > n) n = p.T;
   if (p.NL > n) n = p.NL;
   const int threads = 256;
-  tree_build_kernel<<<(n + threads - 1) / threads, threads, 0, st>>>(a);
-  return (int)cudaGetLastError();
+  return (int)launch_k(tree_build_kernel, dim3((n + threads - 1) / threads), dim3(threads), 0, st, true, a);
 }
 
 }  // namespace medusa

@@ -201,6 +201,8 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();  // the node operand is the previous kernel's output
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -349,6 +351,8 @@ template <bool TYPICAL>
 __global__ void __launch_bounds__(256) verify_merge_kernel(VtcArgs a) {
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_trigger();
+  pdl_wait();
   if (n >= a.N) return;
   Soft m = soft_empty();
   for (int vt0 = 0; vt0 < a.n_vt; vt0 += 128) {
@@ -461,13 +465,11 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, i
   cudaError_t ce = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.n_tiles < p.sm_count ? a.n_tiles : p.sm_count;
-  verify_tc_kernel<<<grid, VT_THREADS, smem, st>>>(tA, tB, a);
-  ce = cudaGetLastError();
+  ce = launch_k(verify_tc_kernel, dim3(grid), dim3(VT_THREADS), smem, st, true, tA, tB, a);
   if (ce != cudaSuccess) return (int)ce;
   const unsigned mgrid = (unsigned)((a.N + 7) / 8);
-  if (a.typical) verify_merge_kernel<true><<<mgrid, 256, 0, st>>>(a);
-  else verify_merge_kernel<false><<<mgrid, 256, 0, st>>>(a);
-  return (int)cudaGetLastError();
+  if (a.typical) return (int)launch_k(verify_merge_kernel<true>, dim3(mgrid), dim3(256), 0, st, true, a);
+  return (int)launch_k(verify_merge_kernel<false>, dim3(mgrid), dim3(256), 0, st, true, a);
 }
 
 }  // namespace medusa
