@@ -32,6 +32,7 @@ constexpr int GT_CONS = 256;           // consumer threads (8 warps)
 constexpr int GT_THREADS = GT_CONS + 32;  // + producer warp
 constexpr uint64_t GT_WAIT_NS = 20ull * 1000 * 1000;
 constexpr int GT_ROWBUF = 2048;        // rows per CTA (top-k row values kept in shared memory)
+constexpr int GT_GROUP = 8;            // max stages per reduction group (32 values per thread)
 
 struct GtArgs {
   const __nv_bfloat16* W;  // [R][H]
@@ -103,8 +104,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(GtArgs a) {
   const size_t row_bytes = (size_t)a.H * 2;
   const size_t stage_bytes = GT_RB * row_bytes;
   float* rowbuf = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);  // [NC][GT_ROWBUF] (EPI_TOPK)
-  float* red = rowbuf + (EPI == 1 ? NC * GT_ROWBUF : 0);                   // [2][8][GT_RB*NC]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * 8 * GT_RB * NC);
+  float* red = rowbuf + (EPI == 1 ? NC * GT_ROWBUF : 0);                   // [2][8 warps][32 values]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * 8 * 32);
   uint64_t* empty = full + S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
 
@@ -173,16 +174,133 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(GtArgs a) {
   const int nvec = a.H / 8;
   float xr[NC][VPL][8];
   int cur_seg = -1;
-  uint32_t k = 0;
-  int piece = 0, piece_row0 = r_begin;
-  for (int row = r_begin; row < r_end; ++k) {
-    int n, seg;
-    next_stage(a, r_end, row, n, seg);
-    if (seg != cur_seg) {
-      if (EPI == 1 && cur_seg >= 0) {  // close the previous piece of rows
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (warp < NC && warp < a.C) {
-          const int kn = gt_kept(a, cur_seg);
+  uint32_t k = 0;           // stage counter (same schedule as the producer)
+  int row = r_begin;
+  int piece = 0, piece_row0 = r_begin, piece_seg = r_begin / a.S;
+  int* grp_row = reinterpret_cast<int*>(full + 2 * S) + 4;  // [GT_GROUP] first row of each slot (-1: none)
+  int* grp_n = grp_row + GT_GROUP;                           // [GT_GROUP] rows in each slot
+  bool aborted = false;
+  constexpr int GR = 32 / NC;           // group rows per column
+  constexpr int GSLOT = GR / GT_RB;     // stages per group
+  for (int grp = 0; row < r_end && !aborted; ++grp) {
+    // ---- a group: GSLOT stages of GT_RB rows; acc[c * GR + r] holds this
+    // thread's partial sum of group row r (GR = 32 / NC rows) for column c
+    float acc[32];
+#pragma unroll
+    for (int g = 0; g < 32; ++g) acc[g] = 0.f;
+#pragma unroll
+    for (int slot = 0; slot < GSLOT; ++slot) {
+      int n = 0, seg = cur_seg;
+      if (row < r_end) next_stage(a, r_end, row, n, seg);
+      if (tid == 0) {
+        grp_row[slot] = n > 0 ? row : -1;
+        grp_n[slot] = n;
+      }
+      if (n > 0) {
+        if (seg != cur_seg) {  // uniform: every consumer reloads its x slice
+          load_x<VPL, NC>(a, seg, tid, xr);
+          cur_seg = seg;
+        }
+        const int s = k % S;
+        const uint32_t ph = (k / S) & 1u;
+        bool ok = tc::mbar_try_wait(&full[s], ph);
+        if (!ok) {
+          const uint64_t t0 = tc::globaltimer_ns();
+          while (!(ok = tc::mbar_try_wait(&full[s], ph))) {
+            if (*abort_flag) break;
+            if (tc::globaltimer_ns() - t0 > GT_WAIT_NS) {
+              set_error(a.ws, MEDUSA_ERR_TIMEOUT);
+              *abort_flag = 1;
+              break;
+            }
+          }
+        }
+        if (ok) {
+          const uint8_t* st = smem + (size_t)s * stage_bytes;
+#pragma unroll
+          for (int rr = 0; rr < GT_RB; ++rr) {
+            uint4 w[VPL];
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+              const int v = tid + GT_CONS * i;
+              w[i] = (rr < n && v < nvec) ? *reinterpret_cast<const uint4*>(st + rr * row_bytes + (size_t)v * 16)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+            }
+            // VPL * NC independent chains of 8 FMAs for this row (rows interleave after unrolling)
+            float part[VPL][NC];
+#pragma unroll
+            for (int i = 0; i < VPL; ++i)
+#pragma unroll
+              for (int c = 0; c < NC; ++c) part[i][c] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+#pragma unroll
+              for (int i = 0; i < VPL; ++i) {
+                const uint32_t wv = e < 2 ? w[i].x : e < 4 ? w[i].y : e < 6 ? w[i].z : w[i].w;
+                const float wf = (e & 1) ? bf16_hi(wv) : bf16_lo(wv);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) part[i][c] = fmaf(wf, xr[c][i][e], part[i][c]);
+              }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+              float t = 0.f;
+#pragma unroll
+              for (int i = 0; i < VPL; ++i) t += part[i][c];
+              acc[c * GR + slot * GT_RB + rr] = t;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[s]);  // this warp has read the stage
+        ++k;
+        row += n;
+      }
+    }
+    // ---- butterfly transpose-reduce over the 32 lanes: lane l ends with the
+    // warp's partial of value l (column l / GR, group row l % GR); 31 exchanges
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+      const int o = 16 >> step, half = 16 >> step;
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = up ? acc[i] : acc[i + half];
+        const float keep = up ? acc[i + half] : acc[i];
+        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    const int par = grp & 1;
+    red[(par * 8 + warp) * 32 + lane] = acc[0];
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (*abort_flag) aborted = true;
+    // ---- row values: thread t < 32 finishes value t (column t / GR, group row t % GR)
+    if (!aborted && tid < 32) {
+      const int c = tid / GR, gr = tid % GR;
+      const int r0 = grp_row[gr / GT_RB];
+      if (r0 >= 0 && (gr % GT_RB) < grp_n[gr / GT_RB] && c < a.C) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) t += red[(par * 8 + w) * 32 + tid];
+        const int r = r0 + gr % GT_RB;
+        const int seg = r / a.S, j = r - seg * a.S;
+        if (EPI == 0) {
+          const float pre = t + __bfloat162float(a.bias[(size_t)seg * a.H + j]);
+          const float silu = pre / (1.f + expf(-pre));
+          a.z[((size_t)c * a.nseg + seg) * a.H + j] = __bfloat162float(a.hres[(size_t)c * a.H + j]) + silu;
+        } else {
+          rowbuf[c * GT_ROWBUF + (r - r_begin)] = t;
+        }
+      }
+    }
+    // ---- top-k of every segment piece that ended in (or before) this group
+    if (EPI == 1) {
+      const int seg_now = row < r_end ? row / a.S : -1;
+      if (seg_now != piece_seg) {
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // rowbuf complete
+        // pieces [piece_row0, end) of piece_seg, and any whole segment in between (none: rpc <= S)
+        const int end = row < r_end ? seg_now * a.S : r_end;
+        if (!aborted && warp < NC && warp < a.C) {
+          const int kn = gt_kept(a, piece_seg);
           float lv[MEDUSA_MAX_TOPK];
           int li[MEDUSA_MAX_TOPK];
 #pragma unroll
@@ -190,14 +308,11 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(GtArgs a) {
             lv[i] = -INFINITY;
             li[i] = INT_MAX;
           }
-          for (int e = lane; e < row - piece_row0; e += 32) {
-            const float v = rowbuf[warp * GT_ROWBUF + (piece_row0 - r_begin) + e];
-            const int id = piece_row0 + e - cur_seg * a.S;
-            // insertion into a best-first list (compare-and-swap pass)
-            float cv = v;
-            int ci = id;
+          for (int e = lane; e < end - piece_row0; e += 32) {
+            float cv = rowbuf[warp * GT_ROWBUF + (piece_row0 - r_begin) + e];
+            int ci = piece_row0 + e - piece_seg * a.S;
 #pragma unroll
-            for (int i = 0; i < MEDUSA_MAX_TOPK; ++i) {
+            for (int i = 0; i < MEDUSA_MAX_TOPK; ++i) {  // compare-and-swap insertion
               const bool sw = (i < kn) && better(cv, ci, lv[i], li[i]);
               const float ov = lv[i];
               const int oi = li[i];
@@ -236,150 +351,16 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(GtArgs a) {
             }
           }
         }
-        if (tid == 0) a.cand_seg[blockIdx.x * kMaxPieces + piece] = cur_seg;
+        if (tid == 0) a.cand_seg[blockIdx.x * kMaxPieces + piece] = aborted ? -1 : piece_seg;
         ++piece;
-        piece_row0 = row;
-      }
-      load_x<VPL, NC>(a, seg, tid, xr);
-      cur_seg = seg;
-    }
-    const int s = k % S;
-    const uint32_t ph = (k / S) & 1u;
-    bool ok = tc::mbar_try_wait(&full[s], ph);
-    if (!ok) {
-      const uint64_t t0 = tc::globaltimer_ns();
-      while (!(ok = tc::mbar_try_wait(&full[s], ph))) {
-        if (*abort_flag) break;
-        if (tc::globaltimer_ns() - t0 > GT_WAIT_NS) {
-          set_error(a.ws, MEDUSA_ERR_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
+        piece_row0 = end;
+        piece_seg = seg_now;
       }
     }
-    float acc[GT_RB][NC];
-#pragma unroll
-    for (int rr = 0; rr < GT_RB; ++rr)
-#pragma unroll
-      for (int c = 0; c < NC; ++c) acc[rr][c] = 0.f;
-    if (ok) {
-      const uint8_t* st = smem + (size_t)s * stage_bytes;
-#pragma unroll
-      for (int rr = 0; rr < GT_RB; ++rr) {
-        if (rr < n) {
-#pragma unroll
-          for (int i = 0; i < VPL; ++i) {
-            const int v = tid + GT_CONS * i;
-            if (v < nvec) {
-              const uint4 w = *reinterpret_cast<const uint4*>(st + rr * row_bytes + (size_t)v * 16);
-              const float wf[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                                   bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-#pragma unroll
-              for (int c = 0; c < NC; ++c) {
-                float t = acc[rr][c];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t = fmaf(wf[e], xr[c][i][e], t);
-                acc[rr][c] = t;
-              }
-            }
-          }
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&empty[s]);  // this warp has read the stage
-    // ---- reduce the 256 partial sums of each (row, column)
-    const int par = k & 1;
-#pragma unroll
-    for (int rr = 0; rr < GT_RB; ++rr)
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const float t = warp_sum(acc[rr][c]);
-        if (lane == 0) red[(par * 8 + warp) * GT_RB * NC + rr * NC + c] = t;
-      }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (*abort_flag) break;
-    if (tid < GT_RB * NC) {
-      const int rr = tid / NC, c = tid - rr * NC;
-      if (rr < n && c < a.C) {
-        float t = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) t += red[(par * 8 + w) * GT_RB * NC + tid];
-        const int r = row + rr, j = r - seg * a.S;
-        if (EPI == 0) {
-          const float pre = t + __bfloat162float(a.bias[(size_t)seg * a.H + j]);
-          const float silu = pre / (1.f + expf(-pre));
-          a.z[((size_t)c * a.nseg + seg) * a.H + j] = __bfloat162float(a.hres[(size_t)c * a.H + j]) + silu;
-        } else {
-          rowbuf[c * GT_ROWBUF + (r - r_begin)] = t;
-        }
-      }
-    }
-    row += n;
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // grp_row / grp_n are rewritten by the next group
   }
-  if (EPI == 1) {
-    // last piece, then mark the unused candidate slots
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (cur_seg >= 0 && !*abort_flag && warp < NC && warp < a.C) {
-      const int kn = gt_kept(a, cur_seg);
-      float lv[MEDUSA_MAX_TOPK];
-      int li[MEDUSA_MAX_TOPK];
-#pragma unroll
-      for (int i = 0; i < MEDUSA_MAX_TOPK; ++i) {
-        lv[i] = -INFINITY;
-        li[i] = INT_MAX;
-      }
-      for (int e = lane; e < r_end - piece_row0; e += 32) {
-        const float v = rowbuf[warp * GT_ROWBUF + (piece_row0 - r_begin) + e];
-        const int id = piece_row0 + e - cur_seg * a.S;
-        float cv = v;
-        int ci = id;
-#pragma unroll
-        for (int i = 0; i < MEDUSA_MAX_TOPK; ++i) {
-          const bool sw = (i < kn) && better(cv, ci, lv[i], li[i]);
-          const float ov = lv[i];
-          const int oi = li[i];
-          lv[i] = sw ? cv : ov;
-          li[i] = sw ? ci : oi;
-          cv = sw ? ov : cv;
-          ci = sw ? oi : ci;
-        }
-      }
-      const size_t base = ((size_t)(blockIdx.x * kMaxPieces + piece) * a.C + warp) * a.kmax;
-      for (int rnk = 0; rnk < a.kmax; ++rnk) {
-        float bv = lv[0];
-        int bi = li[0];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (better(ov, oi, bv, bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        if (bi != INT_MAX && lv[0] == bv && li[0] == bi) {
-#pragma unroll
-          for (int i = 0; i < MEDUSA_MAX_TOPK - 1; ++i) {
-            lv[i] = lv[i + 1];
-            li[i] = li[i + 1];
-          }
-          lv[MEDUSA_MAX_TOPK - 1] = -INFINITY;
-          li[MEDUSA_MAX_TOPK - 1] = INT_MAX;
-        }
-        if (lane == 0) {
-          const bool live = rnk < kn && bi != INT_MAX;
-          a.cand_val[base + rnk] = live ? bv : -INFINITY;
-          a.cand_idx[base + rnk] = live ? bi : INT_MAX;
-        }
-      }
-    }
-    if (tid == 0) {
-      int p = piece;
-      if (cur_seg >= 0) a.cand_seg[blockIdx.x * kMaxPieces + p++] = *abort_flag ? -1 : cur_seg;
-      for (; p < kMaxPieces; ++p) a.cand_seg[blockIdx.x * kMaxPieces + p] = -1;
-    }
-  }
+  if (EPI == 1 && tid == 0)
+    for (int p = piece; p < kMaxPieces; ++p) a.cand_seg[blockIdx.x * kMaxPieces + p] = -1;
 }
 
 // ------------------------------------------------------------------- host --
@@ -399,7 +380,7 @@ static int gemv_tma_launch(GtArgs a, int sm_count, int nc, cudaStream_t st, int*
   if (ctas > kMaxStreamCtas) return (int)cudaErrorNotSupported;
   a.rpc = rpc;
   const size_t stage = (size_t)GT_RB * a.H * 2;
-  const size_t fixed = 128 + (EPI == 1 ? (size_t)nc * GT_ROWBUF * 4 : 0) + 2 * 8 * GT_RB * nc * 4 + 256;
+  const size_t fixed = 128 + (EPI == 1 ? (size_t)nc * GT_ROWBUF * 4 : 0) + 2 * 8 * 32 * 4 + 512;
   int S = (int)((220 * 1024 - fixed) / stage);
   if (S > 8) S = 8;
   if (S < 2) return (int)cudaErrorNotSupported;
