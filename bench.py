@@ -317,7 +317,7 @@ def run_medusa(args, world, rank, local):
             "roofline": roofline,
             "e2e": {"value": round(world / e2e_dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * nk, "clocks": clk.summary()}
+            "gpu_launches": args.steps * M.step_launches(cfg), "clocks": clk.summary()}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(s, inp, budget_s=args.cpu_budget)
     if rank == 0:

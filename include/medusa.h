@@ -201,6 +201,11 @@ int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* wo
 int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
                          void* const* events, int32_t n_events);
 
+/* Number of kernel launches one medusa_step makes for this config on the
+ * current device (the kernels chosen depend on the shape and the SM count);
+ * negative medusa_status_t on an invalid config.  Host-only. */
+int medusa_step_launches(const medusa_config_t* cfg);
+
 /* Copies the device error word of `workspace` to *code (host pointer; 0 = no
  * error, else a medusa_status_t) after synchronising `stream`, then clears it. */
 int medusa_get_device_error(void* workspace, int32_t* code, void* stream);

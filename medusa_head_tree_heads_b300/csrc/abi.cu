@@ -307,6 +307,22 @@ int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io,
   return run_step(cfg, io, workspace, stream, events, n_events);
 }
 
+int medusa_step_launches(const medusa_config_t* cfg) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  finish_plan(&p);
+  int n = 6;                        // one launch per stage
+  n += 1;                           // top-k candidate merge
+  if (p.bf16) {
+    int NS, cb;
+    attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &NS, &cb);
+    if (NS > 1) n += 1;             // split-attention combine
+    n += 1;                         // verification partial merge
+  }
+  return n;
+}
+
 int medusa_get_device_error(void* workspace, int32_t* code, void* stream) {
   if (!workspace || !code) return MEDUSA_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;

@@ -85,8 +85,7 @@ __global__ void __launch_bounds__(NW * 32, 12 / NW) tree_attn_mma_kernel(AmArgs 
   const int nrows = a.T * a.G;
   const int rbase = blockIdx.x * 16 * NW + warp * 16;
   const size_t kv_row = (size_t)a.Hkv * DH;  // elements between consecutive keys
-  pdl_trigger();
-  pdl_wait();
+  pdl_trigger();  // (pdl_wait comes before the first read of the tree mask)
 
   // ---- Q fragments (rows gq and gq+8 of this warp), scale folded in later
   uint32_t qf[KS][4];
@@ -178,6 +177,7 @@ __global__ void __launch_bounds__(NW * 32, 12 / NW) tree_attn_mma_kernel(AmArgs 
     // ---- mask, scale, online softmax (rows gq and gq+8)
     uint32_t mw[2][2] = {{0u, 0u}, {0u, 0u}};
     if (tree) {
+      pdl_wait();  // the mask is written by the tree-build kernel
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr)
         if (node[hr] >= 0) {

@@ -43,6 +43,7 @@ struct Plan {
 int make_plan(const medusa_config_t* cfg, Plan* p);  // medusa_status_t
 size_t verify_tc_part_bytes(int V, int N);
 size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh);
+void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks);
 int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
                      float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 

@@ -39,8 +39,8 @@ __global__ void tree_build_kernel(TreeArgs a) {
   const int gid = blockIdx.x * blockDim.x + threadIdx.x;
   const int T = td.T;
   pdl_trigger();
-  pdl_wait();
   if (gid < a.B * T) {
+    pdl_wait();  // the top-k lists come from the previous kernel
     const int b = gid / T, i = gid - b * T;
     const int d = node_depth(td, i);
     int tok;

@@ -202,23 +202,39 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();
-  pdl_wait();  // the node operand is the previous kernel's output
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t g = 0;
       bool ok = true;
+      // lm_head is a weight no kernel writes: the first ring of its tiles is
+      // requested before waiting for the kernel that produces the node operand
+      const int first_t = blockIdx.x;
+      const int npre = first_t < a.n_tiles ? (a.nk < S ? a.nk : S) : 0;
+      for (int kb = 0; kb < npre; ++kb) {
+        const int vt = first_t / a.n_nt;
+        uint8_t* sa = smem + (size_t)kb * stage_bytes;
+        tc::mbar_arrive_expect_tx(&full[kb], stage_bytes);
+#pragma unroll
+        for (int h = 0; h < VT_SUB; ++h)
+          tc::tma_load_2d(sa + h * bytesA1, &tmA, &full[kb], kb * VT_BK, (vt * VT_SUB + h) * VT_M);
+      }
+      pdl_wait();  // the node operand is the previous kernel's output
       for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x) {
         const int vt = t / a.n_nt, nt = t - vt * a.n_nt;
         for (int kb = 0; kb < a.nk; ++kb, ++g) {
           const int s = g % S;
           const uint32_t ph = (g / S) & 1u;
+          uint8_t* sa = smem + (size_t)s * stage_bytes;
+          if (g < (uint32_t)npre) {  // A already requested: add the node tile
+            tc::tma_load_2d(sa + bytesA, &tmB, &full[s], kb * VT_BK, nt * a.BN);
+            continue;
+          }
           if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.ws)) {
             ok = false;
             break;
           }
-          uint8_t* sa = smem + (size_t)s * stage_bytes;
           tc::mbar_arrive_expect_tx(&full[s], stage_bytes);
 #pragma unroll
           for (int h = 0; h < VT_SUB; ++h)

@@ -25,7 +25,7 @@ STATUS = {0: "MEDUSA_OK", -1: "MEDUSA_ERR_INVALID_ARG", -2: "MEDUSA_ERR_UNSUPPOR
 # every symbol include/medusa.h declares
 EXPORTS = ("medusa_workspace_bytes", "medusa_tree_size", "medusa_heads_topk", "medusa_tree_build",
            "medusa_tree_attn", "medusa_verify_accept", "medusa_step", "medusa_step_profiled",
-           "medusa_get_device_error", "medusa_status_string")
+           "medusa_step_launches", "medusa_get_device_error", "medusa_status_string")
 STEP_KERNELS = ("head_layer", "head_proj_topk", "tree_build", "tree_attn", "verify_proj", "accept")
 
 
@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.medusa_step.argtypes = [cfgp, ctypes.POINTER(StepIO), vp, vp]
         L.medusa_step_profiled.argtypes = [cfgp, ctypes.POINTER(StepIO), vp, vp, ctypes.POINTER(vp), ctypes.c_int32]
         L.medusa_get_device_error.argtypes = [vp, i32p, vp]
+        L.medusa_step_launches.argtypes = [cfgp]
         L.medusa_status_string.argtypes = [ctypes.c_int]
         L.medusa_status_string.restype = ctypes.c_char_p
         for f in EXPORTS:
@@ -220,6 +221,13 @@ def medusa_get_device_error(ws, stream=None) -> int:
     code = ctypes.c_int32()
     _check("medusa_get_device_error", lib().medusa_get_device_error(_p(ws), ctypes.byref(code), _stream(stream)))
     return code.value
+
+
+def step_launches(cfg: Config) -> int:
+    n = lib().medusa_step_launches(ctypes.byref(cfg))
+    if n < 0:
+        raise MedusaError("medusa_step_launches", n)
+    return n
 
 
 def status_string(code: int) -> str:
