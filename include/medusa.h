@@ -158,6 +158,20 @@ int medusa_heads_topk(const medusa_config_t* cfg, const void* h, const void* W1,
 int medusa_tree_build(const medusa_config_t* cfg, const int32_t* topk_idx, const int32_t* root_token,
                       const medusa_tree_t* tree, void* stream);
 
+/* medusa_heads_topk without a caller workspace, for callers that cannot
+ * allocate device memory (a frozen allocator in a serving loop, a memory
+ * budget that forbids new allocations, a host runtime with no CUDA
+ * allocator).  It has no counterpart in the method's description: it exists
+ * only for this calling constraint.  Same inputs, outputs and results as
+ * medusa_heads_topk; the scratch lives in a fixed 16 MiB device array inside
+ * the library (held on every GPU that loads it until exit), so a config that
+ * needs more returns MEDUSA_ERR_UNSUPPORTED.  All calls on a device share that
+ * array -- calls that overlap on the GPU race, so serialise them.  The first
+ * call on a device looks up the array's address (make it before any stream
+ * capture).  Device-side error codes are not reported by this variant. */
+int medusa_heads_topk_noalloc(const medusa_config_t* cfg, const void* h, const void* W1, const void* b1,
+                              const void* W2, int32_t* topk_idx, float* topk_val, void* stream);
+
 /* Tree attention in one pass ("Attenzione sull'albero e accettazione"; "Plongee
  * profonde"): for each b, q head h (kv head h / (Hq/Hkv)) and node i,
  *   o = sum_j softmax_j(q.k_j / sqrt(Dh)) v_j

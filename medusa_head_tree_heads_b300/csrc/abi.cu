@@ -15,15 +15,15 @@ int launch_proj_tma(const Plan& p, const void* W2, int32_t* topk_idx, float* top
 
 // head layer / head projection: the TMA-fed small-batch kernel where it
 // applies (bf16, batch <= 4), else the general streaming kernel
-static int launch_head_layer(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws,
+int launch_head_layer(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws,
                              cudaStream_t st) {
   if (gemv_tma_supported(p)) return launch_fc_tma(p, h, W1, b1, ws, st);
   return launch_fc(p, h, W1, b1, ws, st);
 }
 int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                      cudaStream_t st);
-static int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
-                            cudaStream_t st);
+int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
+                     cudaStream_t st);
 
 int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
                        float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
@@ -133,7 +133,7 @@ int make_plan(const medusa_config_t* c, Plan* p) {
 }
 
 // launch shapes need the device's SM count
-static void finish_plan(Plan* p) {
+void finish_plan(Plan* p) {
   p->sm_count = sm_count();
   p->fc_nc = pick_nc(p->H, p->B);
   p->fc_ctiles = (p->B + p->fc_nc - 1) / p->fc_nc;
@@ -143,8 +143,8 @@ static void finish_plan(Plan* p) {
   p->vf_ctiles = (p->B * p->T + p->vf_nc - 1) / p->vf_nc;
 }
 
-static int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
-                            cudaStream_t st) {
+int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
+                     cudaStream_t st) {
   if (gemv_tma_supported(p)) return launch_proj_tma(p, W2, topk_idx, topk_val, ws, st);
   return launch_proj_topk(p, W2, topk_idx, topk_val, ws, st);
 }

@@ -41,6 +41,11 @@ struct Plan {
 };
 
 int make_plan(const medusa_config_t* cfg, Plan* p);  // medusa_status_t
+void finish_plan(Plan* p);                            // launch shapes for the current device
+// the two launches of the heads stage (shape-dependent kernel choice)
+int launch_head_layer(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
+int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
+                     cudaStream_t st);
 size_t verify_tc_part_bytes(int V, int N);
 size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh);
 void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks);

@@ -1,0 +1,77 @@
+// medusa_heads_topk_noalloc: the heads + per-head top-k stage for callers
+// that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocating routine) at the
+// point where they run the heads: a serving loop whose allocator is frozen
+// after warm-up, code running under a memory budget that forbids new
+// allocations, or a host runtime that owns no CUDA allocator at all.  They can
+// still pass their inputs and outputs, but not a workspace.  This entry point
+// therefore keeps the stage's scratch -- the fp32 head activations z and the
+// per-CTA top-k candidates -- in one fixed array compiled into the library.
+//
+// Limits and sharing:
+//   * the array holds kNoAllocScratchBytes (16 MiB) on every GPU that loads
+//     the library, until the process exits; a config whose heads scratch is
+//     larger is rejected with MEDUSA_ERR_UNSUPPORTED before any launch;
+//   * every call on a device uses the same array and leaves its contents
+//     behind; the call clears the part that must start at zero (the device
+//     error word and tickets) before its kernels run;
+//   * calls whose work overlaps on the GPU (other streams, other host
+//     threads) race on the array: serialise them;
+//   * device-side error codes land in the array's error word, which this
+//     entry point does not report.
+// The array's device address is looked up once per device with
+// cudaGetSymbolAddress, on the first call made with that device current;
+// make that first call before any stream capture.
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace medusa {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+static void* g_scratch_addr[kMaxDevices];
+static std::mutex g_scratch_mu;
+
+// Device address of the scratch array for the current device (set-up on first use).
+static int scratch_for_current_device(uint8_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MEDUSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MEDUSA_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = static_cast<uint8_t*>(g_scratch_addr[dev]);
+  return MEDUSA_OK;
+}
+
+static bool al16(const void* x) { return x && ((uintptr_t)x & 15u) == 0; }
+
+}  // namespace medusa
+
+using namespace medusa;
+
+extern "C" int medusa_heads_topk_noalloc(const medusa_config_t* cfg, const void* h, const void* W1, const void* b1,
+                                         const void* W2, int32_t* topk_idx, float* topk_val, void* stream) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!al16(h) || !al16(W1) || !al16(b1) || !al16(W2) || !topk_idx || !topk_val) return MEDUSA_ERR_INVALID_ARG;
+  // the heads stage uses the workspace up to the end of the candidate slots
+  const size_t need = p.off_cand_seg + (size_t)kMaxStreamCtas * kMaxPieces * sizeof(int);
+  if (need > kNoAllocScratchBytes) return MEDUSA_ERR_UNSUPPORTED;
+  uint8_t* ws = nullptr;
+  if ((s = scratch_for_current_device(&ws)) != MEDUSA_OK) return s;
+  finish_plan(&p);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return MEDUSA_ERR_CUDA;  // error word + tickets
+  int e = launch_head_layer(p, h, W1, b1, ws, st);
+  if (e) return MEDUSA_ERR_CUDA;
+  e = launch_head_proj(p, W2, topk_idx, topk_val, ws, st);
+  return e ? MEDUSA_ERR_CUDA : MEDUSA_OK;
+}

@@ -25,7 +25,8 @@ STATUS = {0: "MEDUSA_OK", -1: "MEDUSA_ERR_INVALID_ARG", -2: "MEDUSA_ERR_UNSUPPOR
 # every symbol include/medusa.h declares
 EXPORTS = ("medusa_workspace_bytes", "medusa_tree_size", "medusa_heads_topk", "medusa_tree_build",
            "medusa_tree_attn", "medusa_verify_accept", "medusa_step", "medusa_step_profiled",
-           "medusa_step_launches", "medusa_get_device_error", "medusa_status_string")
+           "medusa_step_launches", "medusa_get_device_error", "medusa_status_string",
+           "medusa_heads_topk_noalloc")
 STEP_KERNELS = ("head_layer", "head_proj_topk", "tree_build", "tree_attn", "verify_proj", "accept")
 
 
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         L.medusa_step_profiled.argtypes = [cfgp, ctypes.POINTER(StepIO), vp, vp, ctypes.POINTER(vp), ctypes.c_int32]
         L.medusa_get_device_error.argtypes = [vp, i32p, vp]
         L.medusa_step_launches.argtypes = [cfgp]
+        L.medusa_heads_topk_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp]
         L.medusa_status_string.argtypes = [ctypes.c_int]
         L.medusa_status_string.restype = ctypes.c_char_p
         for f in EXPORTS:
@@ -154,6 +156,13 @@ def _tree_struct(t: Dict[str, torch.Tensor]) -> Tree:
 def medusa_heads_topk(cfg: Config, h, W1, b1, W2, topk_idx, topk_val, ws, stream=None) -> None:
     _check("medusa_heads_topk", lib().medusa_heads_topk(ctypes.byref(cfg), _p(h), _p(W1), _p(b1), _p(W2),
                                                         _p(topk_idx), _p(topk_val), _p(ws), _stream(stream)))
+
+
+def medusa_heads_topk_noalloc(cfg: Config, h, W1, b1, W2, topk_idx, topk_val, stream=None) -> None:
+    """medusa_heads_topk for callers that cannot allocate device memory: no
+    workspace argument; the library's fixed device scratch array is used."""
+    _check("medusa_heads_topk_noalloc", lib().medusa_heads_topk_noalloc(
+        ctypes.byref(cfg), _p(h), _p(W1), _p(b1), _p(W2), _p(topk_idx), _p(topk_val), _stream(stream)))
 
 
 def medusa_tree_build(cfg: Config, topk_idx, root_token, tree: Dict[str, torch.Tensor], stream=None) -> None:
