@@ -220,6 +220,13 @@ int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io,
  * negative medusa_status_t on an invalid config.  Host-only. */
 int medusa_step_launches(const medusa_config_t* cfg);
 
+/* Checks, on the current device, the bounded-wait path every kernel of the
+ * library uses: one CTA waits on an mbarrier that nothing completes; after
+ * budget_us microseconds (1..1000000) the wait gives up, MEDUSA_ERR_TIMEOUT
+ * is recorded in the workspace error word and the kernel returns, leaving the
+ * context usable.  Read the result with medusa_get_device_error. */
+int medusa_check_bounded_wait(void* workspace, int32_t budget_us, void* stream);
+
 /* Copies the device error word of `workspace` to *code (host pointer; 0 = no
  * error, else a medusa_status_t) after synchronising `stream`, then clears it. */
 int medusa_get_device_error(void* workspace, int32_t* code, void* stream);

@@ -9,6 +9,7 @@ namespace medusa {
 
 int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
 bool gemv_tma_supported(const Plan& p);
+int launch_bounded_wait_probe(uint8_t* ws, uint64_t budget_ns, cudaStream_t st);
 int launch_fc_tma(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
 int launch_proj_tma(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                     cudaStream_t st);
@@ -305,6 +306,12 @@ int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io,
                          void* const* events, int32_t n_events) {
   if (!events) return MEDUSA_ERR_INVALID_ARG;
   return run_step(cfg, io, workspace, stream, events, n_events);
+}
+
+int medusa_check_bounded_wait(void* workspace, int32_t budget_us, void* stream) {
+  if (!aligned16(workspace) || budget_us < 1 || budget_us > 1000000) return MEDUSA_ERR_INVALID_ARG;
+  return cuda_status(launch_bounded_wait_probe((uint8_t*)workspace, (uint64_t)budget_us * 1000,
+                                               (cudaStream_t)stream));
 }
 
 int medusa_step_launches(const medusa_config_t* cfg) {

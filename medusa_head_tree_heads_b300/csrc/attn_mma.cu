@@ -5,14 +5,16 @@
 //   o[b][i][h] = sum_j softmax_j(q . k_j / sqrt(Dh)) v_j
 //   over cache rows j < L, then tree nodes j allowed by the node's mask row.
 //
-// A CTA owns 16*NW query rows of one (sequence b, kv head g); query row r is
+// A CTA owns 16*NW query rows (NW <= 12 warps: all rows of the (b, g) pair
+// when they fit, so K/V are read once for all of them) of one (sequence b,
+// kv head g); query row r is
 // (node r / G, q head g*G + r % G).  Each warp holds 16 rows: their Q
 // fragments stay in registers for the whole pass, S = Q K^T and O += P V are
 // m16n8k16 bf16 MMAs with fp32 accumulation, the online softmax keeps its
 // running max and sum per row in registers, and P is repacked from the S
-// accumulators straight into A fragments.  K/V blocks of 64 keys are
-// double-buffered in shared memory with cp.async (rows padded to break bank
-// conflicts); cache blocks need no mask, tree blocks test one mask bit per
+// accumulators straight into A fragments.  K/V blocks of 64 keys stream
+// through an S-deep cp.async ring in shared memory (rows padded to break
+// bank conflicts); cache blocks need no mask, tree blocks test one mask bit per
 // (row, key).  When (rows / 32) * Hkv * B is too small to fill the GPU the key
 // range is split (flash-decoding): a few cache chunks plus one tree chunk per
 // (b, g, row block), each writing an unnormalised partial (o, max, sum) that
@@ -69,15 +71,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int DH, int NW>
-__global__ void __launch_bounds__(NW * 32, 12 / NW) tree_attn_mma_kernel(AmArgs a) {
+template <int DH, int NW, int S>
+__global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
   constexpr int LD = DH + 8;  // padded smem row (elements)
   constexpr int NT = NW * 32;
   constexpr int KS = DH / 16;  // k-steps of Q K^T
   constexpr int ND = DH / 8;   // n-tiles of O
   extern __shared__ float4 am_smem[];
-  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(am_smem);  // [2][AM_KB][LD]
-  __nv_bfloat16* Vs = Ks + 2 * AM_KB * LD;                          // [2][AM_KB][LD]
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(am_smem);  // [S][AM_KB][LD]
+  __nv_bfloat16* Vs = Ks + S * AM_KB * LD;                          // [S][AM_KB][LD]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;  // mma group / thread-in-group
@@ -142,15 +144,19 @@ __global__ void __launch_bounds__(NW * 32, 12 / NW) tree_attn_mma_kernel(AmArgs 
     cp_async_commit();
   };
 
-  if (blk_lo < blk_hi) load_block(blk_lo, 0);
+  // S-deep ring: S-1 blocks in flight ahead of the one being computed (one
+  // cp.async group per block; empty groups keep the count uniform)
+#pragma unroll
+  for (int pi = 0; pi < S - 1; ++pi) {
+    if (blk_lo + pi < blk_hi) load_block(blk_lo + pi, pi);
+    else cp_async_commit();
+  }
   for (int blk = blk_lo; blk < blk_hi; ++blk) {
-    const int buf = (blk - blk_lo) & 1;
-    if (blk + 1 < blk_hi) {
-      load_block(blk + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int i = blk - blk_lo;
+    const int buf = i % S;
+    if (blk + S - 1 < blk_hi) load_block(blk + S - 1, (i + S - 1) % S);
+    else cp_async_commit();
+    cp_async_wait<S - 1>();  // every group but the S-1 newest has landed: block blk is in
     __syncthreads();
 
     const bool tree = blk >= nb_cache;
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(NW * 32, 12 / NW) tree_attn_mma_kernel(AmArgs 
         mma16816(o[j + 1], af, bf[2], bf[3]);
       }
     }
-    __syncthreads();  // this buffer is refilled two blocks later
+    __syncthreads();  // this buffer is refilled S-1 blocks later
   }
 
   // ---- split mode: unnormalised partial; else normalise and store (bf16)
@@ -317,9 +323,24 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(AmArgs a) {
 
 // Key splits for a shape (device independent, so the workspace can be sized
 // from the config alone): split when fewer than ~2 waves of 2-warp CTAs exist.
+// Warps per CTA (16 query rows each) for a shape: all rows of one (b, kv head)
+// in one CTA when they fit 12 warps (K/V blocks are then loaded once for every
+// row), else row blocks of 12 warps.
+static int attn_warps(int rows) {
+  if (rows <= 64) return 4;
+  if (rows <= 128) return 8;
+  return 12;
+}
+
+// Key splits for a shape (device independent, so the workspace can be sized
+// from the config alone): when the (row block, b, kv head) CTAs do not cover
+// the ~148 SMs of a B300, the cache is cut into chunks and the tree becomes
+// one more split, each CTA writing a partial that the combine kernel merges.
 void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks) {
-  constexpr int kSlots = 444;  // ~3 resident 4-warp CTAs on each of 148 SMs
-  const int row_blocks = (T * G + 63) / 64;
+  constexpr int kSlots = 148;
+  const int rows = T * G;
+  const int nw = attn_warps(rows);
+  const int row_blocks = (rows + 16 * nw - 1) / (16 * nw);
   const int base = row_blocks * Hkv * B;
   const int nbc = (L + AM_KB - 1) / AM_KB;
   *NS = 1;
@@ -366,12 +387,21 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);
   a.part_ml = reinterpret_cast<float2*>(ws + p.off_attn_part + rows_all * p.Dh * sizeof(float));
   const int rows = p.T * p.G;
-  const int nw = 4;  // 64 query rows per CTA; three CTAs fit an SM (registers and shared memory)
+  const int nw = attn_warps(rows);
   dim3 grid((rows + 16 * nw - 1) / (16 * nw), p.Hkv * a.NS, p.B);
-  const size_t smem = (size_t)4 * AM_KB * (p.Dh + 8) * sizeof(__nv_bfloat16);
-  void (*k)(AmArgs);
-  if (p.Dh == 128) k = nw == 4 ? tree_attn_mma_kernel<128, 4> : tree_attn_mma_kernel<128, 2>;
-  else k = nw == 4 ? tree_attn_mma_kernel<64, 4> : tree_attn_mma_kernel<64, 2>;
+  // a 4-block ring (one CTA per SM) when the grid is a single wave, else a
+  // 2-block ring so that several CTAs share an SM
+  const int ctas = (int)(grid.x * grid.y * grid.z);
+  const int S = ctas <= p.sm_count ? 4 : 2;
+  const size_t smem = (size_t)2 * S * AM_KB * (p.Dh + 8) * sizeof(__nv_bfloat16);
+  void (*k)(AmArgs) = nullptr;
+#define AM_PICK(D, W, SS) \
+  if (p.Dh == D && nw == W && S == SS) k = tree_attn_mma_kernel<D, W, SS>;
+  AM_PICK(128, 4, 2) AM_PICK(128, 8, 2) AM_PICK(128, 12, 2) AM_PICK(128, 4, 4) AM_PICK(128, 8, 4)
+  AM_PICK(128, 12, 4) AM_PICK(64, 4, 2) AM_PICK(64, 8, 2) AM_PICK(64, 12, 2) AM_PICK(64, 4, 4)
+  AM_PICK(64, 8, 4) AM_PICK(64, 12, 4)
+#undef AM_PICK
+  if (!k) return (int)cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   e = launch_k(k, grid, dim3(nw * 32), smem, st, true, a);

@@ -401,6 +401,22 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(VtcArgs a) {
   }
 }
 
+// One CTA waits on an mbarrier that no thread or copy ever completes, with
+// the same bounded wait as the kernels above, then reports the timeout.
+__global__ void bounded_wait_probe_kernel(uint8_t* ws, uint64_t budget_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+    if (!tc::mbar_wait(&bar, 0, budget_ns)) set_error(ws, MEDUSA_ERR_TIMEOUT);
+  }
+}
+
+int launch_bounded_wait_probe(uint8_t* ws, uint64_t budget_ns, cudaStream_t st) {
+  bounded_wait_probe_kernel<<<1, 32, 0, st>>>(ws, budget_ns);
+  return (int)cudaGetLastError();
+}
+
 // ------------------------------------------------------------------- host --
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,

@@ -26,7 +26,7 @@ STATUS = {0: "MEDUSA_OK", -1: "MEDUSA_ERR_INVALID_ARG", -2: "MEDUSA_ERR_UNSUPPOR
 EXPORTS = ("medusa_workspace_bytes", "medusa_tree_size", "medusa_heads_topk", "medusa_tree_build",
            "medusa_tree_attn", "medusa_verify_accept", "medusa_step", "medusa_step_profiled",
            "medusa_step_launches", "medusa_get_device_error", "medusa_status_string",
-           "medusa_heads_topk_noalloc")
+           "medusa_heads_topk_noalloc", "medusa_check_bounded_wait")
 STEP_KERNELS = ("head_layer", "head_proj_topk", "tree_build", "tree_attn", "verify_proj", "accept")
 
 
@@ -81,6 +81,7 @@ def lib() -> ctypes.CDLL:
         L.medusa_get_device_error.argtypes = [vp, i32p, vp]
         L.medusa_step_launches.argtypes = [cfgp]
         L.medusa_heads_topk_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp]
+        L.medusa_check_bounded_wait.argtypes = [vp, ctypes.c_int32, vp]
         L.medusa_status_string.argtypes = [ctypes.c_int]
         L.medusa_status_string.restype = ctypes.c_char_p
         for f in EXPORTS:
@@ -230,6 +231,10 @@ def medusa_get_device_error(ws, stream=None) -> int:
     code = ctypes.c_int32()
     _check("medusa_get_device_error", lib().medusa_get_device_error(_p(ws), ctypes.byref(code), _stream(stream)))
     return code.value
+
+
+def medusa_check_bounded_wait(ws, budget_us: int, stream=None) -> None:
+    _check("medusa_check_bounded_wait", lib().medusa_check_bounded_wait(_p(ws), budget_us, _stream(stream)))
 
 
 def step_launches(cfg: Config) -> int:

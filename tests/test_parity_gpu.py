@@ -132,6 +132,23 @@ def test_out_of_range_token_sets_device_error():
     assert M.medusa_get_device_error(ws) == 0  # read clears it
 
 
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """Failure detection without a fault: a wait on an mbarrier nothing
+    completes gives up after its budget, records MEDUSA_ERR_TIMEOUT, and the
+    context keeps working (a full step afterwards matches the oracle)."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs("7b-mini")
+    cfg = M.make_config(s)
+    ws = M.alloc_workspace(cfg)
+    M.medusa_check_bounded_wait(ws, 2000)
+    torch.cuda.synchronize()
+    assert M.medusa_get_device_error(ws) == -4
+    assert M.medusa_get_device_error(ws) == 0
+    ref = O.step(U.np_inputs(inp), s)
+    res = U.gpu_step(s, U.to_device(inp))
+    U.compare_step(s, res, ref)
+
+
 def _sample_nodes(s, plan, b, rng, extra=4):
     planted = [p[0] for p in plan["seqs"][b]["plant"]]
     rand = rng.choice(s.n_nodes, size=min(extra, s.n_nodes), replace=False).tolist()
