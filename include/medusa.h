@@ -177,7 +177,8 @@ int medusa_heads_topk_noalloc(const medusa_config_t* cfg, const void* h, const v
  *   o = sum_j softmax_j(q.k_j / sqrt(Dh)) v_j
  * over the L cache rows and the tree nodes j with mask[i] bit j.
  * attn_out [B][T][H] holds o of q head h at columns h*Dh .. h*Dh+Dh-1, in the
- * config's dtype.  Only tree->mask is read. */
+ * config's dtype.  Only tree->mask is read (the bf16 kernel derives the same
+ * ancestor-or-self relation from the config's Cartesian layout). */
 int medusa_tree_attn(const medusa_config_t* cfg, const void* q, const void* k_tree, const void* v_tree,
                      const void* k_cache, const void* v_cache, const medusa_tree_t* tree, void* attn_out,
                      void* workspace, void* stream);

@@ -139,13 +139,13 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
 }
 
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                         const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st);
+                         void* out, uint8_t* ws, cudaStream_t st, bool overlap);
 
 // bf16: tensor-core kernel (attn_mma.cu); fp32: this CUDA-core kernel (no TF32)
 int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
                      const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st) {
   (void)ws;
-  if (p.bf16) return launch_tree_attn_mma(p, q, kt, vt, kc, vc, mask, out, ws, st);
+  if (p.bf16) return launch_tree_attn_mma(p, q, kt, vt, kc, vc, out, ws, st, false);
   AttnArgs a;
   a.q = q;
   a.kt = kt;

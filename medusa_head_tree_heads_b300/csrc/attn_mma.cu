@@ -28,7 +28,7 @@ constexpr int AM_KB = 64;  // keys per block
 
 struct AmArgs {
   const __nv_bfloat16 *q, *kt, *vt, *kc, *vc;
-  const uint32_t* mask;
+  TreeDims td;  // the Cartesian tree: each CTA derives its rows' ancestor masks from it
   __nv_bfloat16* out;
   int B, T, W, Hq, Hkv, G, L, Lc, H;
   int NS;          // key splits per (b, g): 1 = no split, else NS-1 cache chunks + the tree
@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
   extern __shared__ float4 am_smem[];
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(am_smem);  // [S][AM_KB][LD]
   __nv_bfloat16* Vs = Ks + S * AM_KB * LD;                          // [S][AM_KB][LD]
+  uint32_t* mrow = reinterpret_cast<uint32_t*>(Vs + S * AM_KB * LD);  // [16*NW][W] ancestor-or-self bits
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;  // mma group / thread-in-group
@@ -87,7 +88,27 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
   const int nrows = a.T * a.G;
   const int rbase = blockIdx.x * 16 * NW + warp * 16;
   const size_t kv_row = (size_t)a.Hkv * DH;  // elements between consecutive keys
-  pdl_trigger();  // (pdl_wait comes before the first read of the tree mask)
+  pdl_trigger();
+  // Ancestor-or-self mask rows of this CTA's query rows, from the closed-form
+  // layout (level d starts at off[d]; local index m has parent off[d-1] + m / k_d).
+  // The kernel reads nothing an earlier kernel of the step writes.
+  for (int rr = threadIdx.x; rr < 16 * NW; rr += NT) {
+    const int r = blockIdx.x * 16 * NW + rr;
+    uint32_t* mr = mrow + (size_t)rr * a.W;
+    for (int w = 0; w < a.W; ++w) mr[w] = 0u;
+    if (r < nrows) {
+      int j = r / a.G, d = 0;
+      for (int e = 1; e <= a.td.D; ++e)
+        if (j >= a.td.off[e]) d = e;
+      while (true) {
+        mr[j >> 5] |= 1u << (j & 31);
+        if (d == 0) break;
+        j = d == 1 ? 0 : a.td.off[d - 1] + (j - a.td.off[d]) / a.td.k[d];
+        --d;
+      }
+    }
+  }
+  __syncthreads();
 
   // ---- Q fragments (rows gq and gq+8 of this warp), scale folded in later
   uint32_t qf[KS][4];
@@ -112,7 +133,7 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
   float o[ND][4];
 #pragma unroll
   for (int j = 0; j < ND; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  float mrow_m[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
   const int nb_cache = (a.L + AM_KB - 1) / AM_KB;
   const int nb_tree = (a.T + AM_KB - 1) / AM_KB;
@@ -183,13 +204,13 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
     // ---- mask, scale, online softmax (rows gq and gq+8)
     uint32_t mw[2][2] = {{0u, 0u}, {0u, 0u}};
     if (tree) {
-      pdl_wait();  // the mask is written by the tree-build kernel
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr)
         if (node[hr] >= 0) {
           const int w0 = k0 >> 5;
-          mw[hr][0] = a.mask[(size_t)node[hr] * a.W + w0];
-          mw[hr][1] = (w0 + 1 < a.W) ? a.mask[(size_t)node[hr] * a.W + w0 + 1] : 0u;
+          const uint32_t* mr = mrow + (size_t)(warp * 16 + gq + hr * 8) * a.W;
+          mw[hr][0] = mr[w0];
+          mw[hr][1] = (w0 + 1 < a.W) ? mr[w0 + 1] : 0u;
         }
     }
     float mx[2] = {-INFINITY, -INFINITY};
@@ -210,10 +231,10 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
     for (int hr = 0; hr < 2; ++hr) {
       mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
       mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-      const float mn = fmaxf(mrow[hr], mx[hr]);
+      const float mn = fmaxf(mrow_m[hr], mx[hr]);
       // mn == -inf: nothing visible yet for this row; keep everything at zero
-      corr[hr] = (mn == -INFINITY) ? 1.f : exp2f(mrow[hr] - mn);
-      mrow[hr] = mn;
+      corr[hr] = (mn == -INFINITY) ? 1.f : exp2f(mrow_m[hr] - mn);
+      mrow_m[hr] = mn;
     }
     float ls[2] = {0.f, 0.f};
     uint32_t pf[4][4];  // A fragments of P for the 4 k-steps of P V
@@ -223,7 +244,7 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int hr = e >> 1;
-        p[e] = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - mrow[hr]);
+        p[e] = (s[nt][e] == -INFINITY) ? 0.f : exp2f(s[nt][e] - mrow_m[hr]);
         ls[hr] += p[e];
       }
       const int kk2 = nt >> 1, half = nt & 1;
@@ -274,8 +295,9 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
 #pragma unroll
       for (int j = 0; j < ND; ++j)
         *reinterpret_cast<float2*>(po + j * 8 + 2 * tq) = make_float2(o[j][hr * 2], o[j][hr * 2 + 1]);
-      if (tq == 0) a.part_ml[pr] = make_float2(mrow[hr], lrow[hr]);
+      if (tq == 0) a.part_ml[pr] = make_float2(mrow_m[hr], lrow[hr]);
     }
+    pdl_wait();  // completes only after the preceding kernel (keeps the stream's order transitive)
     return;
   }
 #pragma unroll
@@ -289,6 +311,7 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
     for (int j = 0; j < ND; ++j)
       *reinterpret_cast<uint32_t*>(op + j * 8 + 2 * tq) = pack_bf16(o[j][hr * 2] * inv, o[j][hr * 2 + 1] * inv);
   }
+  pdl_wait();  // completes only after the preceding kernel (keeps the stream's order transitive)
 }
 
 // Merges the NS partials of every (b, q head, node): one warp per row.
@@ -362,15 +385,18 @@ size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh) {
   return rows * Dh * sizeof(float) + rows * sizeof(float2) + 256;
 }
 
+// overlap: launched (with programmatic dependent launch) right after the head
+// projection, sized to share the projection's SMs (4 warps, 2-block ring, no
+// key split); otherwise a plain stream-ordered launch sized for the whole GPU.
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                         const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st) {
+                         void* out, uint8_t* ws, cudaStream_t st, bool overlap) {
   AmArgs a;
   a.q = (const __nv_bfloat16*)q;
   a.kt = (const __nv_bfloat16*)kt;
   a.vt = (const __nv_bfloat16*)vt;
   a.kc = (const __nv_bfloat16*)(kc ? kc : kt);
   a.vc = (const __nv_bfloat16*)(vc ? vc : vt);
-  a.mask = mask;
+  a.td = p.tree;
   a.out = (__nv_bfloat16*)out;
   a.B = p.B;
   a.T = p.T;
@@ -383,17 +409,22 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   a.H = p.H;
   a.qscale = 1.4426950408889634f / sqrtf((float)p.Dh);
   attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &a.NS, &a.chunk_blks);
+  if (overlap) {
+    a.NS = 1;
+    a.chunk_blks = (p.L + AM_KB - 1) / AM_KB;
+  }
   const size_t rows_all = (size_t)p.B * p.Hq * p.T * a.NS;
   a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);
   a.part_ml = reinterpret_cast<float2*>(ws + p.off_attn_part + rows_all * p.Dh * sizeof(float));
   const int rows = p.T * p.G;
-  const int nw = attn_warps(rows);
+  const int nw = overlap ? 4 : attn_warps(rows);
   dim3 grid((rows + 16 * nw - 1) / (16 * nw), p.Hkv * a.NS, p.B);
   // a 4-block ring (one CTA per SM) when the grid is a single wave, else a
   // 2-block ring so that several CTAs share an SM
   const int ctas = (int)(grid.x * grid.y * grid.z);
-  const int S = ctas <= p.sm_count ? 4 : 2;
-  const size_t smem = (size_t)2 * S * AM_KB * (p.Dh + 8) * sizeof(__nv_bfloat16);
+  const int S = (!overlap && ctas <= p.sm_count) ? 4 : 2;
+  const size_t smem = (size_t)2 * S * AM_KB * (p.Dh + 8) * sizeof(__nv_bfloat16) +
+                      (size_t)16 * nw * p.W * sizeof(uint32_t);
   void (*k)(AmArgs) = nullptr;
 #define AM_PICK(D, W, SS) \
   if (p.Dh == D && nw == W && S == SS) k = tree_attn_mma_kernel<D, W, SS>;
@@ -404,7 +435,7 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   if (!k) return (int)cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  e = launch_k(k, grid, dim3(nw * 32), smem, st, true, a);
+  e = launch_k(k, grid, dim3(nw * 32), smem, st, overlap, a);
   if (e != cudaSuccess || a.NS == 1) return (int)e;
   const size_t nrow = (size_t)p.B * p.Hq * p.T;
   const unsigned cgrid = (unsigned)((nrow + 7) / 8);

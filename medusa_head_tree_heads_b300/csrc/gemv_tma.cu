@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(GtArgs a) {
 // Returns cudaErrorNotSupported when the shape is outside this kernel's range
 // (the caller then uses the general streaming kernel).
 template <int EPI>
-static int gemv_tma_launch(GtArgs a, int sm_count, int nc, cudaStream_t st, int* ctas_out) {
+static int gemv_tma_launch(GtArgs a, int sm_count, int nc, cudaStream_t st, int* ctas_out, int max_stages = 8) {
   const int nvec = a.H / 8;
   const int vpl = (nvec + GT_CONS - 1) / GT_CONS;
   if (vpl > 4 || nc > 4 || a.C > nc) return (int)cudaErrorNotSupported;
@@ -382,7 +382,7 @@ static int gemv_tma_launch(GtArgs a, int sm_count, int nc, cudaStream_t st, int*
   const size_t stage = (size_t)GT_RB * a.H * 2;
   const size_t fixed = 128 + (EPI == 1 ? (size_t)nc * GT_ROWBUF * 4 : 0) + 2 * 8 * 32 * 4 + 512;
   int S = (int)((220 * 1024 - fixed) / stage);
-  if (S > 8) S = 8;
+  if (S > max_stages) S = max_stages;
   if (S < 2) return (int)cudaErrorNotSupported;
   a.stages = S;
   const size_t smem = fixed + (size_t)S * stage;
@@ -430,6 +430,31 @@ int launch_fc_tma(const Plan& p, const void* h, const void* W1, const void* b1, 
 
 int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc,
                       cudaStream_t st);
+
+// The projection kernel alone (its candidates merged later by launch_topk_merge);
+// max_stages bounds the shared ring so another kernel can share the SM.
+int launch_proj_tma_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t st, int max_stages, int* ctas,
+                         int* rpc) {
+  GtArgs a{};
+  a.W = reinterpret_cast<const __nv_bfloat16*>(W2);
+  a.x = ws + p.off_z;
+  a.x_f32 = 1;
+  a.x_cs = (long long)p.K * p.H;
+  a.x_ss = p.H;
+  a.R = p.K * p.V;
+  a.S = p.V;
+  a.H = p.H;
+  a.C = p.B;
+  a.nseg = p.K;
+  a.ws = ws;
+  a.kmax = p.kmax;
+  for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) a.topk_n[k] = p.topk_n[k];
+  a.cand_val = reinterpret_cast<float*>(ws + p.off_cand_val);
+  a.cand_idx = reinterpret_cast<int*>(ws + p.off_cand_idx);
+  a.cand_seg = reinterpret_cast<int*>(ws + p.off_cand_seg);
+  *rpc = (a.R + p.sm_count - 1) / p.sm_count;
+  return gemv_tma_launch<1>(a, p.sm_count, gt_nc(p.B), st, ctas, max_stages);
+}
 
 int launch_proj_tma(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                     cudaStream_t st) {

@@ -56,6 +56,27 @@ def test_stage_calls_equal_fused_step(name):
                                b[k].view(torch.int8) if b[k].dtype == torch.bfloat16 else b[k]), k
 
 
+@pytest.mark.parametrize("name", ["7b-mini", "33b-mini"])
+def test_profiled_step_equals_step(name):
+    """medusa_step_profiled (sequential stage order, events between stages)
+    gives the same results as medusa_step (overlapped order)."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs(name)
+    d = U.to_device(inp)
+    cfg = M.make_config(s)
+    ws = M.alloc_workspace(cfg)
+    a, b = M.alloc_outputs(cfg), M.alloc_outputs(cfg)
+    M.medusa_step(cfg, M.step_io(d, a), ws)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(M.STEP_KERNELS))]
+    for e in evs:
+        e.record()
+    M.medusa_step_profiled(cfg, M.step_io(d, b), ws, evs)
+    torch.cuda.synchronize()
+    for k in ("topk_idx", "node_argmax", "accept_len", "acc_nodes", "bonus", "node_maxlogit"):
+        assert torch.equal(a[k], b[k]), k
+    assert torch.equal(a["attn_out"].view(torch.int16), b["attn_out"].view(torch.int16))
+
+
 @pytest.mark.parametrize("name", ["7b-mini", "gqa-mini"])
 def test_repeated_steps_are_identical(name):
     """The workspace tickets reset themselves: back-to-back steps agree bitwise."""
