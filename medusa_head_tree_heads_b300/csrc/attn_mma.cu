@@ -435,6 +435,8 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   if (!k) return (int)cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return (int)e;
   e = launch_k(k, grid, dim3(nw * 32), smem, st, overlap, a);
   if (e != cudaSuccess || a.NS == 1) return (int)e;
   const size_t nrow = (size_t)p.B * p.Hq * p.T;

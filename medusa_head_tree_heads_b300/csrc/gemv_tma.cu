@@ -396,6 +396,10 @@ static int gemv_tma_launch(GtArgs a, int sm_count, int nc, cudaStream_t st, int*
   if (!k) return (int)cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
+  // the whole unified L1/shared array as shared memory, so that a kernel
+  // co-scheduled on the same SM (the tree attention) finds room beside this one
+  e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return (int)e;
   if (ctas_out) *ctas_out = ctas;
   return (int)launch_k(k, dim3(ctas), dim3(GT_THREADS), smem, st, EPI == 1, a);
 }
