@@ -209,9 +209,11 @@ int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* wo
  * graph) of events[2k] just before and events[2k+1] just after stage k
  * (events: host array of n_events >= 2 * MEDUSA_STEP_KERNELS cudaEvent_t
  * created by the caller).  Stages, each one or two kernel launches: 0 head
- * layer, 1 head projection + top-k (stream kernel, candidate merge), 2 tree
- * build, 3 tree attention (+ split combine), 4 verification projection
- * (+ partial merge), 5 acceptance. */
+ * layer, 1 head projection (at batch <= 4 with bf16 the streaming kernel
+ * alone; otherwise with its top-k candidate merge), 2 tree build (at batch
+ * <= 4 with bf16 fused with the top-k candidate merge), 3 tree attention
+ * (+ split combine), 4 verification projection (+ partial merge),
+ * 5 acceptance. */
 #define MEDUSA_STEP_KERNELS 6
 int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
                          void* const* events, int32_t n_events);

@@ -14,6 +14,8 @@ int launch_proj_tma_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_
                          int* rpc);
 int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc,
                       cudaStream_t st);
+int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
+                      const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, cudaStream_t st);
 int launch_fc_tma(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
 int launch_proj_tma(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                     cudaStream_t st);
@@ -270,27 +272,6 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   finish_plan(&p);
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = (uint8_t*)workspace;
-  if (!events && p.bf16 && gemv_tma_supported(p)) {
-    // Overlapped order: the tree attention depends on no other kernel of the
-    // step, so it is launched right behind the HBM-bound head projection and
-    // shares its SMs (the projection keeps a 4-stage ring to leave room);
-    // every later kernel waits for its predecessor, so the order stays
-    // transitive (the attention waits for the projection before it completes).
-    int ctas = 0, rpc = 0, e;
-    if ((e = launch_head_layer(p, io->h, io->W1, io->b1, ws, st))) return cuda_status(e);
-    if ((e = launch_proj_tma_only(p, io->W2, ws, st, 4, &ctas, &rpc))) return cuda_status(e);
-    if ((e = launch_tree_attn_mma(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->attn_out, ws, st,
-                                  true)))
-      return cuda_status(e);
-    if ((e = launch_topk_merge(p, io->topk_idx, io->topk_val, ws, ctas, rpc, st))) return cuda_status(e);
-    if ((e = launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))) return cuda_status(e);
-    if ((e = launch_verify(p, io->attn_out, io->lm_head, io->node_argmax, io->node_maxlogit, io->node_lse,
-                           io->node_entropy, ws, st)))
-      return cuda_status(e);
-    return cuda_status(launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse,
-                                     io->node_entropy, io->accept_len, io->acc_tokens, io->acc_nodes, io->bonus, ws,
-                                     st));
-  }
   int k = 0, e = 0;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (events && cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MEDUSA_ERR_CUDA;
@@ -307,8 +288,16 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   ++k;                      \
   if (e) return cuda_status(e);
   MEDUSA_STAGE(launch_head_layer(p, io->h, io->W1, io->b1, ws, st))
-  MEDUSA_STAGE(launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
-  MEDUSA_STAGE(launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
+  if (gemv_tma_supported(p)) {
+    // small batch: the projection kernel alone, then one kernel for the
+    // candidate merge and the tree
+    int ctas = 0, rpc = 0;
+    MEDUSA_STAGE(launch_proj_tma_only(p, io->W2, ws, st, 8, &ctas, &rpc))
+    MEDUSA_STAGE(launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, rpc, st))
+  } else {
+    MEDUSA_STAGE(launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
+    MEDUSA_STAGE(launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
+  }
   MEDUSA_STAGE(launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->tree.mask,
                                 io->attn_out, ws, st))
   MEDUSA_STAGE(launch_verify(p, io->attn_out, io->lm_head, io->node_argmax, io->node_maxlogit, io->node_lse,
@@ -345,12 +334,11 @@ int medusa_step_launches(const medusa_config_t* cfg) {
   if (s != MEDUSA_OK) return s;
   finish_plan(&p);
   int n = 6;                        // one launch per stage
-  n += 1;                           // top-k candidate merge
+  if (!gemv_tma_supported(p)) n += 1;  // separate top-k candidate merge (else fused with the tree)
   if (p.bf16) {
     int NS, cb;
     attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &NS, &cb);
-    // the overlapped order (small batch) runs the attention unsplit
-    if (NS > 1 && !gemv_tma_supported(p)) n += 1;  // split-attention combine
+    if (NS > 1) n += 1;             // split-attention combine
     n += 1;                         // verification partial merge
   }
   return n;

@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
     const int nk = tree ? min(AM_KB, a.T - k0) : min(AM_KB, a.L - k0);
     const __nv_bfloat16* Kb = Ks + (size_t)buf * AM_KB * LD;
     const __nv_bfloat16* Vb = Vs + (size_t)buf * AM_KB * LD;
+    if (rbase >= nrows) {  // all 16 rows of this warp are padding: no math, keep the barriers
+      __syncthreads();
+      continue;
+    }
 
     // ---- S = Q K^T for 64 keys: 8 n-tiles of 8 keys
     float s[8][4];

@@ -81,6 +81,177 @@ __global__ void tree_build_kernel(TreeArgs a) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused step: final per-head top-k merge and the tree in one kernel, one CTA
+// per sequence.  Warp k merges head k's per-CTA candidate lists (written by
+// the projection kernel: cand[cta][piece][sequence][kmax], the piece's head
+// in cand_seg[cta][piece]); every slot's loads are issued before any is
+// used.  The merged lists go to the topk outputs and to shared memory, from
+// which the same CTA fills the sequence's tree tokens; CTA 0 also writes the
+// sequence-independent arrays.
+struct MergeTreeArgs {
+  TreeArgs t;
+  int S, rpc, nctas;  // rows per head, rows per projection CTA, projection CTAs
+  int topk_n[MEDUSA_MAX_HEADS];
+  const float* cand_val;
+  const int* cand_idx;
+  const int* cand_seg;
+  int32_t* out_idx;  // [B][K][kmax]
+  float* out_val;
+};
+
+__device__ __forceinline__ bool mt_better(float v, int i, float w, int j) { return v > w || (v == w && i < j); }
+
+template <int KM>
+__global__ void __launch_bounds__(256) merge_tree_kernel(MergeTreeArgs a) {
+  __shared__ int s_idx[MEDUSA_MAX_HEADS][MEDUSA_MAX_TOPK];
+  const TreeArgs& ta = a.t;
+  const TreeDims& td = ta.td;
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();  // the candidates come from the projection kernel
+  if (warp < ta.K) {
+    const int seg = warp;
+    int kn = 1;
+#pragma unroll
+    for (int k = 0; k < MEDUSA_MAX_HEADS; ++k)
+      if (k == seg) kn = a.topk_n[k];
+    const int b_lo = (int)(((long long)seg * a.S) / a.rpc);
+    const int b_hi = min(a.nctas - 1, (int)(((long long)(seg + 1) * a.S - 1) / a.rpc));
+    const int n_slots = (b_hi - b_lo + 1) * kMaxPieces;
+    float lv[KM];
+    int li[KM];
+#pragma unroll
+    for (int i = 0; i < KM; ++i) {
+      lv[i] = -INFINITY;
+      li[i] = INT_MAX;
+    }
+    for (int sl0 = 0; sl0 < n_slots; sl0 += 32 * 4) {
+      int sg[4];
+      float cv[4][KM];
+      int ci[4][KM];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {  // all loads of this round first
+        const int sl = sl0 + u * 32 + lane;
+        const bool in = sl < n_slots;
+        const int blk = b_lo + sl / kMaxPieces, pc = sl % kMaxPieces;
+        sg[u] = in ? a.cand_seg[blk * kMaxPieces + pc] : -1;
+        const size_t base = ((size_t)(blk * kMaxPieces + pc) * ta.B + b) * ta.kmax;
+#pragma unroll
+        for (int i = 0; i < KM; ++i) {
+          const bool ok = in && i < kn;
+          cv[u][i] = ok ? a.cand_val[base + i] : -INFINITY;
+          ci[u][i] = ok ? a.cand_idx[base + i] : INT_MAX;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (sg[u] != seg) continue;
+#pragma unroll
+        for (int i = 0; i < KM; ++i) {  // compare-and-swap insertion of candidate i
+          float v = cv[u][i];
+          int id = ci[u][i];
+#pragma unroll
+          for (int j = 0; j < KM; ++j) {
+            const bool sw = (j < kn) && mt_better(v, id, lv[j], li[j]);
+            const float ov = lv[j];
+            const int oi = li[j];
+            lv[j] = sw ? v : ov;
+            li[j] = sw ? id : oi;
+            v = sw ? ov : v;
+            id = sw ? oi : id;
+          }
+        }
+      }
+    }
+    // warp-wide top-kn: the best list head wins each round, its owner pops
+    for (int rnk = 0; rnk < ta.kmax; ++rnk) {
+      float bv = lv[0];
+      int bi = li[0];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (mt_better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (bi != INT_MAX && lv[0] == bv && li[0] == bi) {
+#pragma unroll
+        for (int i = 0; i < KM - 1; ++i) {
+          lv[i] = lv[i + 1];
+          li[i] = li[i + 1];
+        }
+        lv[KM - 1] = -INFINITY;
+        li[KM - 1] = INT_MAX;
+      }
+      if (lane == 0) {
+        const bool live = rnk < kn && bi != INT_MAX;
+        const size_t o = ((size_t)b * ta.K + seg) * ta.kmax + rnk;
+        a.out_idx[o] = live ? bi : -1;
+        a.out_val[o] = live ? bv : -INFINITY;
+        s_idx[seg][rnk] = live ? bi : -1;
+      }
+    }
+  }
+  __syncthreads();
+  const int T = td.T;
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    const int d = node_depth(td, i);
+    ta.t.token[(size_t)b * T + i] = d == 0 ? ta.root[b] : s_idx[d - 1][(i - td.off[d]) % td.k[d]];
+    if (b == 0) {
+      ta.t.depth[i] = d;
+      ta.t.parent[i] = node_parent(td, i, d);
+      ta.t.rank[i] = d == 0 ? 0 : (i - td.off[d]) % td.k[d];
+      ta.t.pos[i] = ta.L + d;
+      for (int w = 0; w < td.W; ++w) {
+        uint32_t word = 0;
+        int j = i, dj = d;
+        while (j >= 0) {
+          if ((j >> 5) == w) word |= 1u << (j & 31);
+          j = node_parent(td, j, dj);
+          dj -= 1;
+        }
+        ta.t.mask[(size_t)i * td.W + w] = word;
+      }
+    }
+  }
+  if (b == 0)
+    for (int l = threadIdx.x; l < td.n_leaves; l += blockDim.x) {
+      int j = td.off[td.D] + l;
+      for (int d = td.D; d >= 0; --d) {
+        ta.t.paths[(size_t)l * (td.D + 1) + d] = j;
+        j = node_parent(td, j, d);
+      }
+    }
+}
+
+int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
+                      const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, cudaStream_t st) {
+  MergeTreeArgs a;
+  a.t.td = p.tree;
+  a.t.B = p.B;
+  a.t.K = p.K;
+  a.t.kmax = p.kmax;
+  a.t.L = p.L;
+  a.t.topk_idx = topk_idx;
+  a.t.root = root;
+  a.t.t = t;
+  a.S = p.V;
+  a.rpc = rpc;
+  a.nctas = nctas;
+  for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) a.topk_n[k] = p.topk_n[k];
+  a.cand_val = reinterpret_cast<const float*>(ws + p.off_cand_val);
+  a.cand_idx = reinterpret_cast<const int*>(ws + p.off_cand_idx);
+  a.cand_seg = reinterpret_cast<const int*>(ws + p.off_cand_seg);
+  a.out_idx = topk_idx;
+  a.out_val = topk_val;
+  if (p.kmax <= 4) return (int)launch_k(merge_tree_kernel<4>, dim3(p.B), dim3(256), 0, st, true, a);
+  if (p.kmax <= 8) return (int)launch_k(merge_tree_kernel<8>, dim3(p.B), dim3(256), 0, st, true, a);
+  return (int)launch_k(merge_tree_kernel<MEDUSA_MAX_TOPK>, dim3(p.B), dim3(256), 0, st, true, a);
+}
+
 int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* root, const medusa_tree_t& t,
                       cudaStream_t st) {
   TreeArgs a;

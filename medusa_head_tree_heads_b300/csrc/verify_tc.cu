@@ -17,10 +17,11 @@
 // (one per SM):
 //   warp 0      TMA producer (one thread), S-stage smem ring
 //   warp 1      TMEM allocator + MMA issuer (one thread)
-//   warps 2..5  epilogue: tcgen05.ld 16 columns at a time; per column a
+//   warps 2..9  epilogue (two per TMEM lane quadrant, columns split in
+//               groups of 64): tcgen05.ld 16 columns at a time; per column a
 //               butterfly "transpose-reduce" across the 32 rows of the warp
 //               (16 exchange rounds per 16 columns instead of 5 per column),
-//               then the 4 warps combine in shared memory and write one
+//               then the warps combine in shared memory and write one
 //               partial (max, sum e, sum e*t, argmax) per (vocab tile, node).
 // A second small kernel merges the vocab-tile partials, one warp per node.
 // Every wait is bounded; on a timeout the kernel sets MEDUSA_ERR_TIMEOUT,
@@ -35,7 +36,8 @@ namespace medusa {
 constexpr int VT_M = 128;       // vocab rows per MMA (M)
 constexpr int VT_SUB = 2;       // MMA halves per tile: a tile is VT_SUB * VT_M vocab rows
 constexpr int VT_BK = 64;       // K elements per stage (128 bytes of bf16)
-constexpr int VT_THREADS = 192; // 6 warps
+constexpr int VT_EPI_WARPS = 8;  // two warps per TMEM lane quadrant, each taking half the columns
+constexpr int VT_THREADS = 64 + 32 * VT_EPI_WARPS;
 constexpr uint32_t VT_TMEM_COLS = 512;
 constexpr uint64_t VT_WAIT_NS = 20ull * 1000 * 1000;  // 20 ms per wait
 
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       tc::mbar_init(&empty[s], 1);
     }
     tc::mbar_init(&tfull[0], 1);
-    tc::mbar_init(&tempty[0], 4);
+    tc::mbar_init(&tempty[0], VT_EPI_WARPS);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -302,10 +304,12 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       const uint32_t aph = tl & 1u;
       // one thread waits, the named barrier hands its verdict to all 128
       if (etid == 0) *ep_ok = wait_or_abort(&tfull[0], aph, abort_flag, a.ws) ? 1 : 0;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (!*ep_ok) break;
       tc::fence_after_sync();
-      for (int ch0 = 0; ch0 < a.BN / 16; ch0 += 4) {
+      // warps 2..5 take the even groups of 4 chunks, warps 6..9 the odd ones
+      const int half = (warp - 2) >> 2;
+      for (int ch0 = 4 * half; ch0 < a.BN / 16; ch0 += 8) {
         const int nch = min(4, a.BN / 16 - ch0);
         Soft col[4];
 #pragma unroll
@@ -338,8 +342,8 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[0]);  // this warp is done with the accumulators
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      for (int col = etid; col < a.BN; col += 128) {
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      for (int col = etid; col < a.BN; col += 32 * VT_EPI_WARPS) {
         const int n = nt * a.BN + col;
         if (n < a.N) {
           Soft m = red[col];
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
           a.part[(size_t)vt * a.N + n] = make_float4(m.m, m.z, m.s, __int_as_float(m.i));
         }
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
     }
   }
 
