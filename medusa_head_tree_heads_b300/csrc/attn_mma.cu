@@ -138,15 +138,10 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
   const int nb_cache = (a.L + AM_KB - 1) / AM_KB;
   const int nb_tree = (a.T + AM_KB - 1) / AM_KB;
   // this CTA's key blocks [blk_lo, blk_hi) of (cache blocks, then tree blocks)
-  int blk_lo = 0, blk_hi = nb_cache + nb_tree;
-  if (a.NS > 1) {
-    if (sp < a.NS - 1) {
-      blk_lo = min(nb_cache, sp * a.chunk_blks);
-      blk_hi = min(nb_cache, (sp + 1) * a.chunk_blks);
-    } else {
-      blk_lo = nb_cache;
-    }
-  }
+  // split sp takes an equal share of the concatenated (cache, tree) block list
+  const int nb_all = nb_cache + nb_tree;
+  const int blk_lo = (int)(((long long)sp * nb_all) / a.NS);
+  const int blk_hi = (int)(((long long)(sp + 1) * nb_all) / a.NS);
 
   auto load_block = [&](int blk, int buf) {
     const bool tree = blk >= nb_cache;
@@ -361,24 +356,24 @@ static int attn_warps(int rows) {
 
 // Key splits for a shape (device independent, so the workspace can be sized
 // from the config alone): when the (row block, b, kv head) CTAs do not cover
-// the ~148 SMs of a B300, the cache is cut into chunks and the tree becomes
-// one more split, each CTA writing a partial that the combine kernel merges.
+// the ~148 SMs of a B300, the key blocks (cache blocks, then tree blocks) are
+// cut into NS equal shares, each CTA writing a partial that the combine
+// kernel merges.
 void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks) {
   constexpr int kSlots = 148;
   const int rows = T * G;
   const int nw = attn_warps(rows);
   const int row_blocks = (rows + 16 * nw - 1) / (16 * nw);
   const int base = row_blocks * Hkv * B;
-  const int nbc = (L + AM_KB - 1) / AM_KB;
+  const int nb_all = (L + AM_KB - 1) / AM_KB + (T + AM_KB - 1) / AM_KB;
   *NS = 1;
-  *chunk_blks = nbc;
-  if (2 * base > kSlots || nbc == 0) return;
-  int ncs = kSlots / base - 1;  // cache chunks; the tree is one more split
-  if (ncs < 1) ncs = 1;
-  if (ncs > nbc) ncs = nbc;
-  const int cb = (nbc + ncs - 1) / ncs;
-  *chunk_blks = cb;
-  *NS = (nbc + cb - 1) / cb + 1;
+  *chunk_blks = nb_all;
+  if (2 * base > kSlots || L == 0) return;
+  int ns = kSlots / base;
+  if (ns > nb_all) ns = nb_all;
+  if (ns < 2) return;
+  *NS = ns;
+  *chunk_blks = (nb_all + ns - 1) / ns;
 }
 
 size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh) {
@@ -415,7 +410,7 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &a.NS, &a.chunk_blks);
   if (overlap) {
     a.NS = 1;
-    a.chunk_blks = (p.L + AM_KB - 1) / AM_KB;
+    a.chunk_blks = (p.L + AM_KB - 1) / AM_KB + (p.T + AM_KB - 1) / AM_KB;
   }
   const size_t rows_all = (size_t)p.B * p.Hq * p.T * a.NS;
   a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);

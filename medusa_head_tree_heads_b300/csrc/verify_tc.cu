@@ -146,6 +146,13 @@ __device__ __forceinline__ Soft column_reduce(const float (&v)[16], int row, boo
   return o;
 }
 
+// float -> int with the same order (negative floats have their magnitude bits flipped)
+__device__ __forceinline__ int order_key(float x) {
+  const int b = __float_as_int(x);
+  return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float order_key_inv(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               uint8_t* ws) {
   if (tc::mbar_try_wait(bar, parity)) return true;
@@ -311,33 +318,87 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       const int half = (warp - 2) >> 2;
       for (int ch0 = 4 * half; ch0 < a.BN / 16; ch0 += 8) {
         const int nch = min(4, a.BN / 16 - ch0);
-        Soft col[4];
+        if (typical) {
+          Soft col[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) col[c] = soft_empty();
+          for (int c = 0; c < 4; ++c) col[c] = soft_empty();
 #pragma unroll
-        for (int h = 0; h < VT_SUB; ++h) {
-          const int row = (vt * VT_SUB + h) * VT_M + q * 32 + lane;
-          const bool row_ok = row < a.V;
-          float v[4][16];
-          const uint32_t tb = tmem + h * 256 + ((uint32_t)(q * 32) << 16) + ch0 * 16;
+          for (int h = 0; h < VT_SUB; ++h) {
+            const int row = (vt * VT_SUB + h) * VT_M + q * 32 + lane;
+            const bool row_ok = row < a.V;
+            float v[4][16];
+            const uint32_t tb = tmem + h * 256 + ((uint32_t)(q * 32) << 16) + ch0 * 16;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if (c < nch) tc::tmem_ld16_nowait(tb + c * 16, v[c]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tc::tmem_regs_ready(v[c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (c >= nch) break;
+              col[c] = soft_join(col[c], column_reduce<true>(v[c], row, row_ok, lane, a.inv_temp), true,
+                                 a.inv_temp);
+            }
+          }
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            if (c < nch) tc::tmem_ld16_nowait(tb + c * 16, v[c]);
-          tc::tmem_wait_ld();
+            if (c < nch && (lane & 1) == 0) red[q * a.BN + (ch0 + c) * 16 + (lane >> 1)] = col[c];
+        } else {
+          // greedy: per column, the best of this thread's two rows, then a
+          // warp max of an order-preserving integer key and a warp min of the
+          // rows that reach it (ties to the lowest row), both single
+          // instructions (redux.sync)
+          const int row0 = vt * VT_SUB * VT_M + q * 32 + lane;  // half 1 adds VT_M
+          const bool ok0 = row0 < a.V, ok1 = row0 + VT_M < a.V;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tc::tmem_regs_ready(v[c]);
+          for (int cp = 0; cp < 4; cp += 2) {  // two chunks (both halves) per TMEM wait
+            if (cp >= nch) break;
+            float v[VT_SUB][2][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (c >= nch) break;
-            Soft r;
-            if (typical) r = column_reduce<true>(v[c], row, row_ok, lane, a.inv_temp);
-            else r = column_reduce<false>(v[c], row, row_ok, lane, a.inv_temp);
-            col[c] = soft_join(col[c], r, typical, a.inv_temp);
+            for (int h = 0; h < VT_SUB; ++h) {
+              const uint32_t tb = tmem + h * 256 + ((uint32_t)(q * 32) << 16) + (ch0 + cp) * 16;
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                if (cp + c < nch) tc::tmem_ld16_nowait(tb + c * 16, v[h][c]);
+            }
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < VT_SUB; ++h)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) tc::tmem_regs_ready(v[h][c]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              if (cp + c >= nch) break;
+              Soft mine;
+              mine.m = -INFINITY;
+              mine.z = 0.f;
+              mine.s = 0.f;
+              mine.i = INT_MAX;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float x0 = ok0 ? v[0][c][j] : -INFINITY;
+                const float x1 = ok1 ? v[1][c][j] : -INFINITY;
+                const bool one = x1 > x0;  // equal values keep half 0 (the lower row)
+                const float x = one ? x1 : x0;
+                const uint32_t r = ok0 ? (uint32_t)(one ? row0 + VT_M : row0) : 0xffffffffu;
+                const int key = order_key(x);
+                int kmax;
+                asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(kmax) : "r"(key));
+                uint32_t rmin;
+                asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;"
+                             : "=r"(rmin)
+                             : "r"(key == kmax ? r : 0xffffffffu));
+                if (lane == j && rmin != 0xffffffffu) {
+                  mine.m = order_key_inv(kmax);
+                  mine.i = (int)rmin;
+                  mine.z = 1.f;
+                }
+              }
+              if (lane < 16) red[q * a.BN + (ch0 + cp + c) * 16 + lane] = mine;
+            }
           }
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (c < nch && (lane & 1) == 0) red[q * a.BN + (ch0 + c) * 16 + (lane >> 1)] = col[c];
       }
       tc::fence_before_sync();
       __syncwarp();
