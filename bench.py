@@ -53,6 +53,28 @@ def flops(s) -> dict:
             "attn": 4 * B * T * s.n_q_heads * s.head_dim * (s.kv_len + s.depth + 1)}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the dominant kernel, from an ncu capture of the full-size workload, keyed by
+# the SHA-256 of the kernel's source file at capture time: a changed kernel
+# reports null until it is captured again.
+TRAFFIC_CAPTURES = {
+    "7b-bf16": {"source": "medusa_head_tree_heads_b300/csrc/gemv_tma.cu",
+                "sha256": "28890aa391fd11430d695ab99286fd672abacb2d45fdb8db7eef13364951d668",
+                "bytes": 1.31e9 + 2.90e6},
+}
+
+
+def captured_traffic(workload: str):
+    c = TRAFFIC_CAPTURES.get(workload)
+    if c is None:
+        return None
+    import hashlib
+    with open(os.path.join(ROOT, c["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != c["sha256"]:
+            return None
+    return c["bytes"]
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -273,7 +295,8 @@ def run_medusa(args, world, rank, local):
     dom = "head_proj_topk"
     achieved = byts[dom] / (per_kernel[dom] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": captured_traffic(s.name) if dom == "head_proj_topk" else None,
                 "peak_source": peaks["source"], "algorithmic_bytes": byts[dom],
                 "kernel_ms": {k: round(v, 4) for k, v in per_kernel.items()},
                 "step_achieved_gbs": round(byts["step"] / (ms * 1e-3) / 1e9, 1),
