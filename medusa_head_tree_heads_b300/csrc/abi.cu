@@ -12,19 +12,19 @@ bool gemv_tma_supported(const Plan& p);
 int launch_bounded_wait_probe(uint8_t* ws, uint64_t budget_ns, cudaStream_t st);
 int launch_proj_tma_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t st, int max_stages, int* ctas,
                          int* rpc);
-int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc,
-                      cudaStream_t st);
 int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
-                      const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, cudaStream_t st);
+                      const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st);
 int launch_fc_tma(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
 int launch_proj_tma(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                     cudaStream_t st);
 
-// head layer / head projection: the TMA-fed small-batch kernel where it
-// applies (bf16, batch <= 4), else the general streaming kernel
+// head layer / head projection: the TMA-fed streaming kernel where it
+// applies (bf16, batch <= 4), the tensor-core kernel for the other bf16
+// batches up to 32, else the general streaming kernel
 int launch_head_layer(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws,
                              cudaStream_t st) {
   if (gemv_tma_supported(p)) return launch_fc_tma(p, h, W1, b1, ws, st);
+  if (heads_tc_supported(p)) return launch_fc_tc(p, h, W1, b1, ws, st);
   return launch_fc(p, h, W1, b1, ws, st);
 }
 int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
@@ -135,6 +135,15 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   if (p->bf16) o = align_up(o + verify_tc_part_bytes(p->V, p->B * p->T), 256);
   p->off_attn_part = o;
   if (p->bf16) o = align_up(o + attn_part_bytes(p->B, p->T, p->G, p->Hkv, p->L, p->Dh), 256);
+  p->off_zs = p->off_ht_slot = p->off_ht_tickets = o;
+  if (p->bf16 && p->B <= kHeadsTcMaxBatch) {  // the tensor-core heads may run (decided per device)
+    p->off_zs = o;
+    o = align_up(o + heads_tc_zs_bytes(p->K, p->B, p->H), 256);
+    p->off_ht_slot = o;
+    o = align_up(o + heads_tc_slot_bytes(p->B), 256);
+    p->off_ht_tickets = o;
+    o = align_up(o + 2 * kHeadsTcMaxCtas * sizeof(int), 256);
+  }
   p->total = o;
   return MEDUSA_OK;
 }
@@ -153,6 +162,7 @@ void finish_plan(Plan* p) {
 int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                      cudaStream_t st) {
   if (gemv_tma_supported(p)) return launch_proj_tma(p, W2, topk_idx, topk_val, ws, st);
+  if (heads_tc_supported(p)) return launch_proj_tc(p, W2, topk_idx, topk_val, ws, st);
   return launch_proj_topk(p, W2, topk_idx, topk_val, ws, st);
 }
 
@@ -293,7 +303,11 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
     // candidate merge and the tree
     int ctas = 0, rpc = 0;
     MEDUSA_STAGE(launch_proj_tma_only(p, io->W2, ws, st, 8, &ctas, &rpc))
-    MEDUSA_STAGE(launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, rpc, st))
+    MEDUSA_STAGE(launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, rpc, p.V, st))
+  } else if (heads_tc_supported(p)) {
+    int ctas = 0, upc = 0, ups = 0;
+    MEDUSA_STAGE(launch_proj_tc_only(p, io->W2, ws, st, &ctas, &upc, &ups))
+    MEDUSA_STAGE(launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, upc, ups, st))
   } else {
     MEDUSA_STAGE(launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
     MEDUSA_STAGE(launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
@@ -334,7 +348,7 @@ int medusa_step_launches(const medusa_config_t* cfg) {
   if (s != MEDUSA_OK) return s;
   finish_plan(&p);
   int n = 6;                        // one launch per stage
-  if (!gemv_tma_supported(p)) n += 1;  // separate top-k candidate merge (else fused with the tree)
+  if (!gemv_tma_supported(p) && !heads_tc_supported(p)) n += 1;  // separate top-k merge (else fused with the tree)
   if (p.bf16) {
     int NS, cb;
     attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &NS, &cb);

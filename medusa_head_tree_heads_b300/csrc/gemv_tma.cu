@@ -432,7 +432,7 @@ int launch_fc_tma(const Plan& p, const void* h, const void* W1, const void* b1, 
   return gemv_tma_launch<0>(a, p.sm_count, gt_nc(p.B), st, nullptr);
 }
 
-int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc,
+int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc, int S,
                       cudaStream_t st);
 
 // The projection kernel alone (its candidates merged later by launch_topk_merge);
@@ -483,7 +483,7 @@ int launch_proj_tma(const Plan& p, const void* W2, int32_t* topk_idx, float* top
   int e = gemv_tma_launch<1>(a, p.sm_count, gt_nc(p.B), st, &ctas);
   if (e) return e;
   const int rpc = (a.R + p.sm_count - 1) / p.sm_count;
-  return launch_topk_merge(p, topk_idx, topk_val, ws, ctas, rpc, st);
+  return launch_topk_merge(p, topk_idx, topk_val, ws, ctas, rpc, p.V, st);
 }
 
 }  // namespace medusa

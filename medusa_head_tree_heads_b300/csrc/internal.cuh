@@ -15,6 +15,8 @@ constexpr int kThreads = 256;   // threads per CTA of the streaming kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxPieces = 4;   // segments one streaming CTA may touch
 constexpr int kMaxStreamCtas = 1024;  // cap of the persistent streaming grids (workspace sizing)
+constexpr int kHeadsTcMaxCtas = 160;  // cap of the tensor-core heads grids (one CTA per SM)
+constexpr int kHeadsTcMaxBatch = 32;  // largest batch of the tensor-core heads (projection N = 2B <= 64)
 
 // ---------------------------------------------------------------- workspace --
 // [0, 256): int32 error word at 0, tickets from word 8 on.
@@ -37,7 +39,9 @@ struct Plan {
   int sm_count;
   int fc_nc, fc_ctiles, pj_nc, pj_ctiles, vf_nc, vf_ctiles;  // columns per CTA, column tiles
   // workspace offsets (bytes)
-  size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, off_vtc_part, off_attn_part, total;
+  size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, off_vtc_part, off_attn_part;
+  size_t off_zs, off_ht_slot, off_ht_tickets;  // tensor-core heads: z pairs, cut-tile partials, tickets
+  size_t total;
 };
 
 int make_plan(const medusa_config_t* cfg, Plan* p);  // medusa_status_t
@@ -47,6 +51,12 @@ int launch_head_layer(const Plan& p, const void* h, const void* W1, const void* 
 int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                      cudaStream_t st);
 size_t verify_tc_part_bytes(int V, int N);
+size_t heads_tc_zs_bytes(int K, int B, int H);
+size_t heads_tc_slot_bytes(int B);
+bool heads_tc_supported(const Plan& p);  // after finish_plan
+int launch_fc_tc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
+int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t st, int* ctas, int* upc, int* ups);
+int launch_proj_tc(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws, cudaStream_t st);
 size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh);
 void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks);
 int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
@@ -133,6 +143,13 @@ inline cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t s
 __device__ __forceinline__ void set_error(uint8_t* ws, int code) {
   atomicCAS(reinterpret_cast<int*>(ws), 0, code);
 }
+
+// float -> int with the same order (negative floats have their magnitude bits flipped)
+__device__ __forceinline__ int order_key(float x) {
+  const int b = __float_as_int(x);
+  return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float order_key_inv(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
 
 // (value desc, index asc) order used by every top-k / argmax
 __device__ __forceinline__ bool better(float v, int i, float w, int j) { return v > w || (v == w && i < j); }

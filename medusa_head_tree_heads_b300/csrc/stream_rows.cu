@@ -469,11 +469,12 @@ static int launch_nc(RowArgs a, int sm_count, int nc, int ctiles, cudaStream_t s
 }
 
 // Final top-k merge for candidates written by any streaming kernel.
-int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc,
+// CTA c of that kernel covered work units [c * rpc, (c + 1) * rpc), S units per head.
+int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc, int S,
                       cudaStream_t st) {
   RowArgs a{};
-  a.R = p.K * p.V;
-  a.S = p.V;
+  a.R = p.K * S;
+  a.S = S;
   a.H = p.H;
   a.C = p.B;
   a.rpc = rpc;

@@ -91,7 +91,7 @@ __global__ void tree_build_kernel(TreeArgs a) {
 // sequence-independent arrays.
 struct MergeTreeArgs {
   TreeArgs t;
-  int S, rpc, nctas;  // rows per head, rows per projection CTA, projection CTAs
+  int S, rpc, nctas;  // work units per head, units per projection CTA (CTA c has [c*rpc, (c+1)*rpc)), CTAs
   int topk_n[MEDUSA_MAX_HEADS];
   const float* cand_val;
   const int* cand_idx;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(MergeTreeArgs a) {
 }
 
 int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
-                      const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, cudaStream_t st) {
+                      const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st) {
   MergeTreeArgs a;
   a.t.td = p.tree;
   a.t.B = p.B;
@@ -238,7 +238,7 @@ int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const i
   a.t.topk_idx = topk_idx;
   a.t.root = root;
   a.t.t = t;
-  a.S = p.V;
+  a.S = S;
   a.rpc = rpc;
   a.nctas = nctas;
   for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) a.topk_n[k] = p.topk_n[k];

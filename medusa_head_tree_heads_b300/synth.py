@@ -121,6 +121,16 @@ _add(Shape("gqa-mini", "bf16", 512, 4099, 4, 2, (4, 3, 2, 2), 257, 4, 2, 128, "t
 _add(Shape("33b-mini", "bf16", 256, 1500, 5, 3, (4, 3, 2, 2, 2), 129, 2, 2, 128, "greedy", ("uniform", 0, 5), 2004))
 _add(Shape("tiny-fp32-gqa", "f32", 256, 777, 3, 2, (3, 2), 70, 4, 2, 64, "typical", ("uniform", 0, 2), 2005,
            kv_capacity=75))
+# batched reduced variants for the tensor-core heads (batch 5..32): odd batch,
+# a GQA typical batch of 16, a batch of 32 with half-tile hidden and ragged
+# reduction, and 7B-wide heads whose tile counts make the 148-way work split
+# cut tiles between CTAs in both the head layer and the projection
+_add(Shape("b5-mini", "bf16", 256, 777, 3, 5, (3, 2), 70, 2, 1, 128, "greedy", ("uniform", 0, 2), 2006))
+_add(Shape("gqa-b16-mini", "bf16", 512, 4099, 4, 16, (4, 3, 2, 2), 257, 4, 2, 128, "typical", ("uniform", 0, 4), 2007,
+           kv_capacity=260))
+_add(Shape("33b-b32-mini", "bf16", 320, 1500, 5, 32, (4, 3, 2, 2, 2), 129, 5, 5, 64, "greedy", ("uniform", 0, 5), 2008))
+_add(Shape("13b-b8-split", "bf16", 4096, 5000, 5, 8, (3, 2, 2, 1), 200, 32, 32, 128, "greedy", ("uniform", 0, 4), 2009,
+           kv_capacity=211))
 # profiling case: the 7B shapes with a quarter-sized vocabulary (still far
 # larger than L2) so that counter replays stay small
 _add(Shape("7b-prof", "bf16", 4096, 8192, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3), 4001,
