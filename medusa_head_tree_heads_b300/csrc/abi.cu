@@ -352,6 +352,7 @@ int medusa_step_launches(const medusa_config_t* cfg) {
   if (p.bf16) {
     int NS, cb;
     attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &NS, &cb);
+    if (attn_tc_supported(p)) NS = attn_tc_splits(p.B, p.T, p.G, p.Hkv, p.L);
     if (NS > 1) n += 1;             // split-attention combine
     n += 1;                         // verification partial merge
   }

@@ -144,7 +144,7 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
 // bf16: tensor-core kernel (attn_mma.cu); fp32: this CUDA-core kernel (no TF32)
 int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
                      const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st) {
-  (void)ws;
+  if (attn_tc_supported(p)) return launch_tree_attn_tc(p, q, kt, vt, kc, vc, out, ws, st);
   if (p.bf16) return launch_tree_attn_mma(p, q, kt, vt, kc, vc, out, ws, st, false);
   AttnArgs a;
   a.q = q;

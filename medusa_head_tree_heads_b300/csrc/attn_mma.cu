@@ -376,9 +376,14 @@ void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_b
   *chunk_blks = (nb_all + ns - 1) / ns;
 }
 
+// sized for the larger key split of the two bf16 attention kernels
 size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh) {
   int NS, cb;
   attn_split_shape(B, T, G, Hkv, L, &NS, &cb);
+  if (Dh == 128) {
+    const int ns_tc = attn_tc_splits(B, T, G, Hkv, L);
+    if (ns_tc > NS) NS = ns_tc;
+  }
   if (NS == 1) return 0;
   const size_t rows = (size_t)B * Hkv * G * T * NS;
   return rows * Dh * sizeof(float) + rows * sizeof(float2) + 256;
@@ -438,6 +443,24 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   if (e != cudaSuccess) return (int)e;
   e = launch_k(k, grid, dim3(nw * 32), smem, st, overlap, a);
   if (e != cudaSuccess || a.NS == 1) return (int)e;
+  const size_t nrow = (size_t)p.B * p.Hq * p.T;
+  const unsigned cgrid = (unsigned)((nrow + 7) / 8);
+  if (p.Dh == 128) return (int)launch_k(tree_attn_combine_kernel<128>, dim3(cgrid), dim3(256), 0, st, true, a);
+  return (int)launch_k(tree_attn_combine_kernel<64>, dim3(cgrid), dim3(256), 0, st, true, a);
+}
+
+// Merge of NS key-split partials ([B][Hq][T][NS] rows of Dh fp32 plus
+// (max, sum)) written by either attention kernel.
+int launch_attn_combine(const Plan& p, float* part_o, float2* part_ml, int NS, void* out, cudaStream_t st) {
+  AmArgs a{};
+  a.out = (__nv_bfloat16*)out;
+  a.B = p.B;
+  a.T = p.T;
+  a.Hq = p.Hq;
+  a.H = p.H;
+  a.NS = NS;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
   const size_t nrow = (size_t)p.B * p.Hq * p.T;
   const unsigned cgrid = (unsigned)((nrow + 7) / 8);
   if (p.Dh == 128) return (int)launch_k(tree_attn_combine_kernel<128>, dim3(cgrid), dim3(256), 0, st, true, a);

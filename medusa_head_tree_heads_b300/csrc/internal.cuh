@@ -67,6 +67,10 @@ int launch_heads(const Plan& p, const void* h, const void* W1, const void* b1, c
                  float* topk_val, uint8_t* ws, cudaStream_t st);
 int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* root, const medusa_tree_t& t,
                       cudaStream_t st);
+int attn_tc_splits(int B, int T, int G, int Hkv, int L);
+bool attn_tc_supported(const Plan& p);
+int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
+                        void* out, uint8_t* ws, cudaStream_t st);
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
                          void* out, uint8_t* ws, cudaStream_t st, bool overlap);
 int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
