@@ -5,31 +5,30 @@
 //   o[b][i][h] = sum_j softmax_j(q . k_j / sqrt(Dh)) v_j
 //   over cache rows j < L, then tree nodes j set in node i's ancestor mask.
 //
-// A CTA owns 128 query rows of one (sequence b, kv head g): row r is
-// (node r / G, q head g*G + r % G), one TMEM lane each.  Keys stream in
-// blocks of 64 (cache blocks, then tree blocks) through 4-deep K and V TMA
-// rings;
-// the 4-D tensor maps give the key axis the extent L (or T), so rows past
-// the valid keys read as zeros.  Per block:
-//   S = Q K^T     tcgen05.mma M=128, N=64 keys, K=128, into one of two TMEM
-//                 buffers (the MMA of block i+1 runs while block i's softmax
-//                 does)
-//   softmax       8 warps, two threads per row (half the keys each): masked,
-//                 scaled row max from TMEM (halves exchanged through shared
-//                 memory), P = exp2(s - m) packed to bf16 into one of two
-//                 128-byte-swizzled shared tiles (P of block i is written
-//                 while P(i-1) V runs); the running max is only raised (and
-//                 O rescaled in TMEM) when it grows by more than 2^8, so the
-//                 same m serves P, the row sum and the final division
+// A CTA owns up to 256 query rows of one (sequence b, kv head g) as two
+// 128-row tiles (row r is (node r / G, q head g*G + r % G), one TMEM lane of
+// its tile each); both tiles share every K/V block, which streams in blocks
+// of 64 keys (cache blocks, then tree blocks) through 3-deep K and V TMA
+// rings.  The 4-D tensor maps give the key axis the extent L (or T), so rows
+// past the valid keys read as zeros.  Per block and tile:
+//   S = Q K^T     tcgen05.mma M=128, N=64, K=128 into one of two TMEM buffers
+//                 of the tile (block i+1's product runs during block i's
+//                 softmax)
+//   softmax       4 warps per tile, one thread per row (64 scores): masked,
+//                 scaled row max, P = exp2(s - m) packed to bf16 into the
+//                 tile's 128-byte-swizzled P tile.  The running max is only
+//                 raised (and O rescaled in TMEM) when it grows by more than
+//                 2^8, so one m serves P, the row sum and the final division.
+//                 The two tiles' softmax chains are independent and hide each
+//                 other's latency.
 //   O += P V      tcgen05.mma with V as an MN-major operand (the [key][dh]
 //                 tile the TMA wrote), O resident in TMEM for the whole pass.
 // Warp roles (one thread each for the first four, so no issue order couples
 // loads or MMAs that do not depend on one another): warp 0 loads K, warp 1
-// loads V, warp 2 allocates TMEM and issues S = Q K^T, warp 3 issues O += P V;
-// warps 4..11 run the softmax (two per TMEM lane quadrant, each taking half
-// of the keys and of the O columns) and the epilogue.  With fewer (row block, b, g) CTAs than SMs the
-// key blocks are split into NS equal shares (partials merged by the combine
-// kernel).  Every wait is bounded.
+// loads V, warp 2 allocates TMEM and issues S = Q K^T, warp 3 issues O += P V,
+// warps 4..7 and 8..11 run the softmax and epilogue of tiles 0 and 1.  With
+// fewer (row pair, b, g) CTAs than SMs the key blocks are split into NS equal
+// shares (partials merged by the combine kernel).  Every wait is bounded.
 #include <limits.h>
 
 #include "internal.cuh"
@@ -37,21 +36,21 @@
 
 namespace medusa {
 
-constexpr int AT_M = 128;   // query rows per CTA
-constexpr int AT_BK = 64;   // keys per block
-constexpr int AT_KH = AT_BK / 2;  // keys per softmax half
+constexpr int AT_M = 128;            // query rows per tile
+constexpr int AT_TILES = 2;          // tiles per CTA
+constexpr int AT_ROWS = AT_M * AT_TILES;
+constexpr int AT_BK = 64;            // keys per block
 constexpr int AT_DH = 128;
-constexpr int AT_STAGES = 4;  // depth of the K ring and of the V ring
-constexpr int AT_SOFT_WARPS = 8;  // two per TMEM lane quadrant, each taking half of the keys
-constexpr int AT_THREADS = 128 + 32 * AT_SOFT_WARPS;
-constexpr uint32_t AT_QCHUNK = AT_M * 128;          // 16 KB: 128 rows x 64 columns, 128-byte swizzled
-constexpr uint32_t AT_QTILE = 2 * AT_QCHUNK;         // Q: [128 rows][128 dh]
-constexpr uint32_t AT_PTILE = AT_M * AT_BK * 2;      // P: [128 rows][64 keys], one chunk
-constexpr uint32_t AT_KVCHUNK = AT_BK * 128;         // 8 KB: 64 keys x 64 dh
-constexpr uint32_t AT_KVTILE = 2 * AT_KVCHUNK;       // K or V: [64 keys][128 dh]
-constexpr uint32_t AT_TMEM_COLS = 256;               // S0, S1 (64 columns each), O (128)
+constexpr int AT_STAGES = 3;         // depth of the K ring and of the V ring
+constexpr int AT_THREADS = 128 + 32 * 4 * AT_TILES;
+constexpr uint32_t AT_QCHUNK = AT_M * 128;        // 16 KB: 128 rows x 64 columns, 128-byte swizzled
+constexpr uint32_t AT_QTILE = 2 * AT_QCHUNK;      // Q of a tile: [128 rows][128 dh]
+constexpr uint32_t AT_PTILE = AT_M * AT_BK * 2;   // P of a tile: [128 rows][64 keys], one chunk
+constexpr uint32_t AT_KVCHUNK = AT_BK * 128;      // 8 KB: 64 keys x 64 dh
+constexpr uint32_t AT_KVTILE = 2 * AT_KVCHUNK;    // K or V: [64 keys][128 dh]
+constexpr uint32_t AT_TMEM_COLS = 512;            // per tile: S0, S1 (64 columns each); then O of each tile (128)
 constexpr uint64_t AT_WAIT_NS = 20ull * 1000 * 1000;
-constexpr float AT_RESCALE_LOG2 = 8.f;               // raise the running max only past 2^8 growth
+constexpr float AT_RESCALE_LOG2 = 8.f;            // raise the running max only past 2^8 growth
 
 struct AtArgs {
   const __nv_bfloat16* q;
@@ -92,8 +91,9 @@ __device__ __forceinline__ bool at_wait_warp(uint64_t* bar, uint32_t parity, vol
   return __shfl_sync(0xffffffffu, okv, 0) != 0;
 }
 
-// 2^x on the special-function unit (relative error ~2^-22; results below the
-// normal range flush to zero, far below what a bf16 probability resolves)
+// 2^x on the special-function unit (relative error ~2^-22; 2^-inf = 0;
+// results below the normal range flush to zero, far below what a bf16
+// probability resolves)
 __device__ __forceinline__ float at_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -110,29 +110,30 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt, AtArgs a) {
   extern __shared__ uint8_t at_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* Qs = smem;                          // [128 rows][128 dh], swizzled chunks
-  uint8_t* Ps = smem + AT_QTILE;               // [2][128 rows][64 keys]: P of even / odd blocks
-  uint8_t* Ks = Ps + 2 * AT_PTILE;             // [AT_STAGES] K tiles
-  uint8_t* Vs = Ks + AT_STAGES * AT_KVTILE;    // [AT_STAGES] V tiles
-  float* xmax = reinterpret_cast<float*>(Vs + AT_STAGES * AT_KVTILE);  // [2 blocks][2 halves][128] row-max exchange
-  uint32_t* mrow = reinterpret_cast<uint32_t*>(xmax + 4 * AT_M);    // [128][W] ancestor masks
-  uint64_t* bars = reinterpret_cast<uint64_t*>(mrow + AT_M * a.W);  // 128 * W words: 8-byte aligned
+  uint8_t* Qs = smem;                                   // [tile] Q tiles
+  uint8_t* Ps = Qs + AT_TILES * AT_QTILE;               // [tile] P tiles
+  uint8_t* Ks = Ps + AT_TILES * AT_PTILE;               // [AT_STAGES] K tiles
+  uint8_t* Vs = Ks + AT_STAGES * AT_KVTILE;             // [AT_STAGES] V tiles
+  uint32_t* mrow = reinterpret_cast<uint32_t*>(Vs + AT_STAGES * AT_KVTILE);  // [256][W] ancestor masks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mrow + AT_ROWS * a.W);       // 256 * W words: 8-byte aligned
   uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + AT_STAGES;
   uint64_t* v_full = k_empty + AT_STAGES;
   uint64_t* v_empty = v_full + AT_STAGES;
-  uint64_t* s_full = v_empty + AT_STAGES;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 1;  // [2]: P V of even / odd blocks complete
-  uint64_t* q_ready = pv_done + 2;
-  uint64_t* drain = q_ready + 1;  // [2]: S issuer, PV issuer
+  uint64_t* s_full = v_empty + AT_STAGES;    // [tile][2]
+  uint64_t* s_free = s_full + 2 * AT_TILES;  // [tile][2]
+  uint64_t* p_full = s_free + 2 * AT_TILES;  // [tile]
+  uint64_t* pv_done = p_full + AT_TILES;     // [tile]
+  uint64_t* q_ready = pv_done + AT_TILES;
+  uint64_t* drain = q_ready + 1;             // [2]: S issuer, PV issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.y / a.NS, sp = blockIdx.y - g * a.NS, b = blockIdx.z;
   const int nrows = a.T * a.G;
+  const int row0 = blockIdx.x * AT_ROWS;
+  const int ntiles = min(AT_TILES, (nrows - row0 + AT_M - 1) / AT_M);
   const int nb_cache = (a.L + AT_BK - 1) / AT_BK;
   const int nb_all = nb_cache + (a.T + AT_BK - 1) / AT_BK;
   const int blk_lo = (int)(((long long)sp * nb_all) / a.NS);
@@ -146,14 +147,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tc::mbar_init(&v_full[s], 1);
       tc::mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&s_full[s], 1);
-      tc::mbar_init(&s_free[s], AT_SOFT_WARPS);
+    for (int t = 0; t < AT_TILES; ++t) {
+      for (int u = 0; u < 2; ++u) {
+        tc::mbar_init(&s_full[2 * t + u], 1);
+        tc::mbar_init(&s_free[2 * t + u], 4);
+      }
+      tc::mbar_init(&p_full[t], 4);
+      tc::mbar_init(&pv_done[t], 1);
     }
-    tc::mbar_init(p_full, AT_SOFT_WARPS);
-    tc::mbar_init(&pv_done[0], 1);
-    tc::mbar_init(&pv_done[1], 1);
-    tc::mbar_init(q_ready, AT_SOFT_WARPS);
+    tc::mbar_init(q_ready, 4 * AT_TILES);
     tc::mbar_init(&drain[0], 1);
     tc::mbar_init(&drain[1], 1);
     *abort_flag = 0;
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (warp <= 1) {
     // ------------------------------------------------- producers (K: warp 0, V: warp 1)
-    // K(i) waits only for S(i - 2), V(i) for P(i - 2) V: each runs ahead on its own
+    // K(i) waits only for the S products of block i - 3, V(i) for its P V
     if (lane == 0) {
       const bool isv = warp == 1;
       uint64_t* full = isv ? v_full : k_full;
@@ -207,25 +209,30 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // ------------------------------------------------- S = Q K^T issue
     if (lane == 0) {
       const uint32_t idS = tc::idesc_bf16_f32(AT_M, AT_BK);
-      const uint32_t qa = tc::smem_u32(Qs);
       bool ok = at_wait(q_ready, 0, abort_flag, a.ws);
-      for (int i = 0; i < nblk && ok; ++i) {  // S(i) into TMEM buffer i % 2
+      for (int i = 0; i < nblk && ok; ++i) {
         const int s = i % AT_STAGES, buf = i & 1;
-        if (!at_wait(&k_full[s], (i / AT_STAGES) & 1u, abort_flag, a.ws) ||
-            !at_wait(&s_free[buf], ((i >> 1) & 1u) ^ 1u, abort_flag, a.ws)) {
+        if (!at_wait(&k_full[s], (i / AT_STAGES) & 1u, abort_flag, a.ws)) {
           ok = false;
           break;
         }
-        tc::fence_after_sync();
         const uint32_t ka = tc::smem_u32(Ks + (size_t)s * AT_KVTILE);
+        for (int t = 0; t < ntiles && ok; ++t) {  // S(t, i) into TMEM buffer i % 2 of tile t
+          if (!at_wait(&s_free[2 * t + buf], ((i >> 1) & 1u) ^ 1u, abort_flag, a.ws)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t qa = tc::smem_u32(Qs + t * AT_QTILE);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)  // dh chunks
+          for (int c = 0; c < 2; ++c)  // dh chunks
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(tmem + buf * AT_BK, tc::sw128_desc(qa + c * AT_QCHUNK) + 2 * kk,
-                         tc::sw128_desc(ka + c * AT_KVCHUNK) + 2 * kk, idS, (c | kk) != 0);
-        tc::mma_commit(&k_empty[s]);
-        tc::mma_commit(&s_full[buf]);
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_bf16(tmem + t * 2 * AT_BK + buf * AT_BK, tc::sw128_desc(qa + c * AT_QCHUNK) + 2 * kk,
+                           tc::sw128_desc(ka + c * AT_KVCHUNK) + 2 * kk, idS, (c | kk) != 0);
+          tc::mma_commit(&s_full[2 * t + buf]);
+        }
+        if (ok) tc::mma_commit(&k_empty[s]);
       }
       tc::mma_commit(&drain[0]);  // every MMA of this thread completes before TMEM is freed
       const uint64_t t0 = tc::globaltimer_ns();
@@ -236,26 +243,31 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // ------------------------------------------------- O += P V issue
     if (lane == 0) {
       const uint32_t idO = tc::idesc_bf16_f32(AT_M, AT_DH) | (1u << 16);  // V: MN-major B operand
-      const uint32_t pa = tc::smem_u32(Ps);
       bool ok = true;
       for (int i = 0; i < nblk && ok; ++i) {
         const int s = i % AT_STAGES;
-        if (!at_wait(&v_full[s], (i / AT_STAGES) & 1u, abort_flag, a.ws) ||
-            !at_wait(p_full, i & 1u, abort_flag, a.ws)) {
+        if (!at_wait(&v_full[s], (i / AT_STAGES) & 1u, abort_flag, a.ws)) {
           ok = false;
           break;
         }
-        tc::fence_after_sync();
         const uint32_t va = tc::smem_u32(Vs + (size_t)s * AT_KVTILE);
+        for (int t = 0; t < ntiles && ok; ++t) {
+          if (!at_wait(&p_full[t], i & 1u, abort_flag, a.ws)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t pa = tc::smem_u32(Ps + t * AT_PTILE);
 #pragma unroll
-        for (int st = 0; st < AT_BK / 16; ++st) {  // 16 keys per MMA
-          const uint64_t da = tc::sw128_desc(pa + (i & 1) * AT_PTILE) + 2 * st;
-          uint64_t db = tc::sw128_desc(va + st * 2048);
-          db = (db & ~(0x3FFFull << 16)) | ((uint64_t)(AT_KVCHUNK >> 4) << 16);  // dh-chunk stride
-          tc::mma_bf16(tmem + 2 * AT_BK, da, db, idO, (i | st) != 0);
+          for (int st = 0; st < AT_BK / 16; ++st) {  // 16 keys per MMA
+            const uint64_t da = tc::sw128_desc(pa) + 2 * st;
+            uint64_t db = tc::sw128_desc(va + st * 2048);
+            db = (db & ~(0x3FFFull << 16)) | ((uint64_t)(AT_KVCHUNK >> 4) << 16);  // dh-chunk stride
+            tc::mma_bf16(tmem + AT_TILES * 2 * AT_BK + t * AT_DH, da, db, idO, (i | st) != 0);
+          }
+          tc::mma_commit(&pv_done[t]);
         }
-        tc::mma_commit(&v_empty[s]);
-        tc::mma_commit(&pv_done[i & 1]);
+        if (ok) tc::mma_commit(&v_empty[s]);
       }
       tc::mma_commit(&drain[1]);
       const uint64_t t0 = tc::globaltimer_ns();
@@ -263,219 +275,188 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax
-    // warps 4..11: two per TMEM lane quadrant; `half` takes keys (and O
-    // columns) [64 half, 64 half + 64) of the quadrant's 32 rows
-    const int q4 = warp & 3;
-    const int half = (warp - 4) >> 2;
+    // ------------------------------------------------- softmax of tile t
+    const int t = (warp - 4) >> 2;
+    const int q4 = warp & 3;                       // TMEM lane quadrant (warps 4..7 and 8..11 take 0..3)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int trow = q4 * 32 + lane;                 // tile row = TMEM lane
-    const int r = blockIdx.x * AT_M + trow;          // query row
+    const int trow = q4 * 32 + lane;               // row within the tile = TMEM lane
+    const int r = row0 + t * AT_M + trow;          // query row
     const bool rvalid = r < nrows;
     const int node = rvalid ? r / a.G : 0;
     const int hq = g * a.G + (rvalid ? r - node * a.G : 0);
-    // Q row half into the swizzled tile (zeros for padding rows)
+    uint8_t* Qt = Qs + t * AT_QTILE;
+    uint8_t* Pt = Ps + t * AT_PTILE;
+    // Q row into the swizzled tile (zeros for padding rows)
     {
       const uint4* src = reinterpret_cast<const uint4*>(a.q + (((size_t)b * a.T + node) * a.Hq + hq) * AT_DH);
 #pragma unroll
-      for (int u = 8 * half; u < 8 * half + 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const uint4 v = rvalid ? src[u] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(Qs + at_sw(trow, u)) = v;
+        *reinterpret_cast<uint4*>(Qt + at_sw(trow, u)) = v;
       }
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(q_ready);
     }
     // ancestor-or-self mask of this row's node (closed-form Cartesian layout)
-    uint32_t* mr = mrow + (size_t)trow * a.W;
-    if (half == 0) {
-      for (int w = 0; w < a.W; ++w) mr[w] = 0u;
-      if (rvalid) {
-        int j = node, d = 0;
-        for (int e = 1; e <= a.td.D; ++e)
-          if (j >= a.td.off[e]) d = e;
-        while (true) {
-          mr[j >> 5] |= 1u << (j & 31);
-          if (d == 0) break;
-          j = d == 1 ? 0 : a.td.off[d - 1] + (j - a.td.off[d]) / a.td.k[d];
-          --d;
-        }
+    uint32_t* mr = mrow + (size_t)(t * AT_M + trow) * a.W;
+    for (int w = 0; w < a.W; ++w) mr[w] = 0u;
+    if (rvalid) {
+      int j = node, d = 0;
+      for (int e = 1; e <= a.td.D; ++e)
+        if (j >= a.td.off[e]) d = e;
+      while (true) {
+        mr[j >> 5] |= 1u << (j & 31);
+        if (d == 0) break;
+        j = d == 1 ? 0 : a.td.off[d - 1] + (j - a.td.off[d]) / a.td.k[d];
+        --d;
       }
     }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    const bool warp_live = (blockIdx.x * AT_M + q4 * 32) < nrows;  // some row of this warp is real
-    const int sc0 = half * (AT_KH / 16);  // first 16-column S chunk of this half
-    const int oc0 = half * (AT_DH / 32);  // first 16-column O chunk of this half
+    const bool warp_live = t < ntiles && (row0 + t * AT_M + q4 * 32) < nrows;  // some row of this warp is real
+    const bool tile_live = t < ntiles;
+    const uint32_t sbase = tmem + lane_off + t * 2 * AT_BK;
+    const uint32_t obase = tmem + lane_off + AT_TILES * 2 * AT_BK + t * AT_DH;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    // A failed wait never skips the named barriers below (the partner warps
-    // would wait forever): the loop runs on with the work switched off.
-    for (int i = 0; i < nblk; ++i) {
+    bool ok = tile_live;
+    for (int i = 0; i < nblk && ok; ++i) {
       const int buf = i & 1;
       const int blk = blk_lo + i;
       const bool tree = blk >= nb_cache;
       const int k0 = tree ? (blk - nb_cache) * AT_BK : blk * AT_BK;
       const int nk = tree ? min(AT_BK, a.T - k0) : min(AT_BK, a.L - k0);
-      uint32_t mw = 0u;  // mask word of this half's 32 keys
+      uint32_t mw0 = 0u, mw1 = 0u;  // mask words of the block's 64 keys
       if (tree) {
-        const int wi = (k0 + AT_KH * half) >> 5;
-        mw = wi < a.W ? mr[wi] : 0u;
+        const int wi = k0 >> 5;
+        mw0 = wi < a.W ? mr[wi] : 0u;
+        mw1 = wi + 1 < a.W ? mr[wi + 1] : 0u;
       }
-      if (ok && !at_wait_warp(&s_full[buf], (i >> 1) & 1u, abort_flag, a.ws, lane)) ok = false;
+      if (!at_wait_warp(&s_full[2 * t + buf], (i >> 1) & 1u, abort_flag, a.ws, lane)) {
+        ok = false;
+        break;
+      }
       tc::fence_after_sync();
-      const uint32_t sb = tmem + lane_off + buf * AT_BK;
-      // this half's 32 scores stay in registers for both passes; the S
-      // buffer is released as soon as they are loaded
-      float v[AT_KH];
-      if (ok && warp_live) {
-        float v0[16], v1[16];
-        tc::tmem_ld16_nowait(sb + sc0 * 16, v0);
-        tc::tmem_ld16_nowait(sb + (sc0 + 1) * 16, v1);
+      // the row's 64 scores into registers; the S buffer is released at once
+      float v[AT_BK];
+      if (warp_live) {
+        float v0[16], v1[16], v2[16], v3[16];
+        const uint32_t sb = sbase + buf * AT_BK;
+        tc::tmem_ld16_nowait(sb, v0);
+        tc::tmem_ld16_nowait(sb + 16, v1);
+        tc::tmem_ld16_nowait(sb + 32, v2);
+        tc::tmem_ld16_nowait(sb + 48, v3);
         tc::tmem_wait_ld();
         tc::tmem_regs_ready(v0);
         tc::tmem_regs_ready(v1);
+        tc::tmem_regs_ready(v2);
+        tc::tmem_regs_ready(v3);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           v[j] = v0[j];
           v[16 + j] = v1[j];
+          v[32 + j] = v2[j];
+          v[48 + j] = v3[j];
         }
       }
-      if (ok) {
-        tc::fence_before_sync();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&s_free[2 * t + buf]);
+      if (!warp_live) {  // no real row: nothing to compute, the handshakes go on
+        if (i > 0 && !at_wait_warp(&pv_done[t], (i - 1) & 1u, abort_flag, a.ws, lane)) {
+          ok = false;
+          break;
+        }
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&s_free[buf]);
+        if (lane == 0) tc::mbar_arrive(&p_full[t]);
+        continue;
       }
-      // a full cache block needs no visibility test
+      // a full cache block needs no visibility test; elsewhere a hidden key
+      // gets -inf (branch-free loops, the test sits outside them)
       const bool plain = !tree && nk >= AT_BK;
-      // pass 1: (masked) scaled max over this half's keys, then the row max
-      float mx = -INFINITY;
-      if (ok && warp_live) {
-        if (plain) {
-          float t[AT_KH / 2];
+      if (!plain) {
 #pragma unroll
-          for (int j = 0; j < AT_KH / 2; ++j) t[j] = fmaxf(v[2 * j], v[2 * j + 1]);
-#pragma unroll
-          for (int w = AT_KH / 4; w >= 1; w >>= 1)
-#pragma unroll
-            for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
-          mx = t[0] * a.qscale;  // the scale is positive
-        } else {  // branch-free: a hidden key contributes -inf
-#pragma unroll
-          for (int kh = 0; kh < AT_KH; ++kh) {
-            bool vis = AT_KH * half + kh < nk;
-            if (tree) vis = vis && ((mw >> kh) & 1u);
-            mx = fmaxf(mx, vis ? v[kh] * a.qscale : -INFINITY);
-          }
+        for (int kk = 0; kk < AT_BK; ++kk) {
+          bool vis = rvalid && kk < nk;
+          if (tree) vis = vis && (((kk < 32 ? mw0 : mw1) >> (kk & 31)) & 1u);
+          v[kk] = vis ? v[kk] : -INFINITY;
         }
       }
-      xmax[((i & 1) * 2 + half) * AT_M + trow] = mx;
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      mx = fmaxf(mx, xmax[((i & 1) * 2 + (half ^ 1)) * AT_M + trow]);
-      if (!ok) continue;
+      float tm[AT_BK / 2];
+#pragma unroll
+      for (int j = 0; j < AT_BK / 2; ++j) tm[j] = fmaxf(v[2 * j], v[2 * j + 1]);
+#pragma unroll
+      for (int w = AT_BK / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) tm[j] = fmaxf(tm[j], tm[j + w]);
+      const float mx = tm[0] * a.qscale;  // the scale is positive; -inf stays -inf
+      // P(i) overwrites P(i-1) and a rescale touches O: both need P(i-1) V done
+      if (i > 0 && !at_wait_warp(&pv_done[t], (i - 1) & 1u, abort_flag, a.ws, lane)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
       {
         const bool raise = mx > m + AT_RESCALE_LOG2 || (m == -INFINITY && mx > -INFINITY);
         const float mn = raise ? mx : m;
         const bool resc = raise && i > 0 && m > -INFINITY;
         const float sc = resc ? exp2f(m - mn) : 1.f;
         if (resc) l *= sc;
-        if (__any_sync(0xffffffffu, resc)) {
-          // a rescale touches O: it waits for P(i-1) V, then scales this
-          // half's O columns in TMEM (whole warp)
-          if (!at_wait_warp(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1u, abort_flag, a.ws, lane)) {
-            ok = false;
-            continue;
-          }
-          tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, resc)) {  // rescale the accumulated O rows in TMEM (whole warp)
 #pragma unroll
-          for (int c = 0; c < AT_DH / 32; ++c) {
+          for (int c = 0; c < AT_DH / 16; ++c) {
             float o[16];
-            const uint32_t oa = tmem + lane_off + 2 * AT_BK + (oc0 + c) * 16;
-            tc::tmem_ld16(oa, o);
+            tc::tmem_ld16(obase + c * 16, o);
 #pragma unroll
             for (int j = 0; j < 16; ++j) o[j] *= sc;
-            tc::tmem_st16(oa, o);
+            tc::tmem_st16(obase + c * 16, o);
           }
           tc::tmem_wait_st();
         }
         m = mn;
       }
-      // P(i) reuses the buffer of P(i-2): that P V must be complete
-      if (i >= 2 && !at_wait_warp(&pv_done[i & 1], ((i - 2) >> 1) & 1u, abort_flag, a.ws, lane)) {
-        ok = false;
-        continue;
-      }
-      tc::fence_after_sync();
-      uint8_t* Pb = Ps + (i & 1) * AT_PTILE;
-      // pass 2: P = exp2(s - m) into this half's 32 keys of the P tile (rows
-      // of warps with no real row are left as they are: they only reach
-      // those rows' outputs, which are never stored)
+      // P = exp2(s * scale - m) (a -inf score gives 0) into the P tile
+      const float nm = (m == -INFINITY) ? 0.f : -m;
       float ls = 0.f;
-      if (warp_live) {
-        // the exponent argument of a hidden key is -inf (2^-inf = 0); the
-        // full-block test sits outside the element loops, which have no
-        // branches
-        float t[AT_KH];
-        if (plain) {
+      uint32_t pk[AT_BK / 2];
 #pragma unroll
-          for (int kh = 0; kh < AT_KH; ++kh) t[kh] = fmaf(v[kh], a.qscale, -m);
-        } else {
-#pragma unroll
-          for (int kh = 0; kh < AT_KH; ++kh) {
-            bool vis = rvalid && AT_KH * half + kh < nk;
-            if (tree) vis = vis && ((mw >> kh) & 1u);
-            t[kh] = vis ? fmaf(v[kh], a.qscale, -m) : -INFINITY;
-          }
-        }
-        uint32_t pk[AT_KH / 2];
-#pragma unroll
-        for (int j = 0; j < AT_KH; j += 2) {
-          const float p0 = at_exp2(t[j]), p1 = at_exp2(t[j + 1]);
-          ls += p0 + p1;
-          pk[j >> 1] = pack2_bf16(p0, p1);
-        }
-        // keys AT_KH half .. +31: four 16-byte units of the row
-#pragma unroll
-        for (int u = 0; u < AT_KH / 8; ++u)
-          *reinterpret_cast<uint4*>(Pb + at_sw(trow, (AT_KH / 8) * half + u)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      for (int j = 0; j < AT_BK; j += 2) {
+        const float p0 = at_exp2(fmaf(v[j], a.qscale, nm)), p1 = at_exp2(fmaf(v[j + 1], a.qscale, nm));
+        ls += p0 + p1;
+        pk[j >> 1] = pack2_bf16(p0, p1);
       }
+#pragma unroll
+      for (int u = 0; u < AT_BK / 8; ++u)
+        *reinterpret_cast<uint4*>(Pt + at_sw(trow, u)) =
+            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
       l += ls;
       tc::fence_before_sync();
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(p_full);
+      if (lane == 0) tc::mbar_arrive(&p_full[t]);
     }
-    // ---- epilogue: row sum of both halves, wait for the last P V, then O / l
-    // (slots of parity nblk & 1: their last readers passed the final loop barrier)
-    xmax[((nblk & 1) * 2 + half) * AT_M + trow] = l;
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    const float lsum = l + xmax[((nblk & 1) * 2 + (half ^ 1)) * AT_M + trow];
-    if (ok && nblk > 0 &&
-        !at_wait_warp(&pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1u, abort_flag, a.ws, lane))
-      ok = false;
+    // ---- epilogue: wait for the last P V, then O / l (or the partial)
+    if (ok && nblk > 0 && !at_wait_warp(&pv_done[t], (nblk - 1) & 1u, abort_flag, a.ws, lane)) ok = false;
     tc::fence_after_sync();
     if (ok && warp_live && nblk > 0) {  // TMEM loads by the whole warp, stores by the real rows
-      const uint32_t ob = tmem + lane_off + 2 * AT_BK + oc0 * 16;
       if (a.NS > 1) {
         const size_t pr = (((size_t)b * a.Hq + hq) * a.T + node) * a.NS + sp;
-        float* po = a.part_o + pr * AT_DH + 64 * half;
+        float* po = a.part_o + pr * AT_DH;
 #pragma unroll
-        for (int c = 0; c < AT_DH / 32; ++c) {
+        for (int c = 0; c < AT_DH / 16; ++c) {
           float o[16];
-          tc::tmem_ld16(ob + c * 16, o);
+          tc::tmem_ld16(obase + c * 16, o);
           if (rvalid)
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
               *reinterpret_cast<float4*>(po + c * 16 + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
         }
-        if (rvalid && half == 0) a.part_ml[pr] = make_float2(m, lsum);
+        if (rvalid) a.part_ml[pr] = make_float2(m, l);
       } else {
-        const float inv = rvalid ? 1.f / lsum : 0.f;
-        __nv_bfloat16* op = a.out + ((size_t)b * a.T + node) * a.H + (size_t)hq * AT_DH + 64 * half;
+        const float inv = rvalid ? 1.f / l : 0.f;
+        __nv_bfloat16* op = a.out + ((size_t)b * a.T + node) * a.H + (size_t)hq * AT_DH;
 #pragma unroll
-        for (int c = 0; c < AT_DH / 32; ++c) {
+        for (int c = 0; c < AT_DH / 16; ++c) {
           float o[16];
-          tc::tmem_ld16(ob + c * 16, o);
+          tc::tmem_ld16(obase + c * 16, o);
           if (!rvalid) continue;
           uint4 w0, w1;
           w0.x = pack2_bf16(o[0] * inv, o[1] * inv);
@@ -490,7 +471,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           *reinterpret_cast<uint4*>(op + c * 16 + 8) = w1;
         }
       }
-    } else if (!ok && lane == 0) {
+    } else if (!ok && tile_live && lane == 0) {
       set_error(a.ws, MEDUSA_ERR_TIMEOUT);
     }
   }
@@ -539,7 +520,7 @@ static int at_kv_map(CUtensorMap* m, const void* base, int B, int rows, int rows
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
-// Key splits: when the (128-row block, b, kv head) CTAs do not fill the ~148
+// Key splits: when the (256-row pair, b, kv head) CTAs do not fill the ~148
 // SMs, their key blocks are cut into NS equal shares, NS chosen for the
 // shortest last wave (device independent, so the workspace can be sized from
 // the config alone).  A full grid is never split: the partials would cost
@@ -547,7 +528,7 @@ static int at_kv_map(CUtensorMap* m, const void* base, int B, int rows, int rows
 int attn_tc_splits(int B, int T, int G, int Hkv, int L) {
   constexpr int kSlots = 148;
   if (L == 0) return 1;
-  const long long units = (long long)((T * G + AT_M - 1) / AT_M) * Hkv * B;
+  const long long units = (long long)((T * G + AT_ROWS - 1) / AT_ROWS) * Hkv * B;
   if (units >= kSlots) return 1;
   const int nb_all = (L + AT_BK - 1) / AT_BK + (T + AT_BK - 1) / AT_BK;
   int best = 1;
@@ -597,11 +578,11 @@ int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void
     mkc = mkt;
     mvc = mvt;
   }
-  const size_t smem = 1024 + (size_t)AT_QTILE + 2 * AT_PTILE + (size_t)2 * AT_STAGES * AT_KVTILE + (size_t)4 * AT_M * sizeof(float) +
-                      (size_t)AT_M * p.W * sizeof(uint32_t) + 256;
+  const size_t smem = 1024 + (size_t)AT_TILES * (AT_QTILE + AT_PTILE) + (size_t)2 * AT_STAGES * AT_KVTILE +
+                      (size_t)AT_ROWS * p.W * sizeof(uint32_t) + 256;
   cudaError_t ce = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
-  dim3 grid((p.T * p.G + AT_M - 1) / AT_M, p.Hkv * a.NS, p.B);
+  dim3 grid((p.T * p.G + AT_ROWS - 1) / AT_ROWS, p.Hkv * a.NS, p.B);
   ce = launch_k(tree_attn_tc_kernel, grid, dim3(AT_THREADS), smem, st, false, mkc, mvc, mkt, mvt, a);
   if (ce != cudaSuccess || a.NS == 1) return (int)ce;
   return launch_attn_combine(p, a.part_o, a.part_ml, a.NS, out, st);
