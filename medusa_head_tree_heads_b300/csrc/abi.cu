@@ -34,7 +34,7 @@ int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* to
 
 int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
                        float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
-int launch_verify(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+int launch_verify(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
                   float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, const medusa_tree_t& t,
                   const int32_t* node_argmax, const float* node_lse, const float* node_entropy, int32_t* accept_len,
@@ -144,6 +144,8 @@ int make_plan(const medusa_config_t* c, Plan* p) {
     p->off_ht_tickets = o;
     o = align_up(o + 2 * kHeadsTcMaxCtas * sizeof(int), 256);
   }
+  p->off_keep = o;
+  o = align_up(o + (size_t)p->B * p->T, 256);
   p->total = o;
   return MEDUSA_OK;
 }
@@ -314,7 +316,7 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   }
   MEDUSA_STAGE(launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->tree.mask,
                                 io->attn_out, ws, st))
-  MEDUSA_STAGE(launch_verify(p, io->attn_out, io->lm_head, io->node_argmax, io->node_maxlogit, io->node_lse,
+  MEDUSA_STAGE(launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit, io->node_lse,
                              io->node_entropy, ws, st))
   MEDUSA_STAGE(launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse,
                              io->node_entropy, io->accept_len, io->acc_tokens, io->acc_nodes, io->bonus, ws, st))

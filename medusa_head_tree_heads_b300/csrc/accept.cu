@@ -6,9 +6,10 @@
 // the longest prefix matching what the model would have produced).
 //
 // One CTA per sequence.  Every non-root node c defines the edge
-// parent(c) -> c; its keep flag is computed in parallel (typical mode first
-// scores token_c under the parent's distribution with one dot product
-// lm_head[token_c] . o_parent), then every leaf path counts its leading kept
+// parent(c) -> c; its keep flag is computed in parallel (typical mode scores
+// token_c under the parent's distribution with one dot product
+// lm_head[token_c] . o_parent: for bf16 the verification merge has already
+// done so, one warp per parent), then every leaf path counts its leading kept
 // edges and a block reduction picks the longest (ties: lowest leaf, which is
 // the lowest node id at the first divergence because leaves are numbered in
 // lexicographic rank order).
@@ -33,6 +34,7 @@ struct AcceptArgs {
   const int32_t* node_argmax;
   const float* node_lse;
   const float* node_entropy;
+  const uint8_t* child_keep;  // typical keep flags from the verification merge, or null (computed here)
   int32_t *accept_len, *acc_tokens, *acc_nodes, *bonus;
   uint8_t* ws;
 };
@@ -50,6 +52,8 @@ __global__ void __launch_bounds__(256) accept_kernel(AcceptArgs a) {
   if (!a.typical) {
     for (int c = 1 + threadIdx.x; c < a.T; c += blockDim.x)
       keep[c] = tok[c] == a.node_argmax[(size_t)b * a.T + a.parent[c]];
+  } else if (a.child_keep) {
+    for (int c = 1 + threadIdx.x; c < a.T; c += blockDim.x) keep[c] = a.child_keep[(size_t)b * a.T + c];
   } else {
     const TT* O = reinterpret_cast<const TT*>(a.attn_out);
     const TT* LM = reinterpret_cast<const TT*>(a.lm_head);
@@ -130,6 +134,7 @@ int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, cons
   a.node_argmax = node_argmax;
   a.node_lse = node_lse;
   a.node_entropy = node_entropy;
+  a.child_keep = p.typical && p.bf16 ? ws + p.off_keep : nullptr;
   a.accept_len = accept_len;
   a.acc_tokens = acc_tokens;
   a.acc_nodes = acc_nodes;
@@ -140,9 +145,10 @@ int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, cons
 }
 
 // bf16: tensor-core projection; fp32 (no TF32 anywhere): the CUDA-core stream kernel
-int launch_verify(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+int launch_verify(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
                   float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st) {
-  if (p.bf16) return launch_verify_tc(p, attn_out, lm_head, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
+  if (p.bf16)
+    return launch_verify_tc(p, attn_out, lm_head, token, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
   return launch_verify_rows(p, attn_out, lm_head, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
 }
 
@@ -150,7 +156,7 @@ int launch_verify_accept(const Plan& p, const void* attn_out, const void* lm_hea
                          int32_t* node_argmax, float* node_maxlogit, float* node_lse, float* node_entropy,
                          int32_t* accept_len, int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus, uint8_t* ws,
                          cudaStream_t st) {
-  int e = launch_verify(p, attn_out, lm_head, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
+  int e = launch_verify(p, attn_out, lm_head, t.token, node_argmax, node_maxlogit, node_lse, node_entropy, ws, st);
   if (e) return e;
   return launch_accept(p, attn_out, lm_head, t, node_argmax, node_lse, node_entropy, accept_len, acc_tokens,
                        acc_nodes, bonus, ws, st);

@@ -41,6 +41,7 @@ struct Plan {
   // workspace offsets (bytes)
   size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, off_vtc_part, off_attn_part;
   size_t off_zs, off_ht_slot, off_ht_tickets;  // tensor-core heads: z pairs, cut-tile partials, tickets
+  size_t off_keep;  // [B][T] uint8 typical-acceptance keep flags written by the verification merge
   size_t total;
 };
 
@@ -59,7 +60,7 @@ int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t
 int launch_proj_tc(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws, cudaStream_t st);
 size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh);
 void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks);
-int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
                      float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 
 // launchers (enqueue only; return cudaError_t as int)

@@ -18,12 +18,19 @@
 //   warp 0      TMA producer (one thread), S-stage smem ring
 //   warp 1      TMEM allocator + MMA issuer (one thread)
 //   warps 2..9  epilogue (two per TMEM lane quadrant, columns split in
-//               groups of 64): tcgen05.ld 16 columns at a time; per column a
-//               butterfly "transpose-reduce" across the 32 rows of the warp
-//               (16 exchange rounds per 16 columns instead of 5 per column),
-//               then the warps combine in shared memory and write one
-//               partial (max, sum e, sum e*t, argmax) per (vocab tile, node).
-// A second small kernel merges the vocab-tile partials, one warp per node.
+//               groups of 64): tcgen05.ld 16 columns at a time; per column
+//               the max over the warp's rows and the lowest row reaching it
+//               (redux.sync on an order-preserving integer key); typical
+//               acceptance adds one exponential per element against that
+//               max and a "transpose-reduce" of (sum e, sum e*t) across the
+//               lanes (each exchange round halves the columns a lane carries:
+//               16 rounds per 16 columns instead of 5 per column).  The warps
+//               combine in shared memory and write one partial (max, sum e,
+//               sum e*t, argmax) per (vocab tile, node).
+// A second small kernel merges the vocab-tile partials, one warp per node;
+// with typical acceptance the same warp scores each child token of its node
+// under the node's distribution (one dot product lm_head[token] . o_node)
+// and writes the child's keep flag.
 // Every wait is bounded; on a timeout the kernel sets MEDUSA_ERR_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <limits.h>
@@ -52,6 +59,15 @@ struct VtcArgs {
   float* node_lse;
   float* node_entropy;
   uint8_t* ws;
+  // typical acceptance: every child c of node n is scored under n's
+  // distribution in the merge (keep[c] = p_n(token_c) > threshold_n)
+  TreeDims td;
+  int T;
+  const int32_t* token;             // [B][T]
+  const __nv_bfloat16* attn_out;    // [N][H]
+  const __nv_bfloat16* lm_head;     // [V][H]
+  uint8_t* keep;                    // [B][T]
+  float log_eps, log_delta;
 };
 
 struct Soft {
@@ -96,56 +112,6 @@ __device__ __forceinline__ Soft shfl_soft(const Soft& a, int o) {
   r.i = __shfl_xor_sync(0xffffffffu, a.i, o);
   return r;
 }
-
-// Reduces 16 columns over the 32 rows held by the warp's lanes (one row per
-// lane): a butterfly "transpose-reduce" in which every exchange round halves
-// the number of columns a lane carries, so 16 columns cost 16 rounds instead
-// of 5 per column.  Afterwards lane l holds column l >> 1.
-template <bool TYPICAL>
-__device__ __forceinline__ Soft column_reduce(const float (&v)[16], int row, bool row_ok, int lane, float it) {
-  Soft st[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    st[j].m = row_ok ? v[j] : -INFINITY;
-    st[j].z = row_ok ? 1.f : 0.f;
-    st[j].s = 0.f;
-    st[j].i = row_ok ? row : INT_MAX;
-  }
-#pragma unroll
-  for (int step = 0; step < 4; ++step) {
-    const int o = 16 >> step, half = 8 >> step;
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const Soft send = up ? st[i] : st[i + half];
-      const Soft keep = up ? st[i + half] : st[i];
-      if (TYPICAL) {
-        st[i] = soft_join(keep, shfl_soft(send, o), true, it);
-      } else {  // greedy: only (max, argmax) travel
-        Soft r;
-        r.m = __shfl_xor_sync(0xffffffffu, send.m, o);
-        r.i = __shfl_xor_sync(0xffffffffu, send.i, o);
-        const bool tk = better(r.m, r.i, keep.m, keep.i);
-        st[i].m = tk ? r.m : keep.m;
-        st[i].i = tk ? r.i : keep.i;
-        st[i].z = 1.f;
-        st[i].s = 0.f;
-      }
-    }
-  }
-  if (TYPICAL) return soft_join(st[0], shfl_soft(st[0], 1), true, it);
-  Soft r;
-  r.m = __shfl_xor_sync(0xffffffffu, st[0].m, 1);
-  r.i = __shfl_xor_sync(0xffffffffu, st[0].i, 1);
-  const bool tk = better(r.m, r.i, st[0].m, st[0].i);
-  Soft o;
-  o.m = tk ? r.m : st[0].m;
-  o.i = tk ? r.i : st[0].i;
-  o.z = (o.i == INT_MAX) ? 0.f : 1.f;
-  o.s = 0.f;
-  return o;
-}
-
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               uint8_t* ws) {
@@ -313,31 +279,71 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       for (int ch0 = 4 * half; ch0 < a.BN / 16; ch0 += 8) {
         const int nch = min(4, a.BN / 16 - ch0);
         if (typical) {
-          Soft col[4];
+          // typical: per column the max and argmax as in greedy (redux),
+          // then one exponential per element against that max and a plain
+          // additive transpose-reduce of (sum e, sum e*t) over the 64 rows
+          const int row0 = vt * VT_SUB * VT_M + q * 32 + lane;  // half 1 adds VT_M
+          const bool ok0 = row0 < a.V, ok1 = row0 + VT_M < a.V;
+#pragma unroll 1
+          for (int c = 0; c < nch; ++c) {
+            float v[VT_SUB][16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) col[c] = soft_empty();
-#pragma unroll
-          for (int h = 0; h < VT_SUB; ++h) {
-            const int row = (vt * VT_SUB + h) * VT_M + q * 32 + lane;
-            const bool row_ok = row < a.V;
-            float v[4][16];
-            const uint32_t tb = tmem + h * 256 + ((uint32_t)(q * 32) << 16) + ch0 * 16;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              if (c < nch) tc::tmem_ld16_nowait(tb + c * 16, v[c]);
+            for (int h = 0; h < VT_SUB; ++h)
+              tc::tmem_ld16_nowait(tmem + h * 256 + ((uint32_t)(q * 32) << 16) + (ch0 + c) * 16, v[h]);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tc::tmem_regs_ready(v[c]);
+            for (int h = 0; h < VT_SUB; ++h) tc::tmem_regs_ready(v[h]);
+            float zs[16], ss[16];
+            float my_m = -INFINITY;
+            int my_i = INT_MAX;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              if (c >= nch) break;
-              col[c] = soft_join(col[c], column_reduce<true>(v[c], row, row_ok, lane, a.inv_temp), true,
-                                 a.inv_temp);
+            for (int j = 0; j < 16; ++j) {
+              const float x0 = ok0 ? v[0][j] : -INFINITY;
+              const float x1 = ok1 ? v[1][j] : -INFINITY;
+              const bool one = x1 > x0;  // equal values keep half 0 (the lower row)
+              const int key = order_key(one ? x1 : x0);
+              int kmax;
+              asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(kmax) : "r"(key));
+              const uint32_t r = ok0 ? (uint32_t)(one ? row0 + VT_M : row0) : 0xffffffffu;
+              uint32_t rmin;
+              asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(rmin) : "r"(key == kmax ? r : 0xffffffffu));
+              const float mj = order_key_inv(kmax);
+              const bool any = rmin != 0xffffffffu;
+              const float t0 = ok0 && any ? (x0 - mj) * a.inv_temp : 0.f;
+              const float t1 = ok1 && any ? (x1 - mj) * a.inv_temp : 0.f;
+              const float e0 = ok0 && any ? expf(t0) : 0.f;
+              const float e1 = ok1 && any ? expf(t1) : 0.f;
+              zs[j] = e0 + e1;
+              ss[j] = e0 * t0 + e1 * t1;
+              if ((lane >> 1) == j) {  // this lane ends up holding column j
+                my_m = any ? mj : -INFINITY;
+                my_i = any ? (int)rmin : INT_MAX;
+              }
+            }
+            // after the four halving rounds lane l holds column l >> 1
+#pragma unroll
+            for (int step = 0; step < 4; ++step) {
+              const int o = 16 >> step, hh = 8 >> step;
+              const bool up = (lane & o) != 0;
+#pragma unroll
+              for (int k = 0; k < hh; ++k) {
+                const float sz = up ? zs[k] : zs[k + hh], kz = up ? zs[k + hh] : zs[k];
+                const float sv = up ? ss[k] : ss[k + hh], kv = up ? ss[k + hh] : ss[k];
+                zs[k] = kz + __shfl_xor_sync(0xffffffffu, sz, o);
+                ss[k] = kv + __shfl_xor_sync(0xffffffffu, sv, o);
+              }
+            }
+            zs[0] += __shfl_xor_sync(0xffffffffu, zs[0], 1);
+            ss[0] += __shfl_xor_sync(0xffffffffu, ss[0], 1);
+            if ((lane & 1) == 0) {
+              Soft o;
+              o.m = my_m;
+              o.i = my_i;
+              o.z = my_i == INT_MAX ? 0.f : zs[0];
+              o.s = my_i == INT_MAX ? 0.f : ss[0];
+              red[q * a.BN + (ch0 + c) * 16 + (lane >> 1)] = o;
             }
           }
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (c < nch && (lane & 1) == 0) red[q * a.BN + (ch0 + c) * 16 + (lane >> 1)] = col[c];
         } else {
           // greedy: per column, the best of this thread's two rows, then a
           // warp max of an order-preserving integer key and a warp min of the
@@ -449,13 +455,51 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(VtcArgs a) {
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = soft_join(m, shfl_soft(m, o), TYPICAL, a.inv_temp);
+  const float lz = logf(m.z);
+  const float lse = m.m * a.inv_temp + lz, ent = lz - m.s / m.z;
   if (lane == 0) {
     a.node_argmax[n] = m.i;
     a.node_maxlogit[n] = m.m;
     if (TYPICAL) {
-      const float lz = logf(m.z);
-      a.node_lse[n] = m.m * a.inv_temp + lz;
-      a.node_entropy[n] = lz - m.s / m.z;
+      a.node_lse[n] = lse;
+      a.node_entropy[n] = ent;
+    }
+  }
+  if (!TYPICAL) return;
+  // children of this node (closed-form Cartesian layout): the child's token
+  // under this node's softmax at the temperature, against the threshold
+  const int b = n / a.T, i = n - b * a.T;
+  int d = 0;
+  for (int e = 1; e <= a.td.D; ++e)
+    if (i >= a.td.off[e]) d = e;
+  if (d >= a.td.D) return;
+  const int kc = a.td.k[d + 1];
+  const int c0 = a.td.off[d + 1] + (i - a.td.off[d]) * kc;
+  const float logthr = fminf(a.log_eps, a.log_delta - ent);
+  const uint4* on = reinterpret_cast<const uint4*>(a.attn_out + (size_t)n * a.H);
+  for (int r = 0; r < kc; ++r) {
+    const int c = c0 + r;
+    const int t = a.token[(size_t)b * a.T + c];
+    const bool t_ok = t >= 0 && t < a.V;
+    float s0 = 0.f, s1 = 0.f;
+    if (t_ok) {
+      const uint4* lr = reinterpret_cast<const uint4*>(a.lm_head + (size_t)t * a.H);
+      for (int j = lane; j < a.H / 8; j += 32) {  // 8 bf16 per 16-byte load
+        const uint4 x = __ldg(lr + j), y = __ldg(on + j);
+        s0 = fmaf(bf16_lo(x.x), bf16_lo(y.x), s0);
+        s1 = fmaf(bf16_hi(x.x), bf16_hi(y.x), s1);
+        s0 = fmaf(bf16_lo(x.y), bf16_lo(y.y), s0);
+        s1 = fmaf(bf16_hi(x.y), bf16_hi(y.y), s1);
+        s0 = fmaf(bf16_lo(x.z), bf16_lo(y.z), s0);
+        s1 = fmaf(bf16_hi(x.z), bf16_hi(y.z), s1);
+        s0 = fmaf(bf16_lo(x.w), bf16_lo(y.w), s0);
+        s1 = fmaf(bf16_hi(x.w), bf16_hi(y.w), s1);
+      }
+    }
+    const float sdot = warp_sum(s0 + s1);
+    if (lane == 0) {
+      if (!t_ok) set_error(a.ws, MEDUSA_ERR_DEVICE);
+      a.keep[(size_t)b * a.T + c] = t_ok && (sdot * a.inv_temp - lse > logthr);
     }
   }
 }
@@ -536,7 +580,7 @@ size_t verify_tc_part_bytes(int V, int N) {
   return (size_t)((V + VT_SUB * VT_M - 1) / (VT_SUB * VT_M)) * N * sizeof(float4);
 }
 
-int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
                      float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st) {
   VtcArgs a;
   a.V = p.V;
@@ -555,6 +599,14 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, i
   a.node_lse = node_lse;
   a.node_entropy = node_entropy;
   a.ws = ws;
+  a.td = p.tree;
+  a.T = p.T;
+  a.token = token;
+  a.attn_out = reinterpret_cast<const __nv_bfloat16*>(attn_out);
+  a.lm_head = reinterpret_cast<const __nv_bfloat16*>(lm_head);
+  a.keep = ws + p.off_keep;
+  a.log_eps = p.typical ? logf(p.eps) : 0.f;
+  a.log_delta = p.typical && p.delta > 0.f ? logf(p.delta) : -INFINITY;
   const size_t stage = (size_t)(VT_SUB * VT_M + a.BN) * VT_BK * 2;
   const size_t fixed = 1024 + (size_t)4 * a.BN * sizeof(Soft) + 256;
   const size_t budget = 227 * 1024;
