@@ -433,8 +433,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&p_full[t]);
     }
-    // ---- epilogue: wait for the last P V, then O / l (or the partial)
+    // ---- epilogue: wait for the last P V, then O / l (or the partial).  The
+    // stores wait for the preceding grid (the previous step may still read
+    // the output); everything above reads only this step's inputs.
     if (ok && nblk > 0 && !at_wait_warp(&pv_done[t], (nblk - 1) & 1u, abort_flag, a.ws, lane)) ok = false;
+    pdl_wait();
     tc::fence_after_sync();
     if (ok && warp_live && nblk > 0) {  // TMEM loads by the whole warp, stores by the real rows
       if (a.NS > 1) {
@@ -583,7 +586,9 @@ int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void
   cudaError_t ce = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   dim3 grid((p.T * p.G + AT_ROWS - 1) / AT_ROWS, p.Hkv * a.NS, p.B);
-  ce = launch_k(tree_attn_tc_kernel, grid, dim3(AT_THREADS), smem, st, false, mkc, mvc, mkt, mvt, a);
+  // programmatic dependent launch: the pass runs beside the preceding kernels,
+  // only the stores wait for them
+  ce = launch_k(tree_attn_tc_kernel, grid, dim3(AT_THREADS), smem, st, true, mkc, mvc, mkt, mvt, a);
   if (ce != cudaSuccess || a.NS == 1) return (int)ce;
   return launch_attn_combine(p, a.part_o, a.part_ml, a.NS, out, st);
 }

@@ -401,7 +401,9 @@ static int gemv_tma_launch(GtArgs a, int sm_count, int nc, cudaStream_t st, int*
   e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return (int)e;
   if (ctas_out) *ctas_out = ctas;
-  return (int)launch_k(k, dim3(ctas), dim3(GT_THREADS), smem, st, EPI == 1, a);
+  // programmatic dependent launch for both: the producer streams weights
+  // (written by no kernel) at once; x, z and the outputs wait for the grid before
+  return (int)launch_k(k, dim3(ctas), dim3(GT_THREADS), smem, st, true, a);
 }
 
 static int gt_nc(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : 4); }

@@ -506,9 +506,10 @@ int launch_fc_tc(const Plan& p, const void* h, const void* W1, const void* b1, u
   if (e) return e;
   e = make_tmap_bf16(&tB, h, p.B, p.H, n);
   if (e) return e;
-  // first kernel of the step: launched without the programmatic dependency
-  if (n == 16) return ht_launch<0, 16, 4>(tA, tB, a, grid, false, st);
-  return ht_launch<0, 32, 4>(tA, tB, a, grid, false, st);
+  // programmatic dependent launch: W1 boxes stream before the wait, h and the
+  // outputs after it
+  if (n == 16) return ht_launch<0, 16, 4>(tA, tB, a, grid, true, st);
+  return ht_launch<0, 32, 4>(tA, tB, a, grid, true, st);
 }
 
 int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t st, int* ctas, int* upc,
