@@ -57,11 +57,7 @@ def flops(s) -> dict:
 # the dominant kernel, from an ncu capture of the full-size workload, keyed by
 # the SHA-256 of the kernel's source file at capture time: a changed kernel
 # reports null until it is captured again.
-TRAFFIC_CAPTURES = {
-    "7b-bf16": {"source": "medusa_head_tree_heads_b300/csrc/gemv_tma.cu",
-                "sha256": "28890aa391fd11430d695ab99286fd672abacb2d45fdb8db7eef13364951d668",
-                "bytes": 1.31e9 + 2.90e6},
-}
+TRAFFIC_CAPTURES: dict = {}  # workload -> {"source": file, "sha256": digest, "bytes": per launch}
 
 
 def captured_traffic(workload: str):
@@ -84,16 +80,50 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "source": "fallback"}
 
 
+class _Nvml:
+    """The few read-only NVML queries the clock sampler needs, bound with
+    ctypes to the driver's libnvidia-ml (no Python NVML package required)."""
+
+    CLOCK_SM = 1
+    REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+                   ("hw_thermal_slowdown", 0x40))
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        pr = torch.cuda.get_device_properties(cuda_index)
+        bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) != 0:
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(self.h)) != 0:
+                raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_clock(self, maximum=False) -> float:
+        v = self.c.c_uint()
+        fn = self.lib.nvmlDeviceGetMaxClockInfo if maximum else self.lib.nvmlDeviceGetClockInfo
+        if fn(self.h, self.CLOCK_SM, self.c.byref(v)) != 0:
+            raise OSError("clock query failed")
+        return float(v.value)
+
+    def reasons(self) -> set:
+        v = self.c.c_ulonglong()
+        if self.reasons_fn(self.h, self.c.byref(v)) != 0:
+            raise OSError("reason query failed")
+        return {n for n, bit in self.REASON_BITS if v.value & bit}
+
+
 class Clocks:
     """SM clock and throttle-reason samples taken during a region: an NVML
     poller thread (every ~2 ms, so even a region of a few tens of ms gets
     samples), else nvidia-smi at its 100 ms period.  Reads only; no GPU
     setting is touched."""
 
-    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
-               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
-               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
-               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"))
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -103,37 +133,25 @@ class Clocks:
         self.samples = []  # (sm_mhz, max_mhz, set of reasons)
         self.source = None
 
-    def _nvml_handle(self):
-        import pynvml
-        pynvml.nvmlInit()
-        try:
-            uuid = str(torch.cuda.get_device_properties(self.index).uuid)
-            return pynvml, pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
-        except Exception:
-            return pynvml, pynvml.nvmlDeviceGetHandleByIndex(self.index)
-
-    def _poll(self, nv, h):
-        mx = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
-        masks = [(n, getattr(nv, attr)) for n, attr in self.REASONS]
+    def _poll(self, nv):
+        mx = nv.sm_clock(maximum=True)
         while not self.stop.is_set():
             try:
-                sm = nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)
-                bits = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
-            except Exception:
+                self.samples.append((nv.sm_clock(), mx, nv.reasons()))
+            except OSError:
                 break
-            self.samples.append((float(sm), float(mx), {n for n, m in masks if bits & m}))
             self.stop.wait(0.002)
 
     def __enter__(self):
         import threading
         try:
-            nv, h = self._nvml_handle()
+            nv = _Nvml(self.index)
             self.stop = threading.Event()
-            self.thread = threading.Thread(target=self._poll, args=(nv, h), daemon=True)
+            self.thread = threading.Thread(target=self._poll, args=(nv,), daemon=True)
             self.thread.start()
             self.source = "nvml"
             return self
-        except Exception:
+        except (OSError, AttributeError, RuntimeError, AssertionError):
             self.source = None
         try:
             self.proc = subprocess.Popen(
@@ -156,7 +174,6 @@ class Clocks:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            names = [n for n, _ in self.REASONS]
             for l in out.splitlines():
                 f = [x.strip() for x in l.split(",")]
                 if len(f) < 6:
@@ -165,7 +182,7 @@ class Clocks:
                     sm, mx = float(f[0]), float(f[1])
                 except ValueError:
                     continue
-                self.samples.append((sm, mx, {n for n, v in zip(names, f[2:6]) if v.lower() == "active"}))
+                self.samples.append((sm, mx, {n for n, v in zip(self.NAMES, f[2:6]) if v.lower() == "active"}))
 
     def summary(self) -> dict:
         if not self.samples:

@@ -8,22 +8,14 @@
 namespace medusa {
 
 int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
-bool gemv_tma_supported(const Plan& p);
 int launch_bounded_wait_probe(uint8_t* ws, uint64_t budget_ns, cudaStream_t st);
-int launch_proj_tma_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t st, int max_stages, int* ctas,
-                         int* rpc);
 int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
                       const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st);
-int launch_fc_tma(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
-int launch_proj_tma(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
-                    cudaStream_t st);
 
-// head layer / head projection: the TMA-fed streaming kernel where it
-// applies (bf16, batch <= 4), the tensor-core kernel for the other bf16
-// batches up to 32, else the general streaming kernel
+// head layer / head projection: the tensor-core kernel for bf16 batches up to
+// 32, else the general streaming kernel
 int launch_head_layer(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws,
                              cudaStream_t st) {
-  if (gemv_tma_supported(p)) return launch_fc_tma(p, h, W1, b1, ws, st);
   if (heads_tc_supported(p)) return launch_fc_tc(p, h, W1, b1, ws, st);
   return launch_fc(p, h, W1, b1, ws, st);
 }
@@ -163,7 +155,6 @@ void finish_plan(Plan* p) {
 
 int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                      cudaStream_t st) {
-  if (gemv_tma_supported(p)) return launch_proj_tma(p, W2, topk_idx, topk_val, ws, st);
   if (heads_tc_supported(p)) return launch_proj_tc(p, W2, topk_idx, topk_val, ws, st);
   return launch_proj_topk(p, W2, topk_idx, topk_val, ws, st);
 }
@@ -300,13 +291,8 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   ++k;                      \
   if (e) return cuda_status(e);
   MEDUSA_STAGE(launch_head_layer(p, io->h, io->W1, io->b1, ws, st))
-  if (gemv_tma_supported(p)) {
-    // small batch: the projection kernel alone, then one kernel for the
-    // candidate merge and the tree
-    int ctas = 0, rpc = 0;
-    MEDUSA_STAGE(launch_proj_tma_only(p, io->W2, ws, st, 8, &ctas, &rpc))
-    MEDUSA_STAGE(launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, rpc, p.V, st))
-  } else if (heads_tc_supported(p)) {
+  if (heads_tc_supported(p)) {
+    // the projection kernel alone, then one kernel for the candidate merge and the tree
     int ctas = 0, upc = 0, ups = 0;
     MEDUSA_STAGE(launch_proj_tc_only(p, io->W2, ws, st, &ctas, &upc, &ups))
     MEDUSA_STAGE(launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, upc, ups, st))
@@ -350,7 +336,7 @@ int medusa_step_launches(const medusa_config_t* cfg) {
   if (s != MEDUSA_OK) return s;
   finish_plan(&p);
   int n = 6;                        // one launch per stage
-  if (!gemv_tma_supported(p) && !heads_tc_supported(p)) n += 1;  // separate top-k merge (else fused with the tree)
+  if (!heads_tc_supported(p)) n += 1;  // separate top-k merge (else fused with the tree)
   if (p.bf16) {
     int NS, cb;
     attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &NS, &cb);

@@ -1,5 +1,5 @@
-// Medusa heads on the 5th-generation tensor cores, for batches where the
-// heads are a real dense contraction ("Medusa Heads": head k maps the last
+// Medusa heads on the 5th-generation tensor cores, bf16, batches 1..32
+// ("Medusa Heads": head k maps the last
 // hidden state h to z_k = h + SiLU(W1_k h + b1_k) and scores the vocabulary
 // with W2_k z_k; the top-k tokens of every head build the candidate tree).
 //
@@ -438,12 +438,10 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
 }
 
 // ------------------------------------------------------------------- host --
-bool gemv_tma_supported(const Plan& p);
-
 static int ht_n_layer(int B) { return B <= 16 ? 16 : 32; }
 static int ht_n_proj(int B) { return 2 * B <= 16 ? 16 : (2 * B <= 32 ? 32 : 64); }
 
-bool heads_tc_supported(const Plan& p) { return p.bf16 && p.B <= kHeadsTcMaxBatch && !gemv_tma_supported(p); }
+bool heads_tc_supported(const Plan& p) { return p.bf16 && p.B <= kHeadsTcMaxBatch; }
 
 size_t heads_tc_zs_bytes(int K, int B, int H) { return (size_t)K * ht_n_proj(B) * H * 2; }
 size_t heads_tc_slot_bytes(int B) {
