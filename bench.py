@@ -57,7 +57,10 @@ def flops(s) -> dict:
 # the dominant kernel, from an ncu capture of the full-size workload, keyed by
 # the SHA-256 of the kernel's source file at capture time: a changed kernel
 # reports null until it is captured again.
-TRAFFIC_CAPTURES: dict = {}  # workload -> {"source": file, "sha256": digest, "bytes": per launch}
+TRAFFIC_CAPTURES = {
+    "7b-bf16": {"source": "medusa_head_tree_heads_b300/csrc/heads_tc.cu", "sha256": "63cec550a0c53eb9877df6e9f0068ce657ae469f0d211df6157bde3fcd365d33",
+                "bytes": 1312811776 + 4263168},
+}
 
 
 def captured_traffic(workload: str):
