@@ -86,19 +86,32 @@ typedef struct {
   float temperature;               /* typical: softmax temperature (> 0) */
   float eps;                       /* typical: threshold cap */
   float delta;                     /* typical: threshold scale, thr = min(eps, delta*exp(-H)) */
+  /* Optional explicit candidate tree ("Medusa Heads", "Attenzione sull'albero
+   * e accettazione" speaks of the tree built from the heads' candidates; a
+   * sparse subset of the Cartesian product is the same structure with fewer
+   * branches).  0 = the Cartesian tree of topk[].  Otherwise tree_nodes = T
+   * nodes in strictly increasing (depth, parent, rank) order, node 0 the root:
+   * tree_parent[i] < i (-1 for node 0), node depth = parent depth + 1 <= depth,
+   * tree_rank[i] < topk[depth - 1] (0 for the root).  Host arrays, read during
+   * the call only; anything else is MEDUSA_ERR_INVALID_ARG (T > 512:
+   * MEDUSA_ERR_UNSUPPORTED). */
+  int32_t tree_nodes;
+  const int32_t* tree_parent;
+  const int32_t* tree_rank;
 } medusa_config_t;
 
 /* Candidate tree, device arrays allocated by the caller (sizes from
  * medusa_tree_size).  Nodes are numbered breadth first: node 0 is the root;
  * depth-d nodes follow depth-(d-1) nodes, ordered by parent then by rank in
- * the head-d list. */
+ * the head-d list.  Leaves are the nodes without children, in increasing
+ * order; a leaf shallower than the tree depth ends its path row with -1. */
 typedef struct {
   int32_t* token;   /* [B][T] candidate token; token[b][0] = root_token[b] */
   int32_t* parent;  /* [T] parent node, -1 for the root */
   int32_t* depth;   /* [T] */
   int32_t* rank;    /* [T] rank of the node's token in its head's list (root 0) */
   uint32_t* mask;   /* [T][W] bit j of word j/32 set iff node j is node i or an ancestor */
-  int32_t* paths;   /* [NL][D+1] node ids from the root to each leaf */
+  int32_t* paths;   /* [NL][D+1] node ids from the root to each leaf, then -1 */
   int32_t* pos;     /* [T] position id kv_len + depth */
 } medusa_tree_t;
 

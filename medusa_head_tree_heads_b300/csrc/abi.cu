@@ -81,25 +81,69 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   p->temperature = c->temperature;
   p->eps = c->eps;
   p->delta = c->delta;
-  // tree sizes
+  // tree tables: the Cartesian tree of topk[] or the caller's explicit tree
   TreeDims& td = p->tree;
   td.D = p->D;
-  td.off[0] = 0;
-  long long level = 1, total = 1;
   p->kmax = 1;
   for (int d = 1; d <= p->D; ++d) {
     const int k = c->topk[d - 1];
     if (k < 1 || k > MEDUSA_MAX_TOPK || k > p->V) return MEDUSA_ERR_UNSUPPORTED;
-    td.k[d] = k;
     if (k > p->kmax) p->kmax = k;
-    td.off[d] = (int)total;
-    level *= k;
-    total += level;
-    if (total > MEDUSA_MAX_NODES) return MEDUSA_ERR_UNSUPPORTED;
   }
-  td.off[p->D + 1] = (int)total;
-  td.T = (int)total;
-  td.n_leaves = (int)level;
+  int T = 0;
+  if (c->tree_nodes == 0) {
+    td.parent[0] = -1;
+    td.depth[0] = 0;
+    td.rank[0] = 0;
+    T = 1;
+    int lv0 = 0, lv1 = 1;  // nodes of the previous level
+    for (int d = 1; d <= p->D; ++d) {
+      const int lv2 = T;
+      for (int par = lv0; par < lv1; ++par)
+        for (int r = 0; r < c->topk[d - 1]; ++r) {
+          if (T >= MEDUSA_MAX_NODES) return MEDUSA_ERR_UNSUPPORTED;
+          td.parent[T] = (int16_t)par;
+          td.depth[T] = (uint8_t)d;
+          td.rank[T] = (uint8_t)r;
+          ++T;
+        }
+      lv0 = lv2;
+      lv1 = T;
+    }
+  } else {
+    T = c->tree_nodes;
+    if (T < 1 || T > MEDUSA_MAX_NODES) return MEDUSA_ERR_UNSUPPORTED;
+    if (!c->tree_parent || !c->tree_rank) return MEDUSA_ERR_INVALID_ARG;
+    if (c->tree_parent[0] != -1 || c->tree_rank[0] != 0) return MEDUSA_ERR_INVALID_ARG;
+    td.parent[0] = -1;
+    td.depth[0] = 0;
+    td.rank[0] = 0;
+    for (int i = 1; i < T; ++i) {
+      const int par = c->tree_parent[i], r = c->tree_rank[i];
+      if (par < 0 || par >= i) return MEDUSA_ERR_INVALID_ARG;
+      const int d = td.depth[par] + 1;
+      if (d > p->D || r < 0 || r >= c->topk[d - 1]) return MEDUSA_ERR_INVALID_ARG;
+      // strictly increasing (depth, parent, rank): breadth-first, no repeated child
+      const int pd = td.depth[i - 1], pp = td.parent[i - 1], pr = td.rank[i - 1];
+      if (!(d > pd || (d == pd && (par > pp || (par == pp && r > pr))))) return MEDUSA_ERR_INVALID_ARG;
+      td.parent[i] = (int16_t)par;
+      td.depth[i] = (uint8_t)d;
+      td.rank[i] = (uint8_t)r;
+    }
+  }
+  td.T = T;
+  td.n_leaves = 0;
+  for (int i = 0; i < T; ++i) {
+    td.first_child[i] = -1;
+    td.n_child[i] = 0;
+  }
+  for (int i = 1; i < T; ++i) {
+    const int par = td.parent[i];
+    if (td.first_child[par] < 0) td.first_child[par] = (int16_t)i;
+    td.n_child[par] += 1;
+  }
+  for (int i = 0; i < T; ++i)
+    if (td.n_child[i] == 0) td.leaf[td.n_leaves++] = (int16_t)i;
   td.W = (td.T + 31) / 32;
   p->T = td.T;
   p->NL = td.n_leaves;

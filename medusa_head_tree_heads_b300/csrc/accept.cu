@@ -10,9 +10,9 @@
 // token_c under the parent's distribution with one dot product
 // lm_head[token_c] . o_parent: for bf16 the verification merge has already
 // done so, one warp per parent), then every leaf path counts its leading kept
-// edges and a block reduction picks the longest (ties: lowest leaf, which is
-// the lowest node id at the first divergence because leaves are numbered in
-// lexicographic rank order).
+// edges and a block reduction picks the longest (ties: the smaller last kept
+// node, which in breadth-first (depth, parent, rank) order is the lower node at
+// the first divergence).
 #include <limits.h>
 
 #include "internal.cuh"
@@ -42,7 +42,7 @@ struct AcceptArgs {
 template <typename TT>
 __global__ void __launch_bounds__(256) accept_kernel(AcceptArgs a) {
   __shared__ unsigned char keep[MEDUSA_MAX_NODES];
-  __shared__ int best_len[256], best_leaf[256];
+  __shared__ int best_len[256], best_node[256], best_leaf[256];
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* tok = a.token + (size_t)b * a.T;
@@ -77,24 +77,32 @@ __global__ void __launch_bounds__(256) accept_kernel(AcceptArgs a) {
   }
   __syncthreads();
 
-  int bl = -1, bleaf = INT_MAX;
+  // per leaf: the kept prefix of its path (rows of shallow leaves end in -1);
+  // the longest wins, ties to the smaller last kept node, which in this node
+  // order is the lower node at the first divergence; then the lower leaf
+  int bl = -1, bnode = INT_MAX, bleaf = INT_MAX;
   for (int leaf = threadIdx.x; leaf < a.NL; leaf += blockDim.x) {
     const int32_t* path = a.paths + (size_t)leaf * (a.D + 1);
     int n = 0;
-    while (n < a.D && keep[path[n + 1]]) ++n;
-    if (n > bl) {  // leaves visited in increasing order: first longest wins
+    while (n < a.D && path[n + 1] >= 0 && keep[path[n + 1]]) ++n;
+    const int node = path[n];
+    if (n > bl || (n == bl && node < bnode)) {  // leaves visited in increasing order
       bl = n;
+      bnode = node;
       bleaf = leaf;
     }
   }
   best_len[threadIdx.x] = bl;
+  best_node[threadIdx.x] = bnode;
   best_leaf[threadIdx.x] = bleaf;
   __syncthreads();
   for (int s = blockDim.x / 2; s > 0; s >>= 1) {
     if (threadIdx.x < s) {
-      const int ol = best_len[threadIdx.x + s], of = best_leaf[threadIdx.x + s];
-      if (ol > best_len[threadIdx.x] || (ol == best_len[threadIdx.x] && of < best_leaf[threadIdx.x])) {
+      const int ol = best_len[threadIdx.x + s], on = best_node[threadIdx.x + s], of = best_leaf[threadIdx.x + s];
+      const int ml = best_len[threadIdx.x], mn = best_node[threadIdx.x], mf = best_leaf[threadIdx.x];
+      if (ol > ml || (ol == ml && (on < mn || (on == mn && of < mf)))) {
         best_len[threadIdx.x] = ol;
+        best_node[threadIdx.x] = on;
         best_leaf[threadIdx.x] = of;
       }
     }

@@ -1,4 +1,4 @@
-// Tree attention on tensor cores (bf16), flash-style ("Medusa Heads",
+// Tree attention with warp-level mma.sync (bf16, head dim 64), flash-style ("Medusa Heads",
 // "Attenzione sull'albero e accettazione": all candidates in one pass, each
 // seeing only its ancestors; "Tetes de decodage Medusa", "Plongee profonde").
 //
@@ -28,7 +28,7 @@ constexpr int AM_KB = 64;  // keys per block
 
 struct AmArgs {
   const __nv_bfloat16 *q, *kt, *vt, *kc, *vc;
-  TreeDims td;  // the Cartesian tree: each CTA derives its rows' ancestor masks from it
+  TreeDims td;  // the tree tables: each CTA derives its rows' ancestor masks from them
   __nv_bfloat16* out;
   int B, T, W, Hq, Hkv, G, L, Lc, H;
   int NS;          // key splits per (b, g): 1 = no split, else NS-1 cache chunks + the tree
@@ -72,7 +72,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 template <int DH, int NW, int S>
-__global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
+__global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(const __grid_constant__ AmArgs a) {
   constexpr int LD = DH + 8;  // padded smem row (elements)
   constexpr int NT = NW * 32;
   constexpr int KS = DH / 16;  // k-steps of Q K^T
@@ -89,24 +89,14 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
   const int rbase = blockIdx.x * 16 * NW + warp * 16;
   const size_t kv_row = (size_t)a.Hkv * DH;  // elements between consecutive keys
   pdl_trigger();
-  // Ancestor-or-self mask rows of this CTA's query rows, from the closed-form
-  // layout (level d starts at off[d]; local index m has parent off[d-1] + m / k_d).
+  // Ancestor-or-self mask rows of this CTA's query rows (chains of parents).
   // The kernel reads nothing an earlier kernel of the step writes.
   for (int rr = threadIdx.x; rr < 16 * NW; rr += NT) {
     const int r = blockIdx.x * 16 * NW + rr;
     uint32_t* mr = mrow + (size_t)rr * a.W;
     for (int w = 0; w < a.W; ++w) mr[w] = 0u;
-    if (r < nrows) {
-      int j = r / a.G, d = 0;
-      for (int e = 1; e <= a.td.D; ++e)
-        if (j >= a.td.off[e]) d = e;
-      while (true) {
-        mr[j >> 5] |= 1u << (j & 31);
-        if (d == 0) break;
-        j = d == 1 ? 0 : a.td.off[d - 1] + (j - a.td.off[d]) / a.td.k[d];
-        --d;
-      }
-    }
+    if (r < nrows)
+      for (int j = r / a.G; j >= 0; j = a.td.parent[j]) mr[j >> 5] |= 1u << (j & 31);
   }
   __syncthreads();
 
@@ -315,7 +305,7 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(AmArgs a) {
 
 // Merges the NS partials of every (b, q head, node): one warp per row.
 template <int DH>
-__global__ void __launch_bounds__(256) tree_attn_combine_kernel(AmArgs a) {
+__global__ void __launch_bounds__(256) tree_attn_combine_kernel(const __grid_constant__ AmArgs a) {
   const int lane = threadIdx.x & 31;
   const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // (b, h, i) flattened
   pdl_trigger();
@@ -432,9 +422,8 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   void (*k)(AmArgs) = nullptr;
 #define AM_PICK(D, W, SS) \
   if (p.Dh == D && nw == W && S == SS) k = tree_attn_mma_kernel<D, W, SS>;
-  AM_PICK(128, 4, 2) AM_PICK(128, 8, 2) AM_PICK(128, 12, 2) AM_PICK(128, 4, 4) AM_PICK(128, 8, 4)
-  AM_PICK(128, 12, 4) AM_PICK(64, 4, 2) AM_PICK(64, 8, 2) AM_PICK(64, 12, 2) AM_PICK(64, 4, 4)
-  AM_PICK(64, 8, 4) AM_PICK(64, 12, 4)
+  // head dim 128 runs on the tensor-core kernel (attn_tc.cu)
+  AM_PICK(64, 4, 2) AM_PICK(64, 8, 2) AM_PICK(64, 12, 2) AM_PICK(64, 4, 4) AM_PICK(64, 8, 4) AM_PICK(64, 12, 4)
 #undef AM_PICK
   if (!k) return (int)cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

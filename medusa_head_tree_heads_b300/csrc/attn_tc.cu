@@ -107,7 +107,8 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmKc, const __grid_constant__ CUtensorMap tmVc,
-                        const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt, AtArgs a) {
+                        const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmVt,
+                        const __grid_constant__ AtArgs a) {
   extern __shared__ uint8_t at_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = smem;                                   // [tile] Q tiles
@@ -298,20 +299,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(q_ready);
     }
-    // ancestor-or-self mask of this row's node (closed-form Cartesian layout)
+    // ancestor-or-self mask of this row's node (the chain of parents)
     uint32_t* mr = mrow + (size_t)(t * AT_M + trow) * a.W;
     for (int w = 0; w < a.W; ++w) mr[w] = 0u;
-    if (rvalid) {
-      int j = node, d = 0;
-      for (int e = 1; e <= a.td.D; ++e)
-        if (j >= a.td.off[e]) d = e;
-      while (true) {
-        mr[j >> 5] |= 1u << (j & 31);
-        if (d == 0) break;
-        j = d == 1 ? 0 : a.td.off[d - 1] + (j - a.td.off[d]) / a.td.k[d];
-        --d;
-      }
-    }
+    if (rvalid)
+      for (int j = node; j >= 0; j = a.td.parent[j]) mr[j >> 5] |= 1u << (j & 31);
     const bool warp_live = t < ntiles && (row0 + t * AT_M + q4 * 32) < nrows;  // some row of this warp is real
     const bool tile_live = t < ntiles;
     const uint32_t sbase = tmem + lane_off + t * 2 * AT_BK;

@@ -22,10 +22,18 @@ constexpr int kHeadsTcMaxBatch = 32;  // largest batch of the tensor-core heads 
 // [0, 256): int32 error word at 0, tickets from word 8 on.
 enum Ticket { TICKET_FC = 8, TICKET_PROJ = 9, TICKET_VERIFY = 10 };
 
+// The candidate tree as tables, filled on the host for the Cartesian tree of
+// the per-depth list sizes or for a caller's explicit tree.  Nodes are in
+// (depth, parent, rank) order with node 0 the root, so a node's children are
+// consecutive.  Kernels take them in their grid-constant parameters.
 struct TreeDims {
   int T, n_leaves, W, D;
-  int off[MEDUSA_MAX_DEPTH + 2];  // first node of depth d (off[D+1] = T)
-  int k[MEDUSA_MAX_DEPTH + 1];    // k[d] for d = 1..D
+  int16_t parent[MEDUSA_MAX_NODES];       // -1 for the root
+  uint8_t depth[MEDUSA_MAX_NODES];
+  uint8_t rank[MEDUSA_MAX_NODES];         // rank in the head list of the node's depth (root 0)
+  int16_t first_child[MEDUSA_MAX_NODES];  // first child (children are consecutive), -1 for a leaf
+  uint8_t n_child[MEDUSA_MAX_NODES];
+  int16_t leaf[MEDUSA_MAX_NODES];         // leaf ids, increasing
 };
 
 struct Plan {

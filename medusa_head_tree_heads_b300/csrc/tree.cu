@@ -1,13 +1,13 @@
-// Cartesian candidate tree ("Medusa Heads", "Attenzione sull'albero e
-// accettazione": the heads' best tokens combined by Cartesian product into a
-// prefix-sharing tree; each token may attend only to its own ancestors).
+// Candidate tree ("Medusa Heads", "Attenzione sull'albero e accettazione":
+// the heads' best tokens combined into a prefix-sharing tree -- the Cartesian
+// product of the lists, or a caller's subset of it; each token may attend only
+// to its own ancestors).
 //
-// Layout (closed form, no search): level d holds prod_{j<=d} k_j nodes
-// starting at off[d]; the node with local index m at level d has rank
-// m % k_d in the head-d list and parent off[d-1] + m / k_d (the root for
-// d = 1).  One thread per (sequence, node) fills the tokens; the
-// sequence-independent arrays (parent, depth, rank, pos, mask rows, leaf
-// paths) are written by the first threads.
+// The layout tables (parent, depth, rank, children, leaves) come from the
+// host plan; a node's token is the rank-th entry of the head list of its
+// depth.  One thread per (sequence, node) fills the tokens; the sequence-
+// independent arrays (parent, depth, rank, pos, mask rows, leaf paths) are
+// written by the first threads.
 #include "internal.cuh"
 
 namespace medusa {
@@ -20,21 +20,33 @@ struct TreeArgs {
   medusa_tree_t t;
 };
 
-__device__ __forceinline__ int node_depth(const TreeDims& td, int i) {
-  int d = 0;
-#pragma unroll 1
-  for (int e = 1; e <= td.D; ++e)
-    if (i >= td.off[e]) d = e;
-  return d;
+// mask row word w of node i: the bits of the nodes on its chain to the root
+__device__ __forceinline__ uint32_t mask_word(const TreeDims& td, int i, int w) {
+  uint32_t word = 0;
+  for (int j = i; j >= 0; j = td.parent[j])
+    if ((j >> 5) == w) word |= 1u << (j & 31);
+  return word;
 }
 
-__device__ __forceinline__ int node_parent(const TreeDims& td, int i, int d) {
-  if (d == 0) return -1;
-  const int m = i - td.off[d];
-  return d == 1 ? 0 : td.off[d - 1] + m / td.k[d];
+// the sequence-independent tree arrays, node i / leaf l
+__device__ __forceinline__ void write_node(const TreeDims& td, const medusa_tree_t& t, int L, int i) {
+  t.depth[i] = td.depth[i];
+  t.parent[i] = td.parent[i];
+  t.rank[i] = td.rank[i];
+  t.pos[i] = L + td.depth[i];
+  for (int w = 0; w < td.W; ++w) t.mask[(size_t)i * td.W + w] = mask_word(td, i, w);
+}
+__device__ __forceinline__ void write_path(const TreeDims& td, const medusa_tree_t& t, int l) {
+  const int leaf = td.leaf[l], dl = td.depth[leaf];
+  for (int d = td.D; d > dl; --d) t.paths[(size_t)l * (td.D + 1) + d] = -1;
+  int j = leaf;
+  for (int d = dl; d >= 0; --d) {
+    t.paths[(size_t)l * (td.D + 1) + d] = j;
+    j = td.parent[j];
+  }
 }
 
-__global__ void tree_build_kernel(TreeArgs a) {
+__global__ void tree_build_kernel(const __grid_constant__ TreeArgs a) {
   const TreeDims& td = a.td;
   const int gid = blockIdx.x * blockDim.x + threadIdx.x;
   const int T = td.T;
@@ -42,43 +54,12 @@ __global__ void tree_build_kernel(TreeArgs a) {
   if (gid < a.B * T) {
     pdl_wait();  // the top-k lists come from the previous kernel
     const int b = gid / T, i = gid - b * T;
-    const int d = node_depth(td, i);
-    int tok;
-    if (d == 0) {
-      tok = a.root[b];
-    } else {
-      const int rank = (i - td.off[d]) % td.k[d];
-      tok = a.topk_idx[((size_t)b * a.K + (d - 1)) * a.kmax + rank];
-    }
+    const int d = td.depth[i];
+    const int tok = d == 0 ? a.root[b] : a.topk_idx[((size_t)b * a.K + (d - 1)) * a.kmax + td.rank[i]];
     a.t.token[(size_t)b * T + i] = tok;
   }
-  if (gid < T) {
-    const int i = gid;
-    const int d = node_depth(td, i);
-    a.t.depth[i] = d;
-    a.t.parent[i] = node_parent(td, i, d);
-    a.t.rank[i] = d == 0 ? 0 : (i - td.off[d]) % td.k[d];
-    a.t.pos[i] = a.L + d;
-    // mask row: one 32-bit word at a time, setting the bits of the chain to the root
-    for (int w = 0; w < td.W; ++w) {
-      uint32_t word = 0;
-      int j = i, dj = d;
-      while (j >= 0) {
-        if ((j >> 5) == w) word |= 1u << (j & 31);
-        const int pj = node_parent(td, j, dj);
-        j = pj;
-        dj -= 1;
-      }
-      a.t.mask[(size_t)i * td.W + w] = word;
-    }
-  }
-  if (gid < td.n_leaves) {
-    int j = td.off[td.D] + gid;
-    for (int d = td.D; d >= 0; --d) {
-      a.t.paths[(size_t)gid * (td.D + 1) + d] = j;
-      j = node_parent(td, j, d);
-    }
-  }
+  if (gid < T) write_node(td, a.t, a.L, gid);
+  if (gid < td.n_leaves) write_path(td, a.t, gid);
 }
 
 // ---------------------------------------------------------------------------
@@ -103,7 +84,7 @@ struct MergeTreeArgs {
 __device__ __forceinline__ bool mt_better(float v, int i, float w, int j) { return v > w || (v == w && i < j); }
 
 template <int KM>
-__global__ void __launch_bounds__(256) merge_tree_kernel(MergeTreeArgs a) {
+__global__ void __launch_bounds__(256) merge_tree_kernel(const __grid_constant__ MergeTreeArgs a) {
   __shared__ int s_idx[MEDUSA_MAX_HEADS][MEDUSA_MAX_TOPK];
   const TreeArgs& ta = a.t;
   const TreeDims& td = ta.td;
@@ -198,33 +179,12 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(MergeTreeArgs a) {
   __syncthreads();
   const int T = td.T;
   for (int i = threadIdx.x; i < T; i += blockDim.x) {
-    const int d = node_depth(td, i);
-    ta.t.token[(size_t)b * T + i] = d == 0 ? ta.root[b] : s_idx[d - 1][(i - td.off[d]) % td.k[d]];
-    if (b == 0) {
-      ta.t.depth[i] = d;
-      ta.t.parent[i] = node_parent(td, i, d);
-      ta.t.rank[i] = d == 0 ? 0 : (i - td.off[d]) % td.k[d];
-      ta.t.pos[i] = ta.L + d;
-      for (int w = 0; w < td.W; ++w) {
-        uint32_t word = 0;
-        int j = i, dj = d;
-        while (j >= 0) {
-          if ((j >> 5) == w) word |= 1u << (j & 31);
-          j = node_parent(td, j, dj);
-          dj -= 1;
-        }
-        ta.t.mask[(size_t)i * td.W + w] = word;
-      }
-    }
+    const int d = td.depth[i];
+    ta.t.token[(size_t)b * T + i] = d == 0 ? ta.root[b] : s_idx[d - 1][td.rank[i]];
+    if (b == 0) write_node(td, ta.t, ta.L, i);
   }
   if (b == 0)
-    for (int l = threadIdx.x; l < td.n_leaves; l += blockDim.x) {
-      int j = td.off[td.D] + l;
-      for (int d = td.D; d >= 0; --d) {
-        ta.t.paths[(size_t)l * (td.D + 1) + d] = j;
-        j = node_parent(td, j, d);
-      }
-    }
+    for (int l = threadIdx.x; l < td.n_leaves; l += blockDim.x) write_path(td, ta.t, l);
 }
 
 int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,

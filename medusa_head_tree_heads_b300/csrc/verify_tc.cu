@@ -129,7 +129,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 }
 
 __global__ void __launch_bounds__(VT_THREADS, 1)
-    verify_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, VtcArgs a) {
+    verify_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ VtcArgs a) {
   extern __shared__ uint8_t vt_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(vt_smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
 // folds a strided subset of the vocab tiles (loads issued back to back), then
 // a butterfly joins the 32 lane states.
 template <bool TYPICAL>
-__global__ void __launch_bounds__(256) verify_merge_kernel(VtcArgs a) {
+__global__ void __launch_bounds__(256) verify_merge_kernel(const __grid_constant__ VtcArgs a) {
   const int lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_trigger();
@@ -466,15 +467,11 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(VtcArgs a) {
     }
   }
   if (!TYPICAL) return;
-  // children of this node (closed-form Cartesian layout): the child's token
-  // under this node's softmax at the temperature, against the threshold
+  // children of this node (consecutive nodes): the child's token under this
+  // node's softmax at the temperature, against the threshold
   const int b = n / a.T, i = n - b * a.T;
-  int d = 0;
-  for (int e = 1; e <= a.td.D; ++e)
-    if (i >= a.td.off[e]) d = e;
-  if (d >= a.td.D) return;
-  const int kc = a.td.k[d + 1];
-  const int c0 = a.td.off[d + 1] + (i - a.td.off[d]) * kc;
+  const int kc = a.td.n_child[i];
+  const int c0 = a.td.first_child[i];
   const float logthr = fminf(a.log_eps, a.log_delta - ent);
   const uint4* on = reinterpret_cast<const uint4*>(a.attn_out + (size_t)n * a.H);
   for (int r = 0; r < kc; ++r) {

@@ -42,7 +42,8 @@ class Config(ctypes.Structure):
                 ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_len", ctypes.c_int32), ("kv_capacity", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("accept_mode", ctypes.c_int32), ("temperature", ctypes.c_float), ("eps", ctypes.c_float),
-                ("delta", ctypes.c_float)]
+                ("delta", ctypes.c_float), ("tree_nodes", ctypes.c_int32),
+                ("tree_parent", ctypes.POINTER(ctypes.c_int32)), ("tree_rank", ctypes.POINTER(ctypes.c_int32))]
 
 
 class Tree(ctypes.Structure):
@@ -118,9 +119,23 @@ def make_config(shape, **over) -> Config:
     c.dtype = F32 if shape.dtype == "f32" else BF16
     c.accept_mode = TYPICAL if shape.accept == "typical" else GREEDY
     c.temperature, c.eps, c.delta = shape.temperature, shape.eps, shape.delta
+    parent = getattr(shape, "tree_parent", None)
+    if parent is not None:  # explicit tree: host arrays kept alive with the config
+        rank = shape.tree_rank
+        set_tree(c, parent, rank)
     for k, v in over.items():
         setattr(c, k, v)
     return c
+
+
+def set_tree(c: Config, parent, rank) -> None:
+    """Gives the config an explicit tree (host arrays owned by the config)."""
+    n = len(parent)
+    pa, ra = (ctypes.c_int32 * n)(*parent), (ctypes.c_int32 * n)(*rank)
+    c._tree_arrays = (pa, ra)
+    c.tree_nodes = n
+    c.tree_parent = ctypes.cast(pa, ctypes.POINTER(ctypes.c_int32))
+    c.tree_rank = ctypes.cast(ra, ctypes.POINTER(ctypes.c_int32))
 
 
 def workspace_bytes(cfg: Config) -> int:

@@ -69,6 +69,7 @@ class Shape:
     eps: float = 0.3
     delta: float = 0.09
     full_size: bool = False  # the oracle checks every node only when False
+    sparse_nodes: int = 0  # > 0: an explicit tree of that many non-root nodes (see explicit_tree)
 
     @property
     def depth(self) -> int:
@@ -76,12 +77,23 @@ class Shape:
 
     @property
     def n_nodes(self) -> int:
-        """Tree rows including the root (sizes of the level products, summed)."""
+        """Tree rows including the root (sizes of the level products, summed;
+        for an explicit tree its node count)."""
+        if self.sparse_nodes:
+            return self.sparse_nodes + 1
         total, level = 1, 1
         for k in self.topk:
             level *= k
             total += level
         return total
+
+    @property
+    def tree_parent(self) -> Optional[Tuple[int, ...]]:
+        return explicit_tree(self.topk, self.sparse_nodes)[0] if self.sparse_nodes else None
+
+    @property
+    def tree_rank(self) -> Optional[Tuple[int, ...]]:
+        return explicit_tree(self.topk, self.sparse_nodes)[1] if self.sparse_nodes else None
 
     @property
     def cap(self) -> int:
@@ -90,6 +102,40 @@ class Shape:
     @property
     def torch_dtype(self):
         return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+_TREES: Dict[Tuple, Tuple] = {}
+
+
+def explicit_tree(topk: Sequence[int], n: int) -> Tuple[Tuple[int, ...], Tuple[int, ...]]:
+    """A sparse candidate tree of n non-root nodes taken from the Cartesian
+    tree of ``topk`` (a workload definition, the pages fix no rule): every
+    node scores the product of 1/(rank+1) along its path (a head's lower-ranked
+    candidates are less likely to be right) and the n best nodes are kept,
+    ties to the lower node id, so every kept node's parent is kept.  Returns
+    (parent, rank) in (depth, parent, rank) order, node 0 the root."""
+    key = (tuple(topk), n)
+    if key in _TREES:
+        return _TREES[key]
+    parent, rank, score = [-1], [0], [1.0]
+    level = [0]
+    for d in range(1, len(topk) + 1):
+        nxt = []
+        for p in level:
+            for r in range(topk[d - 1]):
+                parent.append(p)
+                rank.append(r)
+                score.append(score[p] / (r + 1))
+                nxt.append(len(parent) - 1)
+        level = nxt
+    if n > len(parent) - 1:
+        raise ValueError("more nodes than the Cartesian tree has")
+    order = sorted(range(1, len(parent)), key=lambda i: (-score[i], i))
+    keep = sorted([0] + order[:n])
+    new_id = {old: i for i, old in enumerate(keep)}
+    out = (tuple(-1 if i == 0 else new_id[parent[i]] for i in keep), tuple(rank[i] for i in keep))
+    _TREES[key] = out
+    return out
 
 
 # The five stated workloads, then reduced variants that keep every structural
@@ -131,6 +177,19 @@ _add(Shape("gqa-b16-mini", "bf16", 512, 4099, 4, 16, (4, 3, 2, 2), 257, 4, 2, 12
 _add(Shape("33b-b32-mini", "bf16", 320, 1500, 5, 32, (4, 3, 2, 2, 2), 129, 5, 5, 64, "greedy", ("uniform", 0, 5), 2008))
 _add(Shape("13b-b8-split", "bf16", 4096, 5000, 5, 8, (3, 2, 2, 1), 200, 32, 32, 128, "greedy", ("uniform", 0, 4), 2009,
            kv_capacity=211))
+# explicit (sparse) trees: subsets of the Cartesian tree chosen by explicit_tree,
+# with leaves at several depths -- reduced greedy / typical / fp32 variants,
+# the GQA workload with its stated 76 nodes, and the 7B shapes with 64 nodes
+_add(Shape("sparse-mini", "bf16", 256, 777, 4, 3, (4, 3, 2, 2), 70, 2, 1, 128, "greedy", ("uniform", 0, 4), 2010,
+           sparse_nodes=24))
+_add(Shape("sparse-typical-mini", "bf16", 512, 1500, 4, 2, (4, 3, 2, 2), 100, 4, 2, 128, "typical",
+           ("uniform", 0, 4), 2011, sparse_nodes=40))
+_add(Shape("sparse-f32", "f32", 256, 600, 3, 2, (3, 3, 2), 40, 4, 2, 64, "greedy", ("uniform", 0, 3), 2012,
+           sparse_nodes=10))
+_add(Shape("gqa76-bf16", "bf16", 4096, 128256, 4, 16, (4, 3, 2, 2), 4096, 32, 8, 128, "typical", ("uniform", 0, 4),
+           1005, full_size=True, sparse_nodes=76))
+_add(Shape("7b-sparse64", "bf16", 4096, 32000, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3),
+           1006, full_size=True, sparse_nodes=64))
 # profiling case: the 7B shapes with a quarter-sized vocabulary (still far
 # larger than L2) so that counter replays stay small
 _add(Shape("7b-prof", "bf16", 4096, 8192, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3), 4001,

@@ -145,34 +145,47 @@ def topk_lists(logits: np.ndarray, topk: Sequence[int]):
 # ----------------------------------------------------------------- the tree --
 
 class Tree:
-    """Cartesian candidate tree [P1, "Attenzione sull'albero e accettazione"]:
-    the heads' top-k lists combined by Cartesian product, prefixes shared.
-    Nodes are numbered breadth-first: node 0 is the root; the nodes of depth d
-    follow those of depth d-1, ordered by parent, then by rank in the head-d
-    list.  Every branch at depth d takes the same head-d list."""
+    """Candidate tree [P1, "Attenzione sull'albero e accettazione"]: the
+    heads' top-k lists combined by Cartesian product, prefixes shared -- or,
+    given ``parent``/``rank``, an explicit subset of that tree (fewer
+    branches, same structure).  Nodes are numbered breadth-first: node 0 is the
+    root; the nodes of depth d follow those of depth d-1, ordered by parent,
+    then by rank in the head-d list.  A node of rank r at depth d carries head
+    d's r-th candidate."""
 
-    def __init__(self, topk: Sequence[int]):
+    def __init__(self, topk: Sequence[int], parent: Optional[Sequence[int]] = None,
+                 rank: Optional[Sequence[int]] = None):
         self.topk = list(topk)
         self.depth_max = len(self.topk)
-        parent, depth, rank = [-1], [0], [0]
-        level = [0]
-        for d in range(1, self.depth_max + 1):
-            nxt = []
-            for p in level:
-                for r in range(self.topk[d - 1]):
-                    parent.append(p)
-                    depth.append(d)
-                    rank.append(r)
-                    nxt.append(len(parent) - 1)
-            level = nxt
+        if parent is None:
+            parent, depth, rank = [-1], [0], [0]
+            level = [0]
+            for d in range(1, self.depth_max + 1):
+                nxt = []
+                for p in level:
+                    for r in range(self.topk[d - 1]):
+                        parent.append(p)
+                        depth.append(d)
+                        rank.append(r)
+                        nxt.append(len(parent) - 1)
+                level = nxt
+        else:
+            parent, rank = list(parent), list(rank)
+            assert parent[0] == -1 and rank[0] == 0
+            depth = [0]
+            for i in range(1, len(parent)):
+                assert 0 <= parent[i] < i
+                depth.append(depth[parent[i]] + 1)
+                assert depth[i] <= self.depth_max and 0 <= rank[i] < self.topk[depth[i] - 1]
+                assert (depth[i - 1], parent[i - 1], rank[i - 1]) < (depth[i], parent[i], rank[i])
         self.parent = np.array(parent, dtype=np.int32)
         self.depth = np.array(depth, dtype=np.int32)
         self.rank = np.array(rank, dtype=np.int32)
         self.T = len(parent)
-        self.leaves = level
         self.children: List[List[int]] = [[] for _ in range(self.T)]
         for i in range(1, self.T):
             self.children[parent[i]].append(i)
+        self.leaves = [i for i in range(self.T) if not self.children[i]]
         # R2: node i sees exactly the nodes on its chain to the root, itself included
         self.mask = np.zeros((self.T, self.T), dtype=bool)
         for i in range(self.T):
@@ -180,7 +193,14 @@ class Tree:
             while j >= 0:
                 self.mask[i, j] = True
                 j = parent[j]
-        self.paths = np.array([self.chain(l) for l in self.leaves], dtype=np.int32)
+        # root-to-leaf node ids, -1 after a leaf shallower than the tree depth
+        self.paths = np.array([self.chain(l) + [-1] * (self.depth_max + 1 - len(self.chain(l)))
+                               for l in self.leaves], dtype=np.int32).reshape(len(self.leaves), self.depth_max + 1)
+
+    @classmethod
+    def for_shape(cls, shape) -> "Tree":
+        """The workload's tree: Cartesian, or its explicit parent/rank lists."""
+        return cls(shape.topk, getattr(shape, "tree_parent", None), getattr(shape, "tree_rank", None))
 
     def chain(self, i: int) -> List[int]:
         """Nodes from the root down to i."""
@@ -345,7 +365,7 @@ def step(inp: Dict[str, np.ndarray], shape, nodes_only: Optional[Dict[int, Seque
     z = head_hidden(inp["h"], inp["W1"], inp["b1"])
     logits = head_logits(z, inp["W2"])
     idx, val = topk_lists(logits, topk)
-    tree = Tree(topk)
+    tree = Tree.for_shape(shape)
     tok = tree.tokens(idx, inp["root_token"])
     B, T = tok.shape
     H = shape.hidden

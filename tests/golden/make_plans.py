@@ -67,7 +67,7 @@ def build_plan(s: synth.Shape, log=print) -> dict:
     Wn = {k: to_np(v) for k, v in W.items()}
     B, D, T = s.batch, s.depth, s.n_nodes
     topk = list(s.topk)
-    tree = O.Tree(topk)
+    tree = O.Tree.for_shape(s)
 
     # 1. h redraws until the head top-k boundaries have margins
     redraw = [0] * B
@@ -98,9 +98,12 @@ def build_plan(s: synth.Shape, log=print) -> dict:
         path = [0]
         plant = []
         for j in range(1, d + 1):
-            r = int(rng.integers(0, topk[j - 1]))
-            child = tree.children[path[-1]][r]
-            plant.append([path[-1], int(topk_idx[b, j - 1, r])])
+            kids = tree.children[path[-1]]
+            if not kids:  # an explicit tree's leaf above the drawn depth ends the path
+                d = j - 1
+                break
+            child = kids[int(rng.integers(0, len(kids)))]
+            plant.append([path[-1], int(topk_idx[b, j - 1, tree.rank[child]])])
             path.append(child)
         excluded = set(topk_idx[b, d, :topk[d]].tolist()) if d < D else set()
         while True:

@@ -44,9 +44,12 @@ def test_tree_size_closed_form(name):
     cfg = M.make_config(s)
     T, NL, W = M.tree_size(cfg)
     assert T == s.n_nodes
-    n = 1
-    for k in s.topk:
-        n *= k
+    if s.tree_parent is None:  # Cartesian: the product of the list sizes
+        n = 1
+        for k in s.topk:
+            n *= k
+    else:  # explicit: the nodes that are nobody's parent
+        n = T - len(set(s.tree_parent[1:]))
     assert NL == n
     assert W == (T + 31) // 32
     assert M.workspace_bytes(cfg) > 0
@@ -79,6 +82,37 @@ def test_topk_and_node_limits():
     assert M.lib().medusa_tree_size(ctypes.byref(cfg), None, None, None) == -2
     cfg = M.make_config(synth.SHAPES["wide-bf16"])
     cfg.topk[2] = 8  # 8 + 64 + 512 nodes: above 512
+    assert M.lib().medusa_tree_size(ctypes.byref(cfg), None, None, None) == -2
+
+
+BAD_TREES = [  # (parent, rank) for topk (2, 2): each breaks one rule of the explicit tree
+    ([0, 0, 0], [0, 0, 1]),          # root's parent is not -1
+    ([-1, 0, 1, 0], [0, 0, 0, 1]),   # (depth, parent, rank) order broken: depth 2 before depth 1
+    ([-1, 0, 0], [0, 1, 0]),         # ranks under one parent out of order
+    ([-1, 0, 0], [0, 0, 0]),         # the same child twice
+    ([-1, 0, 3, 0], [0, 0, 0, 1]),   # parent after the node
+    ([-1, 0, 0], [0, 0, 2]),         # rank beyond the depth-1 list (k = 2)
+    ([-1, 0, 1, 2], [0, 0, 0, 0]),   # depth 3 in a depth-2 tree
+]
+
+
+@pytest.mark.parametrize("parent,rank", BAD_TREES)
+def test_invalid_explicit_trees_are_rejected(parent, rank):
+    s = synth.SHAPES["7b-mini"]
+    cfg = M.make_config(s, depth=2)
+    cfg.topk[0], cfg.topk[1] = 2, 2
+    M.set_tree(cfg, parent, rank)
+    assert M.lib().medusa_tree_size(ctypes.byref(cfg), None, None, None) == -1, (parent, rank)
+    assert M.workspace_bytes(cfg) == 0
+
+
+def test_explicit_tree_sizes_and_limits():
+    s = synth.SHAPES["7b-mini"]
+    cfg = M.make_config(s, depth=2)
+    cfg.topk[0], cfg.topk[1] = 2, 2
+    M.set_tree(cfg, [-1, 0, 0, 1], [0, 0, 1, 0])  # a depth-1 leaf and a depth-2 leaf
+    assert M.tree_size(cfg) == (4, 2, 1)
+    cfg.tree_nodes = 513  # above 512
     assert M.lib().medusa_tree_size(ctypes.byref(cfg), None, None, None) == -2
 
 

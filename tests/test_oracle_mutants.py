@@ -64,18 +64,45 @@ def _topk_high_tie(logits, topk):
 class _DescTree(O.Tree):
     """mask transposed: a node sees its descendants instead of its ancestors"""
 
-    def __init__(self, topk):
-        super().__init__(topk)
+    def __init__(self, topk, parent=None, rank=None):
+        super().__init__(topk, parent, rank)
         self.mask = self.mask.T.copy()
 
 
 class _NoSelfTree(O.Tree):
     """mask without the node itself"""
 
-    def __init__(self, topk):
-        super().__init__(topk)
+    def __init__(self, topk, parent=None, rank=None):
+        super().__init__(topk, parent, rank)
         np.fill_diagonal(self.mask, False)
         self.mask[0, 0] = True
+
+
+class _DeepLeavesTree(O.Tree):
+    """shallow leaves of an explicit tree dropped (paths only at full depth)"""
+
+    def __init__(self, topk, parent=None, rank=None):
+        super().__init__(topk, parent, rank)
+        keep = [i for i, l in enumerate(self.leaves) if self.depth[l] == self.depth_max]
+        self.leaves = [self.leaves[i] for i in keep]
+        self.paths = self.paths[keep]
+
+
+def _typical_last_longest(tree, tokens_b, argmax_b, keep_edge):
+    # ties to the LAST longest chain met (the highest node at the first divergence)
+    best = [0]
+
+    def walk(path):
+        nonlocal best
+        if len(path) >= len(best):
+            best = list(path)
+        for c in tree.children[path[-1]]:
+            if keep_edge(path[-1], c):
+                walk(path + [c])
+
+    walk([0])
+    toks = [int(tokens_b[n]) for n in best[1:]]
+    return len(toks), toks, best, int(argmax_b[best[-1]])
 
 
 def _attn_scale_dh(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=None, batches=None):
@@ -135,6 +162,9 @@ MUTANTS = [
     ("greedy compares the child's own argmax", dict(accept_greedy=_greedy_child_argmax), P.check_greedy_lossless),
     ("argmax ties to the last index", dict(verify_stats=_argmax_last), P.check_verify),
     ("threshold without exp", dict(typical_threshold=_threshold_no_exp), P.check_verify),
+    ("explicit tree loses its shallow leaves", dict(Tree=_DeepLeavesTree), P.check_explicit_tree),
+    ("typical ties to the last longest chain", dict(accept_typical=_typical_last_longest),
+     P.check_typical_shallow_tie),
 ]
 
 

@@ -139,15 +139,22 @@ def _rand_attn_inputs(seed, B, T, Hq, Hkv, Dh, L, cap):
 def check_attention_paths(M) -> None:
     """Tree attention equals, at every node of every root-to-leaf path, causal
     attention over (cache ++ path) computed by torch's scaled_dot_product_attention
-    (one pass over all branches gives what each branch alone would)."""
+    (one pass over all branches gives what each branch alone would) -- for a
+    Cartesian tree and for a sparse one with leaves at several depths."""
     topk = (3, 2, 2)
-    t = M.Tree(topk)
+    parent, rank = synth.explicit_tree(topk, 7)
+    for t in (M.Tree(topk), M.Tree(topk, parent, rank)):
+        _attention_paths_one(M, t)
+
+
+def _attention_paths_one(M, t) -> None:
     B, Hq, Hkv, Dh, L, cap = 2, 4, 2, 16, 11, 13
     q, kt, vt, kc, vc = _rand_attn_inputs(1, B, t.T, Hq, Hkv, Dh, L, cap)
     o = M.tree_attention(q, kt, vt, kc, vc, L, t.mask)
     G = Hq // Hkv
     for b in range(B):
-        for path in t.paths:
+        for row in t.paths:
+            path = [int(x) for x in row if x >= 0]
             n = len(path)
             for h in range(Hq):
                 g = h // G
@@ -289,10 +296,55 @@ def check_typical_special_cases(M) -> None:
     assert n == 0
 
 
+def check_explicit_tree(M) -> None:
+    """An explicit parent/rank tree: the explicit form of a Cartesian tree is
+    that tree; for a sparse subset, every node's depth is the length of its
+    chain of parents, its mask row is that chain, the leaves are the nodes no
+    node names as parent (some shallower than the tree depth) and every path
+    row is a leaf's chain followed by -1."""
+    for topk in [(2, 3), (3, 2, 2), (1, 1, 1), ()]:
+        t = M.Tree(topk)
+        e = M.Tree(topk, t.parent.tolist(), t.rank.tolist())
+        for f in ("parent", "depth", "rank", "mask", "paths"):
+            np.testing.assert_array_equal(getattr(e, f), getattr(t, f))
+        assert e.leaves == t.leaves
+    topk = (4, 3, 2, 2)
+    parent, rank = synth.explicit_tree(topk, 24)
+    t = M.Tree(topk, parent, rank)
+
+    def walk(i):
+        out = []
+        while i >= 0:
+            out.append(i)
+            i = parent[i]
+        return out[::-1]
+
+    for i in range(len(parent)):
+        ch = walk(i)
+        assert t.depth[i] == len(ch) - 1
+        assert set(np.nonzero(t.mask[i])[0].tolist()) == set(ch)
+    leaves = [i for i in range(len(parent)) if i not in set(parent[1:])]
+    assert t.leaves == leaves and len({int(t.depth[l]) for l in leaves}) > 1
+    assert len(t.paths) == len(leaves)
+    for row, l in zip(t.paths.tolist(), leaves):
+        ch = walk(l)
+        assert row == ch + [-1] * (len(topk) + 1 - len(ch))
+
+
+def check_typical_shallow_tie(M) -> None:
+    """Equal kept lengths go to the lower node at the first divergence, also
+    when the other branch ends in a shallower leaf with a lower node id."""
+    t = M.Tree((2, 2), [-1, 0, 0, 1], [0, 0, 1, 0])  # node 2 is a depth-1 leaf, node 3 a child of node 1
+    tok = np.array([9, 1, 2, 3], dtype=np.int32)
+    n, toks, nodes, _ = M.accept_typical(t, tok, np.zeros(4, dtype=np.int64), lambda p, c: c != 3)
+    assert n == 1 and nodes == [0, 1] and toks == [1]
+
+
 def check_plans(M) -> None:
     """On every reduced workload the oracle realises the planted acceptance."""
     plans = synth.load_plans()
-    for name in ["tiny-fp32", "tiny-fp32-gqa", "7b-mini", "13b-mini", "gqa-mini", "33b-mini"]:
+    for name in ["tiny-fp32", "tiny-fp32-gqa", "7b-mini", "13b-mini", "gqa-mini", "33b-mini", "sparse-mini",
+                 "sparse-typical-mini", "sparse-f32"]:
         s = synth.SHAPES[name]
         inp = {k: to_np(v) for k, v in synth.make_inputs(s, plans[name]).items()}
         res = M.step(inp, s)
@@ -335,7 +387,8 @@ def check_silu(M) -> None:
 
 CHECKS = [check_zero_init, check_head_vs_torch, check_topk, check_tree_2x3, check_tree_invariants,
           check_attention_paths, check_attention_single_node, check_verify, check_greedy_lossless,
-          check_typical_special_cases, check_plans, check_bf16_rounding, check_silu]
+          check_typical_special_cases, check_plans, check_bf16_rounding, check_silu, check_explicit_tree,
+          check_typical_shallow_tie]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)

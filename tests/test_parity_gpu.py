@@ -193,7 +193,7 @@ def test_full_size_sampled(name):
     live = idx >= 0
     U.assert_close(res["topk_val"].numpy()[live], val[live], s.dtype, "topk_val")
     # the tree: everything
-    tree = O.Tree(s.topk)
+    tree = O.Tree.for_shape(s)
     np.testing.assert_array_equal(res["tree"]["token"].numpy(), tree.tokens(idx, n["root_token"]))
     np.testing.assert_array_equal(res["tree"]["parent"].numpy(), tree.parent)
     np.testing.assert_array_equal(res["tree"]["mask"].numpy().view(np.uint32), U.pack_mask(tree.mask))
