@@ -142,6 +142,11 @@ typedef struct {
   int32_t* acc_tokens;     /* [B][D] */
   int32_t* acc_nodes;      /* [B][D+1] */
   int32_t* bonus;          /* [B] */
+  /* optional: per-sequence cache lengths (device [B], each in [0, kv_capacity];
+   * the config's kv_len still sizes the key splits).  NULL: kv_len for all.
+   * Cache rows past a sequence's length must hold finite values (e.g. zeros
+   * from allocation): their keys are masked and their values weighted 0. */
+  const int32_t* kv_lens;
 } medusa_step_io_t;
 
 /* Bytes of device workspace the calls below need for this config (0 on an
@@ -190,8 +195,8 @@ int medusa_heads_topk_noalloc(const medusa_config_t* cfg, const void* h, const v
  *   o = sum_j softmax_j(q.k_j / sqrt(Dh)) v_j
  * over the L cache rows and the tree nodes j with mask[i] bit j.
  * attn_out [B][T][H] holds o of q head h at columns h*Dh .. h*Dh+Dh-1, in the
- * config's dtype.  Only tree->mask is read (the bf16 kernel derives the same
- * ancestor-or-self relation from the config's Cartesian layout). */
+ * config's dtype.  Only tree->mask is read (the bf16 kernels derive the same
+ * ancestor-or-self relation from the config's tree). */
 int medusa_tree_attn(const medusa_config_t* cfg, const void* q, const void* k_tree, const void* v_tree,
                      const void* k_cache, const void* v_cache, const medusa_tree_t* tree, void* attn_out,
                      void* workspace, void* stream);
@@ -212,6 +217,33 @@ int medusa_verify_accept(const medusa_config_t* cfg, const void* attn_out, const
                          const medusa_tree_t* tree, int32_t* node_argmax, float* node_maxlogit, float* node_lse,
                          float* node_entropy, int32_t* accept_len, int32_t* acc_tokens, int32_t* acc_nodes,
                          int32_t* bonus, void* workspace, void* stream);
+
+/* medusa_tree_attn with a per-sequence cache length kv_lens[b] (device [B],
+ * each in [0, kv_capacity]; see medusa_step_io_t.kv_lens).  A length outside
+ * that range sets MEDUSA_ERR_DEVICE and is clamped. */
+int medusa_tree_attn_lens(const medusa_config_t* cfg, const void* q, const void* k_tree, const void* v_tree,
+                          const void* k_cache, const void* v_cache, const int32_t* kv_lens,
+                          const medusa_tree_t* tree, void* attn_out, void* workspace, void* stream);
+
+/* KV commit: the accepted branch ("Attenzione sull'albero e accettazione": the
+ * kept branch is appended and feeds the next round) moves into the cache.  For
+ * each sequence b with n = accept_len[b]: the key and value rows of nodes
+ * acc_nodes[b][0..n] (root first) are copied from k_tree / v_tree to cache rows
+ * kv_lens[b] .. kv_lens[b] + n, then kv_lens[b] += n + 1 (device array, in and
+ * out).  A node id outside the tree, n outside [0, depth] or a cache without
+ * room sets MEDUSA_ERR_DEVICE and leaves that sequence unchanged.  The pages
+ * give no such call; it is the step after acceptance. */
+int medusa_kv_commit(const medusa_config_t* cfg, const int32_t* acc_nodes, const int32_t* accept_len,
+                     const void* k_tree, const void* v_tree, void* k_cache, void* v_cache, int32_t* kv_lens,
+                     void* workspace, void* stream);
+
+/* Next-round inputs: h_next[b] ([B][H], config dtype) = attn_out[b][node] for the
+ * last accepted node node = acc_nodes[b][accept_len[b]] (the tree output the
+ * base lm_head read), root_next[b] = bonus[b].  Bad indices set
+ * MEDUSA_ERR_DEVICE.  The pages give no such call; it is the step after. */
+int medusa_next_inputs(const medusa_config_t* cfg, const void* attn_out, const int32_t* acc_nodes,
+                       const int32_t* accept_len, const int32_t* bonus, void* h_next, int32_t* root_next,
+                       void* workspace, void* stream);
 
 /* The whole step: heads_topk, tree_build, tree_attn, verify_accept, in order on
  * `stream`.  io is host memory holding device pointers. */

@@ -272,8 +272,49 @@ int medusa_tree_attn(const medusa_config_t* cfg, const void* q, const void* k_tr
     return MEDUSA_ERR_INVALID_ARG;
   if (p.L > 0 && (!aligned16(k_cache) || !aligned16(v_cache))) return MEDUSA_ERR_INVALID_ARG;
   finish_plan(&p);
-  return cuda_status(launch_tree_attn(p, q, k_tree, v_tree, k_cache, v_cache, tree->mask, attn_out,
+  return cuda_status(launch_tree_attn(p, q, k_tree, v_tree, k_cache, v_cache, nullptr, tree->mask, attn_out,
                                       (uint8_t*)workspace, (cudaStream_t)stream));
+}
+
+int medusa_tree_attn_lens(const medusa_config_t* cfg, const void* q, const void* k_tree, const void* v_tree,
+                          const void* k_cache, const void* v_cache, const int32_t* kv_lens,
+                          const medusa_tree_t* tree, void* attn_out, void* workspace, void* stream) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(attn_out) || !tree || !tree->mask ||
+      !kv_lens || !aligned16(workspace))
+    return MEDUSA_ERR_INVALID_ARG;
+  if (p.Lc > 0 && (!aligned16(k_cache) || !aligned16(v_cache))) return MEDUSA_ERR_INVALID_ARG;
+  finish_plan(&p);
+  return cuda_status(launch_tree_attn(p, q, k_tree, v_tree, k_cache, v_cache, kv_lens, tree->mask, attn_out,
+                                      (uint8_t*)workspace, (cudaStream_t)stream));
+}
+
+int medusa_kv_commit(const medusa_config_t* cfg, const int32_t* acc_nodes, const int32_t* accept_len,
+                     const void* k_tree, const void* v_tree, void* k_cache, void* v_cache, int32_t* kv_lens,
+                     void* workspace, void* stream) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!acc_nodes || !accept_len || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !kv_lens || !aligned16(workspace))
+    return MEDUSA_ERR_INVALID_ARG;
+  return cuda_status(launch_kv_commit(p, acc_nodes, accept_len, k_tree, v_tree, k_cache, v_cache, kv_lens,
+                                      (uint8_t*)workspace, (cudaStream_t)stream));
+}
+
+int medusa_next_inputs(const medusa_config_t* cfg, const void* attn_out, const int32_t* acc_nodes,
+                       const int32_t* accept_len, const int32_t* bonus, void* h_next, int32_t* root_next,
+                       void* workspace, void* stream) {
+  Plan p;
+  int s = make_plan(cfg, &p);
+  if (s != MEDUSA_OK) return s;
+  if (!aligned16(attn_out) || !acc_nodes || !accept_len || !bonus || !aligned16(h_next) || !root_next ||
+      !aligned16(workspace))
+    return MEDUSA_ERR_INVALID_ARG;
+  return cuda_status(launch_next_inputs(p, attn_out, acc_nodes, accept_len, bonus, h_next, root_next,
+                                        (uint8_t*)workspace, (cudaStream_t)stream));
 }
 
 int medusa_verify_accept(const medusa_config_t* cfg, const void* attn_out, const void* lm_head,
@@ -312,7 +353,8 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
       !io->node_maxlogit || !io->accept_len || !io->acc_tokens || !io->acc_nodes || !io->bonus ||
       !aligned16(workspace))
     return MEDUSA_ERR_INVALID_ARG;
-  if (p.L > 0 && (!aligned16(io->k_cache) || !aligned16(io->v_cache))) return MEDUSA_ERR_INVALID_ARG;
+  if ((p.L > 0 || (io->kv_lens && p.Lc > 0)) && (!aligned16(io->k_cache) || !aligned16(io->v_cache)))
+    return MEDUSA_ERR_INVALID_ARG;
   if (p.typical && (!io->node_lse || !io->node_entropy)) return MEDUSA_ERR_INVALID_ARG;
   if ((s = check_tree(p, &io->tree)) != MEDUSA_OK) return s;
   if (events && n_events < 2 * MEDUSA_STEP_KERNELS) return MEDUSA_ERR_INVALID_ARG;
@@ -344,8 +386,8 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
     MEDUSA_STAGE(launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
     MEDUSA_STAGE(launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
   }
-  MEDUSA_STAGE(launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->tree.mask,
-                                io->attn_out, ws, st))
+  MEDUSA_STAGE(launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens,
+                                io->tree.mask, io->attn_out, ws, st))
   MEDUSA_STAGE(launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit, io->node_lse,
                              io->node_entropy, ws, st))
   MEDUSA_STAGE(launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse,

@@ -28,6 +28,8 @@ struct AttnArgs {
   void* out;             // [B][T][H]
   int B, T, W, Hq, Hkv, G, L, Lc, H;
   float qscale;  // log2(e) / sqrt(Dh)
+  const int32_t* lens;  // [B] per-sequence cache lengths, or null (L for all)
+  uint8_t* ws;
 };
 
 template <typename TT, int DH>
@@ -68,12 +70,13 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
     for (int t = 0; t < DPL; ++t) acc[rr][t] = 0.f;
   }
 
-  const int n_cache_tiles = (a.L + AT_KT - 1) / AT_KT;
+  const int Lb = seq_len(a.lens, b, a.L, a.Lc, a.ws);
+  const int n_cache_tiles = (Lb + AT_KT - 1) / AT_KT;
   const int n_tree_tiles = (a.T + AT_KT - 1) / AT_KT;
   for (int tile = 0; tile < n_cache_tiles + n_tree_tiles; ++tile) {
     const bool is_tree = tile >= n_cache_tiles;
     const int k0 = is_tree ? (tile - n_cache_tiles) * AT_KT : tile * AT_KT;
-    const int nk = is_tree ? min(AT_KT, a.T - k0) : min(AT_KT, a.L - k0);
+    const int nk = is_tree ? min(AT_KT, a.T - k0) : min(AT_KT, Lb - k0);
     __syncthreads();
     for (int e = threadIdx.x; e < AT_KT * DH; e += blockDim.x) {
       const int j = e / DH, d = e - j * DH;
@@ -143,9 +146,9 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
 
 // bf16: tensor-core kernel (attn_mma.cu); fp32: this CUDA-core kernel (no TF32)
 int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                     const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st) {
-  if (attn_tc_supported(p)) return launch_tree_attn_tc(p, q, kt, vt, kc, vc, out, ws, st);
-  if (p.bf16) return launch_tree_attn_mma(p, q, kt, vt, kc, vc, out, ws, st, false);
+                     const int32_t* lens, const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st) {
+  if (attn_tc_supported(p)) return launch_tree_attn_tc(p, q, kt, vt, kc, vc, lens, out, ws, st);
+  if (p.bf16) return launch_tree_attn_mma(p, q, kt, vt, kc, vc, lens, out, ws, st);
   AttnArgs a;
   a.q = q;
   a.kt = kt;
@@ -164,6 +167,8 @@ int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* v
   a.Lc = p.Lc;
   a.H = p.H;
   a.qscale = 1.4426950408889634f / sqrtf((float)p.Dh);
+  a.lens = lens;
+  a.ws = ws;
   dim3 grid((p.T * p.G + AT_ROWS - 1) / AT_ROWS, p.Hkv, p.B);
   const size_t smem = (size_t)(AT_ROWS * p.Dh + AT_KT * (p.Dh + 1) + AT_KT * p.Dh) * sizeof(float);
   void (*k)(AttnArgs);

@@ -36,6 +36,8 @@ struct AmArgs {
   float* part_o;   // [B][Hq][T][NS][Dh] unnormalised partial outputs (split mode)
   float2* part_ml; // [B][Hq][T][NS] (running max in log2 units, sum)
   float qscale;    // log2(e) / sqrt(Dh)
+  const int32_t* lens;  // [B] per-sequence cache lengths, or null (L for all)
+  uint8_t* ws;
 };
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
@@ -125,7 +127,8 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(const __grid_
   for (int j = 0; j < ND; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float mrow_m[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
-  const int nb_cache = (a.L + AM_KB - 1) / AM_KB;
+  const int Lb = seq_len(a.lens, b, a.L, a.Lc, a.ws);
+  const int nb_cache = (Lb + AM_KB - 1) / AM_KB;
   const int nb_tree = (a.T + AM_KB - 1) / AM_KB;
   // this CTA's key blocks [blk_lo, blk_hi) of (cache blocks, then tree blocks)
   // split sp takes an equal share of the concatenated (cache, tree) block list
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(const __grid_
   auto load_block = [&](int blk, int buf) {
     const bool tree = blk >= nb_cache;
     const int k0 = tree ? (blk - nb_cache) * AM_KB : blk * AM_KB;
-    const int nk = tree ? min(AM_KB, a.T - k0) : min(AM_KB, a.L - k0);
+    const int nk = tree ? min(AM_KB, a.T - k0) : min(AM_KB, Lb - k0);
     const __nv_bfloat16* kb = tree ? a.kt + ((size_t)b * a.T) * kv_row : a.kc + ((size_t)b * a.Lc) * kv_row;
     const __nv_bfloat16* vb = tree ? a.vt + ((size_t)b * a.T) * kv_row : a.vc + ((size_t)b * a.Lc) * kv_row;
     constexpr int CH = DH / 8;  // 16-byte chunks per row
@@ -167,7 +170,7 @@ __global__ void __launch_bounds__(NW * 32, 1) tree_attn_mma_kernel(const __grid_
 
     const bool tree = blk >= nb_cache;
     const int k0 = tree ? (blk - nb_cache) * AM_KB : blk * AM_KB;
-    const int nk = tree ? min(AM_KB, a.T - k0) : min(AM_KB, a.L - k0);
+    const int nk = tree ? min(AM_KB, a.T - k0) : min(AM_KB, Lb - k0);
     const __nv_bfloat16* Kb = Ks + (size_t)buf * AM_KB * LD;
     const __nv_bfloat16* Vb = Vs + (size_t)buf * AM_KB * LD;
     if (rbase >= nrows) {  // all 16 rows of this warp are padding: no math, keep the barriers
@@ -321,7 +324,8 @@ __global__ void __launch_bounds__(256) tree_attn_combine_kernel(const __grid_con
   for (int t = 0; t < DH / 32; ++t) acc[t] = 0.f;
   for (int s = 0; s < a.NS; ++s) {
     const float2 ml = a.part_ml[row * a.NS + s];
-    const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - mx);
+    if (ml.x == -INFINITY) continue;  // a split that saw no key (its partial output is not read)
+    const float w = exp2f(ml.x - mx);
     l += w * ml.y;
     const float* po = a.part_o + (row * a.NS + s) * DH;
 #pragma unroll
@@ -379,11 +383,8 @@ size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh) {
   return rows * Dh * sizeof(float) + rows * sizeof(float2) + 256;
 }
 
-// overlap: launched (with programmatic dependent launch) right after the head
-// projection, sized to share the projection's SMs (4 warps, 2-block ring, no
-// key split); otherwise a plain stream-ordered launch sized for the whole GPU.
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                         void* out, uint8_t* ws, cudaStream_t st, bool overlap) {
+                         const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st) {
   AmArgs a;
   a.q = (const __nv_bfloat16*)q;
   a.kt = (const __nv_bfloat16*)kt;
@@ -402,21 +403,19 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   a.Lc = p.Lc;
   a.H = p.H;
   a.qscale = 1.4426950408889634f / sqrtf((float)p.Dh);
+  a.lens = lens;
+  a.ws = ws;
   attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &a.NS, &a.chunk_blks);
-  if (overlap) {
-    a.NS = 1;
-    a.chunk_blks = (p.L + AM_KB - 1) / AM_KB + (p.T + AM_KB - 1) / AM_KB;
-  }
   const size_t rows_all = (size_t)p.B * p.Hq * p.T * a.NS;
   a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);
   a.part_ml = reinterpret_cast<float2*>(ws + p.off_attn_part + rows_all * p.Dh * sizeof(float));
   const int rows = p.T * p.G;
-  const int nw = overlap ? 4 : attn_warps(rows);
+  const int nw = attn_warps(rows);
   dim3 grid((rows + 16 * nw - 1) / (16 * nw), p.Hkv * a.NS, p.B);
   // a 4-block ring (one CTA per SM) when the grid is a single wave, else a
   // 2-block ring so that several CTAs share an SM
   const int ctas = (int)(grid.x * grid.y * grid.z);
-  const int S = (!overlap && ctas <= p.sm_count) ? 4 : 2;
+  const int S = ctas <= p.sm_count ? 4 : 2;
   const size_t smem = (size_t)2 * S * AM_KB * (p.Dh + 8) * sizeof(__nv_bfloat16) +
                       (size_t)16 * nw * p.W * sizeof(uint32_t);
   void (*k)(AmArgs) = nullptr;
@@ -430,7 +429,7 @@ int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const voi
   if (e != cudaSuccess) return (int)e;
   e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return (int)e;
-  e = launch_k(k, grid, dim3(nw * 32), smem, st, overlap, a);
+  e = launch_k(k, grid, dim3(nw * 32), smem, st, false, a);
   if (e != cudaSuccess || a.NS == 1) return (int)e;
   const size_t nrow = (size_t)p.B * p.Hq * p.T;
   const unsigned cgrid = (unsigned)((nrow + 7) / 8);

@@ -62,6 +62,8 @@ struct AtArgs {
   float2* part_ml;
   float qscale;  // log2(e) / sqrt(Dh)
   uint8_t* ws;
+  const int32_t* lens;  // [B] per-sequence cache lengths, or null (L for all)
+  int Lc;
 };
 
 __device__ __forceinline__ uint32_t at_sw(int r, int unit) {  // byte offset of 16-byte unit `unit` of row r
@@ -135,7 +137,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const int nrows = a.T * a.G;
   const int row0 = blockIdx.x * AT_ROWS;
   const int ntiles = min(AT_TILES, (nrows - row0 + AT_M - 1) / AT_M);
-  const int nb_cache = (a.L + AT_BK - 1) / AT_BK;
+  const int Lb = seq_len(a.lens, b, a.L, a.Lc, a.ws);
+  const int nb_cache = (Lb + AT_BK - 1) / AT_BK;
   const int nb_all = nb_cache + (a.T + AT_BK - 1) / AT_BK;
   const int blk_lo = (int)(((long long)sp * nb_all) / a.NS);
   const int blk_hi = (int)(((long long)(sp + 1) * nb_all) / a.NS);
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       const int blk = blk_lo + i;
       const bool tree = blk >= nb_cache;
       const int k0 = tree ? (blk - nb_cache) * AT_BK : blk * AT_BK;
-      const int nk = tree ? min(AT_BK, a.T - k0) : min(AT_BK, a.L - k0);
+      const int nk = tree ? min(AT_BK, a.T - k0) : min(AT_BK, Lb - k0);
       uint32_t mw0 = 0u, mw1 = 0u;  // mask words of the block's 64 keys
       if (tree) {
         const int wi = k0 >> 5;
@@ -466,6 +469,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           *reinterpret_cast<uint4*>(op + c * 16 + 8) = w1;
         }
       }
+    } else if (ok && warp_live && nblk == 0 && a.NS > 1 && rvalid) {  // a split with no key block
+      a.part_ml[(((size_t)b * a.Hq + hq) * a.T + node) * a.NS + sp] = make_float2(-INFINITY, 0.f);
     } else if (!ok && tile_live && lane == 0) {
       set_error(a.ws, MEDUSA_ERR_TIMEOUT);
     }
@@ -544,7 +549,7 @@ bool attn_tc_supported(const Plan& p) { return p.bf16 && p.Dh == AT_DH; }
 int launch_attn_combine(const Plan& p, float* part_o, float2* part_ml, int NS, void* out, cudaStream_t st);
 
 int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                        void* out, uint8_t* ws, cudaStream_t st) {
+                        const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st) {
   AtArgs a;
   a.q = (const __nv_bfloat16*)q;
   a.out = (__nv_bfloat16*)out;
@@ -559,6 +564,8 @@ int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void
   a.H = p.H;
   a.qscale = 1.4426950408889634f / sqrtf((float)p.Dh);
   a.ws = ws;
+  a.lens = lens;
+  a.Lc = p.Lc;
   a.NS = attn_tc_splits(p.B, p.T, p.G, p.Hkv, p.L);
   const size_t rows_all = (size_t)p.B * p.Hq * p.T * a.NS;
   a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);
@@ -566,10 +573,13 @@ int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void
   CUtensorMap mkt, mvt, mkc, mvc;
   int e = at_kv_map(&mkt, kt, p.B, p.T, p.T, p.Hkv);
   if (!e) e = at_kv_map(&mvt, vt, p.B, p.T, p.T, p.Hkv);
-  if (!e && p.L > 0) e = at_kv_map(&mkc, kc, p.B, p.L, p.Lc, p.Hkv);
-  if (!e && p.L > 0) e = at_kv_map(&mvc, vc, p.B, p.L, p.Lc, p.Hkv);
+  // key extent: L, or the capacity when each sequence has its own length
+  // (rows past a sequence's length are masked as keys and weighted 0 as values)
+  const int ext = lens ? p.Lc : p.L;
+  if (!e && ext > 0) e = at_kv_map(&mkc, kc, p.B, ext, p.Lc, p.Hkv);
+  if (!e && ext > 0) e = at_kv_map(&mvc, vc, p.B, ext, p.Lc, p.Hkv);
   if (e) return e;
-  if (p.L == 0) {  // no cache blocks exist: the cache maps are never used
+  if (ext == 0) {  // no cache blocks exist: the cache maps are never used
     mkc = mkt;
     mvc = mvt;
   }

@@ -79,11 +79,15 @@ int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* roo
 int attn_tc_splits(int B, int T, int G, int Hkv, int L);
 bool attn_tc_supported(const Plan& p);
 int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                        void* out, uint8_t* ws, cudaStream_t st);
+                        const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st);
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                         void* out, uint8_t* ws, cudaStream_t st, bool overlap);
+                         const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st);
 int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                     const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st);
+                     const int32_t* lens, const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st);
+int launch_kv_commit(const Plan& p, const int32_t* acc_nodes, const int32_t* accept_len, const void* kt,
+                     const void* vt, void* kc, void* vc, int32_t* lens, uint8_t* ws, cudaStream_t st);
+int launch_next_inputs(const Plan& p, const void* attn_out, const int32_t* acc_nodes, const int32_t* accept_len,
+                       const int32_t* bonus, void* h_next, int32_t* root_next, uint8_t* ws, cudaStream_t st);
 int launch_verify_accept(const Plan& p, const void* attn_out, const void* lm_head, const medusa_tree_t& t,
                          int32_t* node_argmax, float* node_maxlogit, float* node_lse, float* node_entropy,
                          int32_t* accept_len, int32_t* acc_tokens, int32_t* acc_nodes, int32_t* bonus, uint8_t* ws,
@@ -163,6 +167,18 @@ __device__ __forceinline__ int order_key(float x) {
   return b >= 0 ? b : b ^ 0x7fffffff;
 }
 __device__ __forceinline__ float order_key_inv(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+
+// cache rows of sequence b: its own length when a per-sequence array is
+// given (a value outside [0, Lc] is a device error and is clamped), else L
+__device__ __forceinline__ int seq_len(const int32_t* lens, int b, int L, int Lc, uint8_t* ws) {
+  if (!lens) return L;
+  const int l = lens[b];
+  if (l < 0 || l > Lc) {
+    set_error(ws, MEDUSA_ERR_DEVICE);
+    return l < 0 ? 0 : Lc;
+  }
+  return l;
+}
 
 // (value desc, index asc) order used by every top-k / argmax
 __device__ __forceinline__ bool better(float v, int i, float w, int j) { return v > w || (v == w && i < j); }

@@ -26,7 +26,8 @@ STATUS = {0: "MEDUSA_OK", -1: "MEDUSA_ERR_INVALID_ARG", -2: "MEDUSA_ERR_UNSUPPOR
 EXPORTS = ("medusa_workspace_bytes", "medusa_tree_size", "medusa_heads_topk", "medusa_tree_build",
            "medusa_tree_attn", "medusa_verify_accept", "medusa_step", "medusa_step_profiled",
            "medusa_step_launches", "medusa_get_device_error", "medusa_status_string",
-           "medusa_heads_topk_noalloc", "medusa_check_bounded_wait")
+           "medusa_heads_topk_noalloc", "medusa_check_bounded_wait", "medusa_tree_attn_lens", "medusa_kv_commit",
+           "medusa_next_inputs")
 STEP_KERNELS = ("head_layer", "head_proj_topk", "tree_build", "tree_attn", "verify_proj", "accept")
 
 
@@ -55,7 +56,7 @@ class StepIO(ctypes.Structure):
         "h", "W1", "b1", "W2", "lm_head", "root_token", "q", "k_tree", "v_tree", "k_cache", "v_cache",
         "topk_idx", "topk_val")] + [("tree", Tree)] + [(n, ctypes.c_void_p) for n in (
             "attn_out", "node_argmax", "node_maxlogit", "node_lse", "node_entropy", "accept_len", "acc_tokens",
-            "acc_nodes", "bonus")]
+            "acc_nodes", "bonus", "kv_lens")]
 
 
 _lib = None
@@ -80,6 +81,9 @@ def lib() -> ctypes.CDLL:
         L.medusa_step.argtypes = [cfgp, ctypes.POINTER(StepIO), vp, vp]
         L.medusa_step_profiled.argtypes = [cfgp, ctypes.POINTER(StepIO), vp, vp, ctypes.POINTER(vp), ctypes.c_int32]
         L.medusa_get_device_error.argtypes = [vp, i32p, vp]
+        L.medusa_tree_attn_lens.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(Tree), vp, vp, vp]
+        L.medusa_kv_commit.argtypes = [cfgp] + [vp] * 9
+        L.medusa_next_inputs.argtypes = [cfgp] + [vp] * 8
         L.medusa_step_launches.argtypes = [cfgp]
         L.medusa_heads_topk_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp]
         L.medusa_check_bounded_wait.argtypes = [vp, ctypes.c_int32, vp]
@@ -219,8 +223,10 @@ def alloc_outputs(cfg: Config, device="cuda") -> Dict[str, torch.Tensor]:
             "acc_nodes": torch.empty(B, D + 1, **i32), "bonus": torch.empty(B, **i32)}
 
 
-def step_io(inputs: Dict[str, torch.Tensor], out: Dict[str, torch.Tensor]) -> StepIO:
+def step_io(inputs: Dict[str, torch.Tensor], out: Dict[str, torch.Tensor], kv_lens=None) -> StepIO:
+    """kv_lens: optional int32 device tensor [B] of per-sequence cache lengths."""
     io = StepIO()
+    io.kv_lens = kv_lens.data_ptr() if kv_lens is not None else None
     for n in ("h", "W1", "b1", "W2", "lm_head", "root_token", "q", "k_tree", "v_tree", "k_cache", "v_cache"):
         setattr(io, n, inputs[n].data_ptr())
     for n in ("topk_idx", "topk_val", "attn_out", "node_argmax", "node_maxlogit", "node_lse", "node_entropy",
@@ -228,6 +234,28 @@ def step_io(inputs: Dict[str, torch.Tensor], out: Dict[str, torch.Tensor]) -> St
         setattr(io, n, out[n].data_ptr())
     io.tree = _tree_struct(out["tree"])
     return io
+
+
+def medusa_tree_attn_lens(cfg: Config, q, k_tree, v_tree, k_cache, v_cache, kv_lens, tree, attn_out, ws,
+                          stream=None) -> None:
+    ts = _tree_struct(tree)
+    _check("medusa_tree_attn_lens", lib().medusa_tree_attn_lens(
+        ctypes.byref(cfg), _p(q), _p(k_tree), _p(v_tree), _p(k_cache), _p(v_cache), _p(kv_lens), ctypes.byref(ts),
+        _p(attn_out), _p(ws), _stream(stream)))
+
+
+def medusa_kv_commit(cfg: Config, acc_nodes, accept_len, k_tree, v_tree, k_cache, v_cache, kv_lens, ws,
+                     stream=None) -> None:
+    _check("medusa_kv_commit", lib().medusa_kv_commit(
+        ctypes.byref(cfg), _p(acc_nodes), _p(accept_len), _p(k_tree), _p(v_tree), _p(k_cache), _p(v_cache),
+        _p(kv_lens), _p(ws), _stream(stream)))
+
+
+def medusa_next_inputs(cfg: Config, attn_out, acc_nodes, accept_len, bonus, h_next, root_next, ws,
+                       stream=None) -> None:
+    _check("medusa_next_inputs", lib().medusa_next_inputs(
+        ctypes.byref(cfg), _p(attn_out), _p(acc_nodes), _p(accept_len), _p(bonus), _p(h_next), _p(root_next),
+        _p(ws), _stream(stream)))
 
 
 def medusa_step(cfg: Config, io: StepIO, ws, stream=None) -> None:

@@ -224,16 +224,16 @@ class Tree:
 
 # --------------------------------------------------------- tree attention ---
 
-def tree_attention(q, k_tree, v_tree, k_cache, v_cache, kv_len: int, mask: np.ndarray,
+def tree_attention(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask: np.ndarray,
                    nodes: Optional[Sequence[int]] = None, batches: Optional[Sequence[int]] = None) -> np.ndarray:
     """Every tree node attends, in one pass, to the whole KV cache and to the
     tree nodes its mask row allows [P1, "Attenzione sull'albero e
     accettazione"; P2, "Plongee profonde"]:
         o[b,i,h] = sum_j softmax_j(q[b,i,h] . k_j / sqrt(Dh)) v_j
     over j in cache[0..kv_len) and {tree node j : mask[i,j]}, with kv head
-    floor(h/G) (R3).  Shapes: q [B,T,Hq,Dh], k/v tree [B,T,Hkv,Dh], k/v cache
-    [B,cap,Hkv,Dh].  Returns o [B,T,Hq*Dh] in float64; rows outside
-    ``nodes`` / ``batches`` are NaN."""
+    floor(h/G) (R3).  ``kv_len`` is one length or one per sequence.  Shapes:
+    q [B,T,Hq,Dh], k/v tree [B,T,Hkv,Dh], k/v cache [B,cap,Hkv,Dh].  Returns
+    o [B,T,Hq*Dh] in float64; rows outside ``nodes`` / ``batches`` are NaN."""
     B, T, Hq, Dh = q.shape
     Hkv = k_tree.shape[2]
     G = Hq // Hkv
@@ -241,10 +241,12 @@ def tree_attention(q, k_tree, v_tree, k_cache, v_cache, kv_len: int, mask: np.nd
     nodes = list(range(T)) if nodes is None else list(nodes)
     batches = list(range(B)) if batches is None else list(batches)
     o = np.full((B, T, Hq * Dh), np.nan)
+    lens = [int(kv_len)] * B if np.ndim(kv_len) == 0 else [int(x) for x in kv_len]
     for b in batches:
+        L = lens[b]
         for g in range(Hkv):
-            Kc = decode(k_cache[b, :kv_len, g, :])
-            Vc = decode(v_cache[b, :kv_len, g, :])
+            Kc = decode(k_cache[b, :L, g, :])
+            Vc = decode(v_cache[b, :L, g, :])
             Kt = decode(k_tree[b, :, g, :])
             Vt = decode(v_tree[b, :, g, :])
             for h in range(g * G, (g + 1) * G):
@@ -256,7 +258,7 @@ def tree_attention(q, k_tree, v_tree, k_cache, v_cache, kv_len: int, mask: np.nd
                 s = s - s.max(axis=1, keepdims=True)
                 p = np.exp(s)
                 p = p / p.sum(axis=1, keepdims=True)
-                out = p[:, :kv_len] @ Vc + p[:, kv_len:] @ Vt
+                out = p[:, :L] @ Vc + p[:, L:] @ Vt
                 o[b, nodes, h * Dh:(h + 1) * Dh] = out
     return o
 
@@ -351,6 +353,35 @@ def accept_typical(tree: Tree, tokens_b: np.ndarray, argmax_b: np.ndarray, keep_
     walk([0])
     toks = [int(tokens_b[n]) for n in best[1:]]
     return len(toks), toks, best, int(argmax_b[best[-1]])
+
+
+# ------------------------------------------------ around the step (commit) --
+
+def kv_commit(k_cache, v_cache, k_tree, v_tree, acc_nodes, accept_len, kv_lens):
+    """The kept branch is appended for the next round [P1, "Attenzione
+    sull'albero e accettazione"]: for each sequence b, the key / value rows of
+    its accepted nodes acc_nodes[b][0..n] (root first, n = accept_len[b]) go
+    to cache rows kv_lens[b] .. kv_lens[b] + n, and the length grows by n + 1.
+    Returns new (k_cache, v_cache, kv_lens); the inputs are not modified."""
+    kc, vc = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+    lens = [int(x) for x in kv_lens]
+    for b in range(len(lens)):
+        n = int(accept_len[b])
+        for d in range(n + 1):
+            node = int(acc_nodes[b][d])
+            kc[b, lens[b] + d] = k_tree[b, node]
+            vc[b, lens[b] + d] = v_tree[b, node]
+        lens[b] += n + 1
+    return kc, vc, np.array(lens, dtype=np.int32)
+
+
+def next_inputs(attn_out_stored, acc_nodes, accept_len, bonus):
+    """The next round starts from the last accepted node: its attention output
+    (what the base lm_head scored, R4) is the next hidden state and the bonus
+    token the next root (R1).  Returns (h_next [B,H], root_next [B])."""
+    B = attn_out_stored.shape[0]
+    h = np.stack([attn_out_stored[b, int(acc_nodes[b][int(accept_len[b])])] for b in range(B)])
+    return h, np.array([int(x) for x in bonus], dtype=np.int32)
 
 
 # -------------------------------------------------------------- whole step --

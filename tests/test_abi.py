@@ -125,6 +125,9 @@ def test_null_pointers_are_rejected_before_any_launch():
     assert L.medusa_verify_accept(ctypes.byref(cfg), None, None, None, *([None] * 10)) == -1
     assert L.medusa_step(ctypes.byref(cfg), None, None, None) == -1
     assert L.medusa_get_device_error(None, None, None) == -1
+    assert L.medusa_tree_attn_lens(ctypes.byref(cfg), *([None] * 10)) == -1
+    assert L.medusa_kv_commit(ctypes.byref(cfg), *([None] * 9)) == -1
+    assert L.medusa_next_inputs(ctypes.byref(cfg), *([None] * 8)) == -1
     # misaligned (not 16-byte) pointers
     assert L.medusa_heads_topk(ctypes.byref(cfg), 8, 16, 16, 16, 16, 16, 16, None) == -1
 

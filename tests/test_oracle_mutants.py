@@ -105,6 +105,17 @@ def _typical_last_longest(tree, tokens_b, argmax_b, keep_edge):
     return len(toks), toks, best, int(argmax_b[best[-1]])
 
 
+def _commit_off_by_one(k_cache, v_cache, k_tree, v_tree, acc_nodes, accept_len, kv_lens):
+    # rows written one position past the cache end
+    return O.kv_commit(k_cache, v_cache, k_tree, v_tree, acc_nodes, accept_len, [l + 1 for l in kv_lens])
+
+
+def _attn_uniform_len(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=None, batches=None):
+    # per-sequence lengths ignored: the first one for every sequence
+    L = kv_len if np.ndim(kv_len) == 0 else int(kv_len[0])
+    return O.tree_attention(q, k_tree, v_tree, k_cache, v_cache, L, mask, nodes, batches)
+
+
 def _attn_scale_dh(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=None, batches=None):
     Dh = q.shape[-1]
     return O.tree_attention(q * (math.sqrt(Dh) / Dh), k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes, batches)
@@ -165,6 +176,8 @@ MUTANTS = [
     ("explicit tree loses its shallow leaves", dict(Tree=_DeepLeavesTree), P.check_explicit_tree),
     ("typical ties to the last longest chain", dict(accept_typical=_typical_last_longest),
      P.check_typical_shallow_tie),
+    ("commit writes one row late", dict(kv_commit=_commit_off_by_one), P.check_kv_commit),
+    ("per-sequence lengths ignored", dict(tree_attention=_attn_uniform_len), P.check_kv_commit),
 ]
 
 

@@ -340,6 +340,54 @@ def check_typical_shallow_tie(M) -> None:
     assert n == 1 and nodes == [0, 1] and toks == [1]
 
 
+def check_ragged_lengths(M) -> None:
+    """Per-sequence cache lengths: each sequence's output equals the one-length
+    call for that sequence alone (0, a middle value and the full capacity)."""
+    t = M.Tree((2, 2))
+    B, Hq, Hkv, Dh, cap = 3, 4, 2, 8, 9
+    q, kt, vt, kc, vc = _rand_attn_inputs(5, B, t.T, Hq, Hkv, Dh, cap, cap)
+    lens = [0, 4, cap]
+    o = M.tree_attention(q, kt, vt, kc, vc, lens, t.mask)
+    for b, L in enumerate(lens):
+        ob = M.tree_attention(q, kt, vt, kc, vc, L, t.mask, batches=[b])
+        np.testing.assert_array_equal(o[b], ob[b])
+
+
+def check_kv_commit(M) -> None:
+    """After the accepted chain is committed, plain attention (torch SDPA) of
+    the last accepted node's query over the grown cache alone reproduces that
+    node's tree-attention output: the committed rows are exactly what the node
+    saw in the tree.  Rows past the old lengths other than the committed ones
+    and the other sequences' rows stay as they were."""
+    topk = (3, 2, 2)
+    t = M.Tree(topk)
+    B, Hq, Hkv, Dh, cap = 3, 4, 2, 16, 20
+    q, kt, vt, kc, vc = _rand_attn_inputs(7, B, t.T, Hq, Hkv, Dh, cap, cap)
+    lens = [5, 0, 9]
+    o = M.tree_attention(q, kt, vt, kc, vc, lens, t.mask)
+    leaf_rows = t.paths.tolist()
+    acc_nodes = [leaf_rows[4][:4], leaf_rows[0][:2] + [-1, -1], leaf_rows[11][:3] + [-1]]
+    accept_len = [3, 1, 2]
+    kc2, vc2, lens2 = M.kv_commit(kc, vc, kt, vt, acc_nodes, accept_len, lens)
+    assert lens2.tolist() == [l + n + 1 for l, n in zip(lens, accept_len)]
+    G = Hq // Hkv
+    for b in range(B):
+        last = acc_nodes[b][accept_len[b]]
+        for h in range(Hq):
+            g = h // G
+            Q = torch.from_numpy(q[b, [last], h])[None, None]
+            K = torch.from_numpy(kc2[b, :lens2[b], g])[None, None]
+            V = torch.from_numpy(vc2[b, :lens2[b], g])[None, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V)[0, 0, 0].numpy()
+            np.testing.assert_allclose(o[b, last, h * Dh:(h + 1) * Dh], ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_array_equal(kc2[b, :lens[b]], kc[b, :lens[b]])
+        np.testing.assert_array_equal(kc2[b, lens2[b]:], kc[b, lens2[b]:])
+    h_next, root_next = M.next_inputs(o, acc_nodes, accept_len, [7, 8, 9])
+    for b in range(B):
+        np.testing.assert_array_equal(h_next[b], o[b, acc_nodes[b][accept_len[b]]])
+    assert root_next.tolist() == [7, 8, 9]
+
+
 def check_plans(M) -> None:
     """On every reduced workload the oracle realises the planted acceptance."""
     plans = synth.load_plans()
@@ -388,7 +436,7 @@ def check_silu(M) -> None:
 CHECKS = [check_zero_init, check_head_vs_torch, check_topk, check_tree_2x3, check_tree_invariants,
           check_attention_paths, check_attention_single_node, check_verify, check_greedy_lossless,
           check_typical_special_cases, check_plans, check_bf16_rounding, check_silu, check_explicit_tree,
-          check_typical_shallow_tie]
+          check_typical_shallow_tie, check_ragged_lengths, check_kv_commit]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
