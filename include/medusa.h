@@ -66,7 +66,13 @@ typedef enum {
 } medusa_status_t;
 
 typedef enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 } medusa_dtype_t;
-typedef enum { MEDUSA_ACCEPT_GREEDY = 0, MEDUSA_ACCEPT_TYPICAL = 1 } medusa_accept_t;
+/* GREEDY: keep a candidate equal to its parent's top choice.  TYPICAL: keep a
+ * candidate whose probability clears an entropy-tied threshold.  SAMPLE: each
+ * node's choice is a draw from its distribution at the temperature (Gumbel-max
+ * with counter-based noise, see medusa_verify_accept); a candidate equal to
+ * its parent's draw is kept, so the accepted tokens follow the base model's
+ * sampling distribution (bf16 only). */
+typedef enum { MEDUSA_ACCEPT_GREEDY = 0, MEDUSA_ACCEPT_TYPICAL = 1, MEDUSA_ACCEPT_SAMPLE = 2 } medusa_accept_t;
 
 /* Sizes and options of one step (host memory, read during the call only). */
 typedef struct {
@@ -98,6 +104,12 @@ typedef struct {
   int32_t tree_nodes;
   const int32_t* tree_parent;
   const int32_t* tree_rank;
+  /* SAMPLE mode: the noise of vocabulary row v at node n = b*T + i is drawn
+   * from Philox4x32-10 with key (sample_seed[0], sample_seed[1]) and counter
+   * (v, n / 4, sample_step, 0), word n % 4; a new step needs a new
+   * sample_step (or seed). */
+  uint32_t sample_seed[2];
+  int32_t sample_step;
 } medusa_config_t;
 
 /* Candidate tree, device arrays allocated by the caller (sizes from
@@ -205,8 +217,11 @@ int medusa_tree_attn(const medusa_config_t* cfg, const void* q, const void* k_tr
  * Scores s_i = lm_head . attn_out[b][i] (fp32 accumulation) for every node:
  *   node_argmax (ties to the lower id), node_maxlogit; typical mode also
  *   node_lse = log sum_v exp(s_v / temperature) and node_entropy = -sum p ln p
- *   of p = softmax(s / temperature).
- * Acceptance: an edge parent->c is kept when (greedy) token_c ==
+ *   of p = softmax(s / temperature).  Sample mode: node_argmax = the argmax of
+ *   s_v / temperature + g_v (a draw from softmax(s / temperature)), with
+ *   Gumbel noise g_v = -ln(-ln u), u = (top 24 bits of the Philox word + 0.5)
+ *   / 2^24, and node_maxlogit = that maximum.
+ * Acceptance: an edge parent->c is kept when (greedy, sample) token_c ==
  * node_argmax[parent], or (typical) p_parent(token_c) > min(eps, delta *
  * exp(-entropy_parent)).  The longest chain of kept edges from the root wins
  * (ties: lowest node id at the first divergence).  accept_len[b] = its

@@ -54,7 +54,11 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->kv_len < 0 || c->kv_capacity < c->kv_len)
     return MEDUSA_ERR_INVALID_ARG;
   if (c->dtype != MEDUSA_F32 && c->dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
-  if (c->accept_mode != MEDUSA_ACCEPT_GREEDY && c->accept_mode != MEDUSA_ACCEPT_TYPICAL) return MEDUSA_ERR_INVALID_ARG;
+  if (c->accept_mode != MEDUSA_ACCEPT_GREEDY && c->accept_mode != MEDUSA_ACCEPT_TYPICAL &&
+      c->accept_mode != MEDUSA_ACCEPT_SAMPLE)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (c->accept_mode == MEDUSA_ACCEPT_SAMPLE && !(c->temperature > 0.f)) return MEDUSA_ERR_INVALID_ARG;
+  if (c->accept_mode == MEDUSA_ACCEPT_SAMPLE && c->dtype != MEDUSA_BF16) return MEDUSA_ERR_UNSUPPORTED;
   if (c->n_heads > MEDUSA_MAX_HEADS || c->depth > MEDUSA_MAX_DEPTH || c->depth > c->n_heads)
     return MEDUSA_ERR_UNSUPPORTED;
   if (c->hidden % 64 != 0) return MEDUSA_ERR_UNSUPPORTED;
@@ -78,6 +82,10 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   p->Lc = c->kv_capacity;
   p->bf16 = c->dtype == MEDUSA_BF16;
   p->typical = c->accept_mode == MEDUSA_ACCEPT_TYPICAL;
+  p->sample = c->accept_mode == MEDUSA_ACCEPT_SAMPLE;
+  p->seed[0] = c->sample_seed[0];
+  p->seed[1] = c->sample_seed[1];
+  p->step = c->sample_step;
   p->temperature = c->temperature;
   p->eps = c->eps;
   p->delta = c->delta;

@@ -39,8 +39,10 @@ struct TreeDims {
 struct Plan {
   // sizes
   int B, H, V, K, D, kmax, T, NL, W, Hq, Hkv, G, Dh, L, Lc;
-  bool bf16, typical;
+  bool bf16, typical, sample;
   float temperature, eps, delta;
+  uint32_t seed[2];
+  int step;
   TreeDims tree;
   int topk_n[MEDUSA_MAX_HEADS];  // entries kept per head
   // streaming partitions

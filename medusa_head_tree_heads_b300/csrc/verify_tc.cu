@@ -52,6 +52,9 @@ struct VtcArgs {
   int V, N, H, BN, n_vt, n_nt, n_tiles, nk, stages;
   uint32_t idesc;
   int typical;
+  int sample;  // node choice = argmax of s / temperature + Gumbel noise
+  uint32_t seed0, seed1;
+  int step;
   float inv_temp;
   float4* part;  // [n_vt][N]: (max, sum e, sum e*t, argmax bits)
   int32_t* node_argmax;
@@ -113,6 +116,31 @@ __device__ __forceinline__ Soft shfl_soft(const Soft& a, int o) {
   return r;
 }
 
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds, each two 32x32->64-bit products of
+// counter words with fixed multipliers, the high halves xored with the other
+// words and the key; the key advances by a Weyl sequence between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// standard Gumbel noise -ln(-ln u) from the top 24 bits of a word (u strictly
+// inside (0, 1), exact in fp32)
+__device__ __forceinline__ float gumbel24(uint32_t x) {
+  const float u = ((float)(x >> 8) + 0.5f) * (1.f / 16777216.f);
+  return -__logf(-__logf(u));  // fast logarithm: the draws near a tie may differ from exact ones
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               uint8_t* ws) {
   if (tc::mbar_try_wait(bar, parity)) return true;
@@ -128,6 +156,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return true;
 }
 
+// MODE: 0 greedy, 1 typical, 2 sample (a compile-time choice, so each
+// instance carries only its own epilogue)
+template <int MODE>
 __global__ void __launch_bounds__(VT_THREADS, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ VtcArgs a) {
@@ -148,7 +179,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
   volatile int* ep_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool typical = a.typical != 0;
+  constexpr bool typical = MODE == 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -279,7 +310,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       const int half = (warp - 2) >> 2;
       for (int ch0 = 4 * half; ch0 < a.BN / 16; ch0 += 8) {
         const int nch = min(4, a.BN / 16 - ch0);
-        if (typical) {
+        if constexpr (typical) {
           // typical: per column the max and argmax as in greedy (redux),
           // then one exponential per element against that max and a plain
           // additive transpose-reduce of (sum e, sum e*t) over the 64 rows
@@ -376,6 +407,22 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
               mine.z = 0.f;
               mine.s = 0.f;
               mine.i = INT_MAX;
+              if constexpr (MODE == 2) {  // s / temperature + Gumbel noise (one Philox call per 4 node columns)
+                const uint32_t n0 = (uint32_t)(nt * a.BN + (ch0 + cp + c) * 16);
+#pragma unroll
+                for (int h = 0; h < VT_SUB; ++h) {
+                  const uint32_t row = (uint32_t)(row0 + h * VT_M);
+#pragma unroll
+                  for (int j4 = 0; j4 < 16; j4 += 4) {
+                    const uint4 w = philox4x32_10(make_uint4(row, (n0 + j4) >> 2, (uint32_t)a.step, 0u), a.seed0,
+                                                  a.seed1);
+                    v[h][c][j4] = v[h][c][j4] * a.inv_temp + gumbel24(w.x);
+                    v[h][c][j4 + 1] = v[h][c][j4 + 1] * a.inv_temp + gumbel24(w.y);
+                    v[h][c][j4 + 2] = v[h][c][j4 + 2] * a.inv_temp + gumbel24(w.z);
+                    v[h][c][j4 + 3] = v[h][c][j4 + 3] * a.inv_temp + gumbel24(w.w);
+                  }
+                }
+              }
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const float x0 = ok0 ? v[0][c][j] : -INFINITY;
@@ -589,7 +636,11 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, c
   a.nk = p.H / VT_BK;
   a.idesc = tc::idesc_bf16_f32(VT_M, a.BN);
   a.typical = p.typical ? 1 : 0;
-  a.inv_temp = p.typical ? 1.f / p.temperature : 1.f;
+  a.sample = p.sample ? 1 : 0;
+  a.seed0 = p.seed[0];
+  a.seed1 = p.seed[1];
+  a.step = p.step;
+  a.inv_temp = (p.typical || p.sample) ? 1.f / p.temperature : 1.f;
   a.part = reinterpret_cast<float4*>(ws + p.off_vtc_part);
   a.node_argmax = node_argmax;
   a.node_maxlogit = node_maxlogit;
@@ -617,10 +668,12 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, c
   if (e) return e;
   e = make_tmap_bf16(&tB, attn_out, a.N, p.H, a.BN);
   if (e) return e;
-  cudaError_t ce = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  void (*kern)(CUtensorMap, CUtensorMap, VtcArgs) =
+      a.typical ? verify_tc_kernel<1> : (a.sample ? verify_tc_kernel<2> : verify_tc_kernel<0>);
+  cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.n_tiles < p.sm_count ? a.n_tiles : p.sm_count;
-  ce = launch_k(verify_tc_kernel, dim3(grid), dim3(VT_THREADS), smem, st, true, tA, tB, a);
+  ce = launch_k(kern, dim3(grid), dim3(VT_THREADS), smem, st, true, tA, tB, a);
   if (ce != cudaSuccess) return (int)ce;
   const unsigned mgrid = (unsigned)((a.N + 7) / 8);
   if (a.typical) return (int)launch_k(verify_merge_kernel<true>, dim3(mgrid), dim3(256), 0, st, true, a);

@@ -61,7 +61,7 @@ class Shape:
     n_q_heads: int
     n_kv_heads: int
     head_dim: int
-    accept: str  # "greedy" or "typical"
+    accept: str  # "greedy", "typical" or "sample"
     planted: Tuple  # ("fixed", d) or ("uniform", lo, hi)
     seed: int
     kv_capacity: int = 0  # cache rows per sequence; 0 means kv_len
@@ -70,6 +70,8 @@ class Shape:
     delta: float = 0.09
     full_size: bool = False  # the oracle checks every node only when False
     sparse_nodes: int = 0  # > 0: an explicit tree of that many non-root nodes (see explicit_tree)
+    sample_seed: Tuple[int, int] = (0x1234567, 0x89ABCDE)  # sampling verification: Philox key and step
+    sample_step: int = 0
 
     @property
     def depth(self) -> int:
@@ -190,6 +192,14 @@ _add(Shape("gqa76-bf16", "bf16", 4096, 128256, 4, 16, (4, 3, 2, 2), 4096, 32, 8,
            1005, full_size=True, sparse_nodes=76))
 _add(Shape("7b-sparse64", "bf16", 4096, 32000, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3),
            1006, full_size=True, sparse_nodes=64))
+# sampling verification: reduced variants (a low temperature keeps the planted
+# draws far from ties) and the 7B shapes at temperature 0.7
+_add(Shape("sample-mini", "bf16", 640, 3001, 5, 2, (4, 3, 2, 2, 1), 300, 5, 5, 128, "sample", ("uniform", 0, 3),
+           2013, kv_capacity=333, temperature=0.3))
+_add(Shape("sample-sparse-mini", "bf16", 256, 777, 4, 3, (4, 3, 2, 2), 70, 2, 1, 128, "sample", ("uniform", 0, 4),
+           2014, sparse_nodes=24, temperature=0.3, sample_seed=(7, 11), sample_step=3))
+_add(Shape("7b-sample", "bf16", 4096, 32000, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "sample", ("fixed", 3),
+           1007, full_size=True))
 # profiling case: the 7B shapes with a quarter-sized vocabulary (still far
 # larger than L2) so that counter replays stay small
 _add(Shape("7b-prof", "bf16", 4096, 8192, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3), 4001,

@@ -301,6 +301,66 @@ def verify_stats(o_stored: np.ndarray, lm_head, temperature: Optional[float] = N
     return res
 
 
+# Counter-based noise for sampling verification.  Philox4x32-10 (Salmon,
+# Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC'11):
+# ten rounds over a 128-bit counter; each round multiplies two counter words
+# by fixed constants, the high halves are xored with the other two words and
+# the key, and the key advances by a Weyl sequence between rounds.
+PHILOX_MUL = (0xD2511F53, 0xCD9E8D57)
+PHILOX_WEYL = (0x9E3779B9, 0xBB67AE85)
+_U32 = 0xFFFFFFFF
+
+
+def philox4x32_10(c0, c1, c2, c3, k0: int, k1: int):
+    """Vectorised over numpy arrays of counter words (held as uint64 < 2^32)."""
+    c = [np.asarray(x, dtype=np.uint64) for x in (c0, c1, c2, c3)]
+    k0, k1 = np.uint64(k0), np.uint64(k1)
+    for r in range(10):
+        if r:
+            k0 = (k0 + np.uint64(PHILOX_WEYL[0])) & np.uint64(_U32)
+            k1 = (k1 + np.uint64(PHILOX_WEYL[1])) & np.uint64(_U32)
+        p0 = np.uint64(PHILOX_MUL[0]) * c[0]
+        p1 = np.uint64(PHILOX_MUL[1]) * c[2]
+        hi0, lo0 = p0 >> np.uint64(32), p0 & np.uint64(_U32)
+        hi1, lo1 = p1 >> np.uint64(32), p1 & np.uint64(_U32)
+        c = [hi1 ^ c[1] ^ k0, lo1, hi0 ^ c[3] ^ k1, lo0]
+    return c
+
+
+def gumbel_noise(seed: Sequence[int], step: int, node: int, V: int) -> np.ndarray:
+    """Noise of vocabulary rows 0..V-1 at global node n (= b*T + i): Philox
+    word n % 4 of counter (v, n // 4, step, 0) under key (seed0, seed1); its top
+    24 bits give u = (w >> 8 + 1/2) / 2^24 in (0, 1) and g = -ln(-ln u), a
+    standard Gumbel variable."""
+    v = np.arange(V, dtype=np.uint64)
+    z = np.zeros(V, dtype=np.uint64)
+    words = philox4x32_10(v, z + np.uint64(node // 4), z + np.uint64(step), z, int(seed[0]), int(seed[1]))
+    u = ((words[node % 4] >> np.uint64(8)).astype(np.float64) + 0.5) / 16777216.0
+    return -np.log(-np.log(u))
+
+
+def sample_stats(o_stored: np.ndarray, lm_head, temperature: float, seed: Sequence[int], step: int,
+                 rows: Optional[Sequence[int]] = None,
+                 node_ids: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
+    """Sampling verification: each node draws its token from softmax(logit /
+    temperature) by the Gumbel-max rule, argmax_v(logit_v / temperature + g_v)
+    (ties to the lower id).  Row r of ``o_stored`` is global node node_ids[r]
+    (default r) for the noise.  Returns 'argmax' (the draw), 'maxlogit' (the
+    winning perturbed score) and 'second' (the runner-up, for margin checks)."""
+    N = o_stored.shape[0]
+    rows = list(range(N)) if rows is None else list(rows)
+    node_ids = list(range(N)) if node_ids is None else list(node_ids)
+    W = decode(lm_head)
+    res = {"argmax": np.full(N, -1, dtype=np.int64), "maxlogit": np.full(N, np.nan), "second": np.full(N, np.nan),
+           "lse": np.full(N, np.nan), "entropy": np.full(N, np.nan)}
+    for n in rows:
+        x = (o_stored[n] @ W.T) / temperature + gumbel_noise(seed, step, node_ids[n], W.shape[0])
+        res["argmax"][n] = int(np.argmax(x))
+        srt = np.sort(x)
+        res["maxlogit"][n], res["second"][n] = srt[-1], srt[-2]
+    return res
+
+
 def token_logprob(o_stored_row: np.ndarray, lm_head, token: int, temperature: float, lse: float) -> float:
     """log p(token) under softmax(lm_head . o / temperature)."""
     return float(o_stored_row @ decode(lm_head[token])) / temperature - lse
@@ -412,7 +472,10 @@ def step(inp: Dict[str, np.ndarray], shape, nodes_only: Optional[Dict[int, Seque
     rows = None
     if nodes_only is not None:
         rows = [b * T + i for b in range(B) for i in nodes_only[b]]
-    stats = verify_stats(flat, inp["lm_head"], shape.temperature if typical else None, rows=rows)
+    if shape.accept == "sample":
+        stats = sample_stats(flat, inp["lm_head"], shape.temperature, shape.sample_seed, shape.sample_step, rows=rows)
+    else:
+        stats = verify_stats(flat, inp["lm_head"], shape.temperature if typical else None, rows=rows)
     argmax = stats["argmax"].reshape(B, T)
     res = {"z": z, "head_logits": logits, "topk_idx": idx, "topk_val": val, "tree": tree, "tokens": tok,
            "attn_out": o_st, "argmax": argmax, "maxlogit": stats["maxlogit"].reshape(B, T),

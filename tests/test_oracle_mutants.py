@@ -116,6 +116,14 @@ def _attn_uniform_len(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=N
     return O.tree_attention(q, k_tree, v_tree, k_cache, v_cache, L, mask, nodes, batches)
 
 
+def _gumbel_sign(seed, step, node, V):
+    return -O.gumbel_noise(seed, step, node, V)  # -g is not Gumbel-max noise
+
+
+def _gumbel_one_word(seed, step, node, V):
+    return O.gumbel_noise(seed, step, node - node % 4, V)  # word 0 for every node of a counter
+
+
 def _attn_scale_dh(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=None, batches=None):
     Dh = q.shape[-1]
     return O.tree_attention(q * (math.sqrt(Dh) / Dh), k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes, batches)
@@ -178,6 +186,8 @@ MUTANTS = [
      P.check_typical_shallow_tie),
     ("commit writes one row late", dict(kv_commit=_commit_off_by_one), P.check_kv_commit),
     ("per-sequence lengths ignored", dict(tree_attention=_attn_uniform_len), P.check_kv_commit),
+    ("Gumbel noise sign flipped", dict(gumbel_noise=_gumbel_sign), P.check_gumbel_max),
+    ("one Philox word for four nodes", dict(gumbel_noise=_gumbel_one_word), P.check_gumbel_max),
 ]
 
 

@@ -388,11 +388,56 @@ def check_kv_commit(M) -> None:
     assert root_next.tolist() == [7, 8, 9]
 
 
+def check_philox(M) -> None:
+    """Philox4x32-10 words: uniform (chi-square over 64 bins for each of the 4
+    words of 2^15 consecutive counters), all distinct (the rounds are a
+    bijection of the counter for a fixed key), and one flipped counter bit
+    changes half of the 128 output bits on average (avalanche)."""
+    n = 1 << 15
+    c = np.arange(n, dtype=np.uint64)
+    z = np.zeros(n, dtype=np.uint64)
+    words = M.philox4x32_10(c, z + np.uint64(5), z, z, 0x1234, 0xABCD)
+    for w in words:
+        counts = np.bincount((w >> np.uint64(26)).astype(np.int64), minlength=64)
+        chi2 = ((counts - n / 64) ** 2 / (n / 64)).sum()
+        assert chi2 < 120, chi2  # 63 degrees of freedom
+    packed = set(zip(*[w.tolist() for w in words]))
+    assert len(packed) == n
+    flips = []
+    for i in range(400):
+        a = M.philox4x32_10(np.uint64(i), np.uint64(9), np.uint64(0), np.uint64(0), 3, 4)
+        b = M.philox4x32_10(np.uint64(i ^ (1 << (i % 32))), np.uint64(9), np.uint64(0), np.uint64(0), 3, 4)
+        flips.append(sum(bin(int(x) ^ int(y)).count("1") for x, y in zip(a, b)))
+    assert abs(np.mean(flips) - 64) < 3, np.mean(flips)
+
+
+def check_gumbel_max(M) -> None:
+    """Gumbel-max draws follow softmax(logit / temperature): over 40000 steps
+    of a 5-token vocabulary the draw frequencies pass a chi-square test (4
+    degrees of freedom, bound at p ~ 1e-4); and the four nodes that share one
+    Philox counter (different words) draw independently (with equal logits
+    they agree about 1/5 of the time, not always)."""
+    logits = np.array([2.0, 1.0, 0.5, 0.0, -1.0])
+    temp = 0.7
+    p = np.exp(logits / temp)
+    p /= p.sum()
+    steps = 40000
+    draws = np.array([int(np.argmax(logits / temp + M.gumbel_noise((11, 12), s, 6, 5))) for s in range(steps)])
+    counts = np.bincount(draws, minlength=5)
+    chi2 = ((counts - steps * p) ** 2 / (steps * p)).sum()
+    assert chi2 < 23.5, (counts, chi2)
+    same = 0
+    for s in range(2000):
+        d = [int(np.argmax(M.gumbel_noise((1, 2), s, n, 5))) for n in range(4)]
+        same += d[0] == d[1]
+    assert abs(same / 2000 - 0.2) < 0.04, same
+
+
 def check_plans(M) -> None:
     """On every reduced workload the oracle realises the planted acceptance."""
     plans = synth.load_plans()
     for name in ["tiny-fp32", "tiny-fp32-gqa", "7b-mini", "13b-mini", "gqa-mini", "33b-mini", "sparse-mini",
-                 "sparse-typical-mini", "sparse-f32"]:
+                 "sparse-typical-mini", "sparse-f32", "sample-mini", "sample-sparse-mini"]:
         s = synth.SHAPES[name]
         inp = {k: to_np(v) for k, v in synth.make_inputs(s, plans[name]).items()}
         res = M.step(inp, s)
@@ -436,7 +481,7 @@ def check_silu(M) -> None:
 CHECKS = [check_zero_init, check_head_vs_torch, check_topk, check_tree_2x3, check_tree_invariants,
           check_attention_paths, check_attention_single_node, check_verify, check_greedy_lossless,
           check_typical_special_cases, check_plans, check_bf16_rounding, check_silu, check_explicit_tree,
-          check_typical_shallow_tie, check_ragged_lengths, check_kv_commit]
+          check_typical_shallow_tie, check_ragged_lengths, check_kv_commit, check_philox, check_gumbel_max]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)

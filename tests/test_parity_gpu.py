@@ -215,7 +215,12 @@ def test_full_size_sampled(name):
         o_st = O.round_to_storage(o[b, nodes], s.dtype)
         got = res["attn_out"][b, nodes].float().numpy()
         U.assert_close(got, o_st, s.dtype, f"attn_out b={b}")
-        st = O.verify_stats(o_st, n["lm_head"], s.temperature if typical else None)
+        sample = s.accept == "sample"
+        ids = [b * s.n_nodes + i for i in nodes]
+        if sample:
+            st = O.sample_stats(o_st, n["lm_head"], s.temperature, s.sample_seed, s.sample_step, node_ids=ids)
+        else:
+            st = O.verify_stats(o_st, n["lm_head"], s.temperature if typical else None)
         U.assert_close(res["node_maxlogit"][b, nodes].numpy(), st["maxlogit"], s.dtype, "maxlogit")
         planted = {p[0] for p in plan["seqs"][b]["plant"]}
         lm = n["lm_head"]
@@ -226,7 +231,10 @@ def test_full_size_sampled(name):
                 assert g == r, (b, i)
             else:  # an unplanted node: the GPU's choice must tie the best within rounding
                 lg = float(o_st[j] @ O.decode(lm[g]))
-                assert st["maxlogit"][j] - lg <= 2e-3 * abs(st["maxlogit"][j]), (b, i, g, r)
+                if sample:
+                    lg = lg / s.temperature + float(O.gumbel_noise(s.sample_seed, s.sample_step, ids[j],
+                                                                   s.vocab)[g])
+                assert st["maxlogit"][j] - lg <= 2e-3 * max(1.0, abs(st["maxlogit"][j])), (b, i, g, r)
         if typical:
             U.assert_close(res["node_lse"][b, nodes].numpy(), st["lse"], s.dtype, "lse")
             U.assert_close(res["node_entropy"][b, nodes].numpy(), st["entropy"], s.dtype, "entropy")
