@@ -41,14 +41,13 @@ constexpr int AT_TILES = 2;          // tiles per CTA
 constexpr int AT_ROWS = AT_M * AT_TILES;
 constexpr int AT_BK = 64;            // keys per block
 constexpr int AT_DH = 128;
-constexpr int AT_STAGES = 3;         // depth of the K ring and of the V ring
+constexpr int AT_STAGES = 4;         // depth of the K ring and of the V ring
 constexpr int AT_THREADS = 128 + 32 * 4 * AT_TILES;
 constexpr uint32_t AT_QCHUNK = AT_M * 128;        // 16 KB: 128 rows x 64 columns, 128-byte swizzled
 constexpr uint32_t AT_QTILE = 2 * AT_QCHUNK;      // Q of a tile: [128 rows][128 dh]
-constexpr uint32_t AT_PTILE = AT_M * AT_BK * 2;   // P of a tile: [128 rows][64 keys], one chunk
 constexpr uint32_t AT_KVCHUNK = AT_BK * 128;      // 8 KB: 64 keys x 64 dh
 constexpr uint32_t AT_KVTILE = 2 * AT_KVCHUNK;    // K or V: [64 keys][128 dh]
-constexpr uint32_t AT_TMEM_COLS = 512;            // per tile: S0, S1 (64 columns each); then O of each tile (128)
+constexpr uint32_t AT_TMEM_COLS = 512;            // per tile: S0, S1 (64 columns each; P over the first 32); then O of each tile (128)
 constexpr uint64_t AT_WAIT_NS = 20ull * 1000 * 1000;
 constexpr float AT_RESCALE_LOG2 = 8.f;            // raise the running max only past 2^8 growth
 
@@ -114,8 +113,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   extern __shared__ uint8_t at_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(at_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Qs = smem;                                   // [tile] Q tiles
-  uint8_t* Ps = Qs + AT_TILES * AT_QTILE;               // [tile] P tiles
-  uint8_t* Ks = Ps + AT_TILES * AT_PTILE;               // [AT_STAGES] K tiles
+  uint8_t* Ks = Qs + AT_TILES * AT_QTILE;               // [AT_STAGES] K tiles
   uint8_t* Vs = Ks + AT_STAGES * AT_KVTILE;             // [AT_STAGES] V tiles
   uint32_t* mrow = reinterpret_cast<uint32_t*>(Vs + AT_STAGES * AT_KVTILE);  // [256][W] ancestor masks
   uint64_t* bars = reinterpret_cast<uint64_t*>(mrow + AT_ROWS * a.W);       // 256 * W words: 8-byte aligned
@@ -124,10 +122,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint64_t* v_full = k_empty + AT_STAGES;
   uint64_t* v_empty = v_full + AT_STAGES;
   uint64_t* s_full = v_empty + AT_STAGES;    // [tile][2]
-  uint64_t* s_free = s_full + 2 * AT_TILES;  // [tile][2]
-  uint64_t* p_full = s_free + 2 * AT_TILES;  // [tile]
-  uint64_t* pv_done = p_full + AT_TILES;     // [tile]
-  uint64_t* q_ready = pv_done + AT_TILES;
+  uint64_t* s_free = s_full + 2 * AT_TILES;  // [tile][2]: the buffer's P V is done
+  // [tile][block parity]: P(i) written by the tile's 4 warps.  A warp can be
+  // at most one block ahead of another (block i + 1 needs S(i + 1), whose
+  // buffer frees only after P(i - 1) V), so two barriers keep arrivals of
+  // neighbouring blocks apart.
+  uint64_t* p_full = s_free + 2 * AT_TILES;
+  // [tile][block parity]: P(i) V complete.  Split by parity for the same
+  // reason: a parity wait must never be more than one phase from its target.
+  uint64_t* pv_done = p_full + 2 * AT_TILES;
+  uint64_t* q_ready = pv_done + 2 * AT_TILES;
   uint64_t* drain = q_ready + 1;             // [2]: S issuer, PV issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -154,10 +158,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     for (int t = 0; t < AT_TILES; ++t) {
       for (int u = 0; u < 2; ++u) {
         tc::mbar_init(&s_full[2 * t + u], 1);
-        tc::mbar_init(&s_free[2 * t + u], 4);
+        tc::mbar_init(&s_free[2 * t + u], 1);
       }
-      tc::mbar_init(&p_full[t], 4);
-      tc::mbar_init(&pv_done[t], 1);
+      tc::mbar_init(&p_full[2 * t], 4);
+      tc::mbar_init(&p_full[2 * t + 1], 4);
+      tc::mbar_init(&pv_done[2 * t], 1);
+      tc::mbar_init(&pv_done[2 * t + 1], 1);
     }
     tc::mbar_init(q_ready, 4 * AT_TILES);
     tc::mbar_init(&drain[0], 1);
@@ -256,20 +262,20 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         const uint32_t va = tc::smem_u32(Vs + (size_t)s * AT_KVTILE);
         for (int t = 0; t < ntiles && ok; ++t) {
-          if (!at_wait(&p_full[t], i & 1u, abort_flag, a.ws)) {
+          if (!at_wait(&p_full[2 * t + (i & 1)], (i >> 1) & 1u, abort_flag, a.ws)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t pa = tc::smem_u32(Ps + t * AT_PTILE);
+          const uint32_t pt = tmem + t * 2 * AT_BK + (i & 1) * AT_BK;  // P(i): bf16 pairs over S(i)
 #pragma unroll
-          for (int st = 0; st < AT_BK / 16; ++st) {  // 16 keys per MMA
-            const uint64_t da = tc::sw128_desc(pa) + 2 * st;
+          for (int st = 0; st < AT_BK / 16; ++st) {  // 16 keys per MMA: 8 TMEM columns of A
             uint64_t db = tc::sw128_desc(va + st * 2048);
             db = (db & ~(0x3FFFull << 16)) | ((uint64_t)(AT_KVCHUNK >> 4) << 16);  // dh-chunk stride
-            tc::mma_bf16(tmem + AT_TILES * 2 * AT_BK + t * AT_DH, da, db, idO, (i | st) != 0);
+            tc::mma_bf16_tmem_a(tmem + AT_TILES * 2 * AT_BK + t * AT_DH, pt + st * 8, db, idO, (i | st) != 0);
           }
-          tc::mma_commit(&pv_done[t]);
+          tc::mma_commit(&pv_done[2 * t + (i & 1)]);
+          tc::mma_commit(&s_free[2 * t + (i & 1)]);  // the S buffer held P(i)
         }
         if (ok) tc::mma_commit(&v_empty[s]);
       }
@@ -289,7 +295,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int node = rvalid ? r / a.G : 0;
     const int hq = g * a.G + (rvalid ? r - node * a.G : 0);
     uint8_t* Qt = Qs + t * AT_QTILE;
-    uint8_t* Pt = Ps + t * AT_PTILE;
     // Q row into the swizzled tile (zeros for padding rows)
     {
       const uint4* src = reinterpret_cast<const uint4*>(a.q + (((size_t)b * a.T + node) * a.Hq + hq) * AT_DH);
@@ -352,16 +357,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           v[48 + j] = v3[j];
         }
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&s_free[2 * t + buf]);
-      if (!warp_live) {  // no real row: nothing to compute, the handshakes go on
-        if (i > 0 && !at_wait_warp(&pv_done[t], (i - 1) & 1u, abort_flag, a.ws, lane)) {
-          ok = false;
-          break;
-        }
+      if (!warp_live) {  // no real row: nothing to compute, the handshake goes on
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&p_full[t]);
+        if (lane == 0) tc::mbar_arrive(&p_full[2 * t + buf]);
         continue;
       }
       // a full cache block needs no visibility test; elsewhere a hidden key
@@ -383,12 +381,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < w; ++j) tm[j] = fmaxf(tm[j], tm[j + w]);
       const float mx = tm[0] * a.qscale;  // the scale is positive; -inf stays -inf
-      // P(i) overwrites P(i-1) and a rescale touches O: both need P(i-1) V done
-      if (i > 0 && !at_wait_warp(&pv_done[t], (i - 1) & 1u, abort_flag, a.ws, lane)) {
-        ok = false;
-        break;
-      }
-      tc::fence_after_sync();
       {
         const bool raise = mx > m + AT_RESCALE_LOG2 || (m == -INFINITY && mx > -INFINITY);
         const float mn = raise ? mx : m;
@@ -396,6 +388,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const float sc = resc ? exp2f(m - mn) : 1.f;
         if (resc) l *= sc;
         if (__any_sync(0xffffffffu, resc)) {  // rescale the accumulated O rows in TMEM (whole warp)
+          // after P(i-1) V has landed in O
+          if (!at_wait_warp(&pv_done[2 * t + ((i - 1) & 1)], ((i - 1) >> 1) & 1u, abort_flag, a.ws, lane)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
 #pragma unroll
           for (int c = 0; c < AT_DH / 16; ++c) {
             float o[16];
@@ -408,30 +406,31 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         m = mn;
       }
-      // P = exp2(s * scale - m) (a -inf score gives 0) into the P tile
+      // P = exp2(s * scale - m) (a -inf score gives 0) as bf16 pairs (the
+      // even key in the low half) over the first 32 columns of S(i) in TMEM
       const float nm = (m == -INFINITY) ? 0.f : -m;
       float ls = 0.f;
-      uint32_t pk[AT_BK / 2];
+      float pk[2][16];
 #pragma unroll
       for (int j = 0; j < AT_BK; j += 2) {
         const float p0 = at_exp2(fmaf(v[j], a.qscale, nm)), p1 = at_exp2(fmaf(v[j + 1], a.qscale, nm));
         ls += p0 + p1;
-        pk[j >> 1] = pack2_bf16(p0, p1);
+        pk[j >> 5][(j >> 1) & 15] = __uint_as_float(pack2_bf16(p0, p1));
       }
-#pragma unroll
-      for (int u = 0; u < AT_BK / 8; ++u)
-        *reinterpret_cast<uint4*>(Pt + at_sw(trow, u)) =
-            make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      tc::tmem_st16(sbase + buf * AT_BK, pk[0]);
+      tc::tmem_st16(sbase + buf * AT_BK + 16, pk[1]);
+      tc::tmem_wait_st();
       l += ls;
       tc::fence_before_sync();
-      tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&p_full[t]);
+      if (lane == 0) tc::mbar_arrive(&p_full[2 * t + buf]);
     }
     // ---- epilogue: wait for the last P V, then O / l (or the partial).  The
     // stores wait for the preceding grid (the previous step may still read
     // the output); everything above reads only this step's inputs.
-    if (ok && nblk > 0 && !at_wait_warp(&pv_done[t], (nblk - 1) & 1u, abort_flag, a.ws, lane)) ok = false;
+    if (ok && nblk > 0 &&
+        !at_wait_warp(&pv_done[2 * t + ((nblk - 1) & 1)], ((nblk - 1) >> 1) & 1u, abort_flag, a.ws, lane))
+      ok = false;
     pdl_wait();
     tc::fence_after_sync();
     if (ok && warp_live && nblk > 0) {  // TMEM loads by the whole warp, stores by the real rows
@@ -583,8 +582,8 @@ int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void
     mkc = mkt;
     mvc = mvt;
   }
-  const size_t smem = 1024 + (size_t)AT_TILES * (AT_QTILE + AT_PTILE) + (size_t)2 * AT_STAGES * AT_KVTILE +
-                      (size_t)AT_ROWS * p.W * sizeof(uint32_t) + 256;
+  const size_t smem = 1024 + (size_t)AT_TILES * AT_QTILE + (size_t)2 * AT_STAGES * AT_KVTILE +
+                      (size_t)AT_ROWS * p.W * sizeof(uint32_t) + 512;
   cudaError_t ce = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   dim3 grid((p.T * p.G + AT_ROWS - 1) / AT_ROWS, p.Hkv * a.NS, p.B);
