@@ -366,31 +366,57 @@ def run_medusa(args, world, rank, local):
                 "step_achieved_gbs": round(byts["step"] / (ms * 1e-3) / 1e9, 1),
                 "step_frac": round(byts["step"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
 
-    # ---- end to end through the public API: per-step inputs from pinned host
-    # memory, results read back to the host every step
+    # ---- end to end through the public API: every step's inputs are copied
+    # from pinned host memory and its result is read back to the host.  Two
+    # buffer sets pipeline the copies with the steps: step n+1's inputs upload
+    # on an upload stream while step n computes, and the host waits for step n's
+    # result while step n+1 runs (each step still copies in and reads out).
     step_in = ["h", "root_token", "q", "k_tree", "v_tree"]
     host_in = {k: inp[k].pin_memory() for k in step_in}
     step_out = ["accept_len", "acc_tokens", "bonus"]
-    host_out = {k: torch.empty(out[k].shape, dtype=out[k].dtype).pin_memory() for k in step_out}
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
-
-    def e2e_step():
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()  # one stream each way: an upload never queues behind a readback
+    sets = []
+    for j in range(2):
+        d_j = dict(dinp)
         for k in step_in:
-            dinp[k].copy_(host_in[k], non_blocking=True)
-        M.medusa_step(cfg, io, ws)
-        for k in step_out:
-            host_out[k].copy_(out[k], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+            d_j[k] = torch.empty_like(dinp[k])
+        o_j = M.alloc_outputs(cfg)
+        sets.append({"in": d_j, "out": o_j, "io": M.step_io(d_j, o_j), "ws": M.alloc_workspace(cfg),
+                     "host_out": {k: torch.empty(o_j[k].shape, dtype=o_j[k].dtype).pin_memory() for k in step_out},
+                     "ev_in": torch.cuda.Event(), "ev_done": torch.cuda.Event(), "ev_out": torch.cuda.Event()})
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in sets[0]["host_out"].values())
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_run(n_steps):
+        last = None
+        for n in range(n_steps):
+            b = sets[n % 2]
+            with torch.cuda.stream(up):
+                up.wait_event(b["ev_done"])  # the set's previous step has finished with its inputs
+                for k in step_in:
+                    b["in"][k].copy_(host_in[k], non_blocking=True)
+                b["ev_in"].record(up)
+            comp.wait_event(b["ev_in"])
+            M.medusa_step(cfg, b["io"], b["ws"], comp)
+            b["ev_done"].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(b["ev_done"])
+                for k in step_out:
+                    b["host_out"][k].copy_(b["out"][k], non_blocking=True)
+                b["ev_out"].record(down)
+            if last is not None:
+                last["ev_out"].synchronize()  # step n-1's result is on the host
+            last = b
+        last["ev_out"].synchronize()
+        return last["host_out"]
+
+    e2e_run(4)
     barrier(world)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
+    res_host = e2e_run(args.steps)
     e2e_dt = reduce_max((time.perf_counter() - t0) / args.steps, world)
-    assert host_out["accept_len"].tolist() == planted
+    assert res_host["accept_len"].tolist() == planted
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
