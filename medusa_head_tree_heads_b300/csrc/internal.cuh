@@ -64,7 +64,7 @@ int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* to
 size_t verify_tc_part_bytes(int V, int N);
 size_t heads_tc_zs_bytes(int K, int B, int H);
 size_t heads_tc_slot_bytes(int B);
-bool heads_tc_supported(const Plan& p);  // after finish_plan
+bool heads_tc_supported(const Plan& p);  // from make_plan's fields alone
 int launch_fc_tc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
 int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t st, int* ctas, int* upc, int* ups);
 int launch_proj_tc(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws, cudaStream_t st);

@@ -62,8 +62,14 @@ extern "C" int medusa_heads_topk_noalloc(const medusa_config_t* cfg, const void*
   int s = make_plan(cfg, &p);
   if (s != MEDUSA_OK) return s;
   if (!al16(h) || !al16(W1) || !al16(b1) || !al16(W2) || !topk_idx || !topk_val) return MEDUSA_ERR_INVALID_ARG;
-  // the heads stage uses the workspace up to the end of the candidate slots
-  const size_t need = p.off_cand_seg + (size_t)kMaxStreamCtas * kMaxPieces * sizeof(int);
+  // the heads stage uses the workspace up to the end of the candidate slots,
+  // and the tensor-core heads also their z pairs, cut-tile partials and
+  // tickets, which the layout places further on
+  size_t need = p.off_cand_seg + (size_t)kMaxStreamCtas * kMaxPieces * sizeof(int);
+  if (heads_tc_supported(p)) {
+    const size_t tc_end = p.off_ht_tickets + 2 * (size_t)kHeadsTcMaxCtas * sizeof(int);
+    if (tc_end > need) need = tc_end;
+  }
   if (need > kNoAllocScratchBytes) return MEDUSA_ERR_UNSUPPORTED;
   uint8_t* ws = nullptr;
   if ((s = scratch_for_current_device(&ws)) != MEDUSA_OK) return s;

@@ -136,3 +136,16 @@ def test_status_strings():
     assert M.status_string(0) == "MEDUSA_OK"
     assert M.status_string(-4) == "MEDUSA_ERR_TIMEOUT"
     assert M.status_string(123) == "MEDUSA_ERR_UNKNOWN"
+
+
+def test_noalloc_rejects_configs_beyond_its_scratch_on_the_host():
+    """The fixed-scratch heads entry point checks the whole stretch of scratch
+    its kernels touch before any launch: at batch 32 the tensor-core heads'
+    buffers lie past 16 MiB (behind the verification partials in the layout)
+    while the candidate slots end below it; both batch 32 and batch 64 are
+    refused with MEDUSA_ERR_UNSUPPORTED and no device call is made."""
+    fake = ctypes.c_void_p(4096)  # aligned, never dereferenced: the call stops on the host
+    for over in (dict(batch=32), dict(batch=64, hidden=8192, n_q_heads=64, n_kv_heads=64, n_heads=8)):
+        cfg = M.make_config(synth.SHAPES["7b-mini"], **over)
+        r = M.lib().medusa_heads_topk_noalloc(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake, None)
+        assert r == -2, (over, r)
