@@ -73,6 +73,14 @@ typedef enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 } medusa_dtype_t;
  * its parent's draw is kept, so the accepted tokens follow the base model's
  * sampling distribution (bf16 only). */
 typedef enum { MEDUSA_ACCEPT_GREEDY = 0, MEDUSA_ACCEPT_TYPICAL = 1, MEDUSA_ACCEPT_SAMPLE = 2 } medusa_accept_t;
+/* Launch order of medusa_step (the results are the same bits either way).
+ * SERIAL: heads, candidate tree, tree attention, verification, acceptance.
+ * OVERLAP: the tree attention runs beside the head projection, on the SMs the
+ * projection's grid leaves free (the attention reads no head output); bf16,
+ * head dim 128 and B <= 32 only, else MEDUSA_ERR_UNSUPPORTED.  AUTO takes
+ * OVERLAP where the attention is short next to the projection's weight stream
+ * (a batch-1 7B-class step), else SERIAL. */
+typedef enum { MEDUSA_SCHEDULE_AUTO = 0, MEDUSA_SCHEDULE_SERIAL = 1, MEDUSA_SCHEDULE_OVERLAP = 2 } medusa_schedule_t;
 
 /* Sizes and options of one step (host memory, read during the call only). */
 typedef struct {
@@ -110,6 +118,7 @@ typedef struct {
    * sample_step (or seed). */
   uint32_t sample_seed[2];
   int32_t sample_step;
+  int32_t schedule; /* medusa_schedule_t, read by medusa_step and medusa_step_launches */
 } medusa_config_t;
 
 /* Candidate tree, device arrays allocated by the caller (sizes from
@@ -260,8 +269,13 @@ int medusa_next_inputs(const medusa_config_t* cfg, const void* attn_out, const i
                        const int32_t* accept_len, const int32_t* bonus, void* h_next, int32_t* root_next,
                        void* workspace, void* stream);
 
-/* The whole step: heads_topk, tree_build, tree_attn, verify_accept, in order on
- * `stream`.  io is host memory holding device pointers. */
+/* The whole step: heads_topk, tree_build, tree_attn, verify_accept on
+ * `stream`, in the order cfg->schedule picks (MEDUSA_SCHEDULE_OVERLAP issues
+ * the tree attention right after the head projection, which it runs beside).
+ * io is host memory holding device pointers.  Everything the step reads may be
+ * written by earlier work in the stream, and everything it writes may be read
+ * by later work: kernels of the step start early only beside other kernels of
+ * the same step, and the first one waits for all earlier work. */
 int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream);
 
 /* medusa_step with timing: the same launches, plus an external event record
@@ -269,11 +283,12 @@ int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* wo
  * graph) of events[2k] just before and events[2k+1] just after stage k
  * (events: host array of n_events >= 2 * MEDUSA_STEP_KERNELS cudaEvent_t
  * created by the caller).  Stages, each one or two kernel launches: 0 head
- * layer, 1 head projection (at batch <= 4 with bf16 the streaming kernel
+ * layer, 1 head projection (at batch <= 32 with bf16 the tensor-core kernel
  * alone; otherwise with its top-k candidate merge), 2 tree build (at batch
- * <= 4 with bf16 fused with the top-k candidate merge), 3 tree attention
+ * <= 32 with bf16 fused with the top-k candidate merge), 3 tree attention
  * (+ split combine), 4 verification projection (+ partial merge),
- * 5 acceptance. */
+ * 5 acceptance.  Under MEDUSA_SCHEDULE_OVERLAP stage 3 is issued before stage
+ * 2; the records around each stage keep the stages from overlapping. */
 #define MEDUSA_STEP_KERNELS 6
 int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
                          void* const* events, int32_t n_events);

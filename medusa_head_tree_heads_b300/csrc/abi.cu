@@ -10,7 +10,7 @@ namespace medusa {
 int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
 int launch_bounded_wait_probe(uint8_t* ws, uint64_t budget_ns, cudaStream_t st);
 int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
-                      const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st);
+                      const medusa_tree_t& t, uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st);
 
 // head layer / head projection: the tensor-core kernel for bf16 batches up to
 // 32, else the general streaming kernel
@@ -59,6 +59,12 @@ int make_plan(const medusa_config_t* c, Plan* p) {
     return MEDUSA_ERR_INVALID_ARG;
   if (c->accept_mode == MEDUSA_ACCEPT_SAMPLE && !(c->temperature > 0.f)) return MEDUSA_ERR_INVALID_ARG;
   if (c->accept_mode == MEDUSA_ACCEPT_SAMPLE && c->dtype != MEDUSA_BF16) return MEDUSA_ERR_UNSUPPORTED;
+  if (c->schedule != MEDUSA_SCHEDULE_AUTO && c->schedule != MEDUSA_SCHEDULE_SERIAL &&
+      c->schedule != MEDUSA_SCHEDULE_OVERLAP)
+    return MEDUSA_ERR_INVALID_ARG;
+  if (c->schedule == MEDUSA_SCHEDULE_OVERLAP &&
+      (c->dtype != MEDUSA_BF16 || c->head_dim != 128 || c->batch > kHeadsTcMaxBatch))
+    return MEDUSA_ERR_UNSUPPORTED;  // needs the tensor-core heads and attention kernels
   if (c->n_heads > MEDUSA_MAX_HEADS || c->depth > MEDUSA_MAX_DEPTH || c->depth > c->n_heads)
     return MEDUSA_ERR_UNSUPPORTED;
   if (c->hidden % 64 != 0) return MEDUSA_ERR_UNSUPPORTED;
@@ -89,6 +95,7 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   p->temperature = c->temperature;
   p->eps = c->eps;
   p->delta = c->delta;
+  p->schedule = c->schedule;
   // tree tables: the Cartesian tree of topk[] or the caller's explicit tree
   TreeDims& td = p->tree;
   td.D = p->D;
@@ -197,6 +204,13 @@ int make_plan(const medusa_config_t* c, Plan* p) {
 // launch shapes need the device's SM count
 void finish_plan(Plan* p) {
   p->sm_count = sm_count();
+  // The tensor-core heads kernels stream their weights faster on ~5/6 of the
+  // SMs than on all of them (7B: 240 vs 252 us for layer + projection; 13B:
+  // 306 vs 315), and the SMs left over host the tree attention under the
+  // overlap schedule.
+  p->heads_ctas = p->sm_count - p->sm_count / 6;
+  if (p->heads_ctas < 1) p->heads_ctas = 1;
+  p->overlap = false;
   p->fc_nc = pick_nc(p->H, p->B);
   p->fc_ctiles = (p->B + p->fc_nc - 1) / p->fc_nc;
   p->pj_nc = pick_nc(p->H, p->B);
@@ -212,6 +226,23 @@ int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* to
 }
 
 static bool aligned16(const void* x) { return x && ((uintptr_t)x & 15u) == 0; }
+
+// medusa_step's schedule (after finish_plan).  AUTO overlaps when the unsplit
+// attention, on the SMs the projection leaves free, is estimated to take at
+// most half the projection's weight stream: per CTA ~15 us fixed plus ~1.3 us
+// per 64-key block (measured on the 7B and 33B shapes), the stream at ~6 TB/s.
+static bool pick_overlap(const Plan& p) {
+  if (p.schedule == MEDUSA_SCHEDULE_SERIAL) return false;
+  if (!heads_tc_supported(p) || !attn_tc_supported(p)) return false;
+  if (p.schedule == MEDUSA_SCHEDULE_OVERLAP) return true;
+  const int free_sms = p.sm_count - heads_tc_proj_grid(p);
+  if (free_sms < 8) return false;
+  const long long ctas = attn_tc_unsplit_ctas(p);
+  const int nb = (p.Lc + 63) / 64 + (p.T + 63) / 64;
+  const double att_us = (double)((ctas + free_sms - 1) / free_sms) * (15.0 + 1.3 * nb);
+  const double proj_us = (double)p.K * p.V * p.H * 2 / 6.0e6;
+  return att_us <= 0.5 * proj_us;
+}
 
 static int cuda_status(int e) { return e == 0 ? MEDUSA_OK : MEDUSA_ERR_CUDA; }
 
@@ -367,9 +398,10 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   if ((s = check_tree(p, &io->tree)) != MEDUSA_OK) return s;
   if (events && n_events < 2 * MEDUSA_STEP_KERNELS) return MEDUSA_ERR_INVALID_ARG;
   finish_plan(&p);
+  p.overlap = pick_overlap(p);
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = (uint8_t*)workspace;
-  int k = 0, e = 0;
+  int e = 0;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (events && cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MEDUSA_ERR_CUDA;
   auto rec = [&](int i) {  // inside a capture only external records keep their timestamps
@@ -378,28 +410,36 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
             ? (int)cudaEventRecordWithFlags((cudaEvent_t)events[i], st, cudaEventRecordExternal)
             : (int)cudaEventRecord((cudaEvent_t)events[i], st);
   };
-#define MEDUSA_STAGE(call)  \
-  rec(2 * k);               \
-  if (e == 0) e = (call);   \
-  rec(2 * k + 1);           \
-  ++k;                      \
+#define MEDUSA_STAGE(k, call) \
+  rec(2 * (k));               \
+  if (e == 0) e = (call);     \
+  rec(2 * (k) + 1);           \
   if (e) return cuda_status(e);
-  MEDUSA_STAGE(launch_head_layer(p, io->h, io->W1, io->b1, ws, st))
+#define MEDUSA_ATTN_STAGE                                                                                    \
+  MEDUSA_STAGE(3, launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, \
+                                   io->tree.mask, io->attn_out, ws, st))
+  MEDUSA_STAGE(0, launch_head_layer(p, io->h, io->W1, io->b1, ws, st))
   if (heads_tc_supported(p)) {
-    // the projection kernel alone, then one kernel for the candidate merge and the tree
+    // the projection kernel alone, then one kernel for the candidate merge and
+    // the tree; under the overlap schedule the attention is issued between them
     int ctas = 0, upc = 0, ups = 0;
-    MEDUSA_STAGE(launch_proj_tc_only(p, io->W2, ws, st, &ctas, &upc, &ups))
-    MEDUSA_STAGE(launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, upc, ups, st))
+    MEDUSA_STAGE(1, launch_proj_tc_only(p, io->W2, ws, st, &ctas, &upc, &ups))
+    if (p.overlap) {
+      MEDUSA_ATTN_STAGE
+    }
+    MEDUSA_STAGE(2, launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, upc, ups, st))
   } else {
-    MEDUSA_STAGE(launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
-    MEDUSA_STAGE(launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
+    MEDUSA_STAGE(1, launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
+    MEDUSA_STAGE(2, launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
   }
-  MEDUSA_STAGE(launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens,
-                                io->tree.mask, io->attn_out, ws, st))
-  MEDUSA_STAGE(launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit, io->node_lse,
+  if (!p.overlap) {
+    MEDUSA_ATTN_STAGE
+  }
+  MEDUSA_STAGE(4, launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit, io->node_lse,
                              io->node_entropy, ws, st))
-  MEDUSA_STAGE(launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse,
+  MEDUSA_STAGE(5, launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse,
                              io->node_entropy, io->accept_len, io->acc_tokens, io->acc_nodes, io->bonus, ws, st))
+#undef MEDUSA_ATTN_STAGE
 #undef MEDUSA_STAGE
   return MEDUSA_OK;
 }
@@ -429,12 +469,13 @@ int medusa_step_launches(const medusa_config_t* cfg) {
   int s = make_plan(cfg, &p);
   if (s != MEDUSA_OK) return s;
   finish_plan(&p);
+  p.overlap = pick_overlap(p);
   int n = 6;                        // one launch per stage
   if (!heads_tc_supported(p)) n += 1;  // separate top-k merge (else fused with the tree)
   if (p.bf16) {
     int NS, cb;
     attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &NS, &cb);
-    if (attn_tc_supported(p)) NS = attn_tc_splits(p.B, p.T, p.G, p.Hkv, p.L);
+    if (attn_tc_supported(p)) NS = p.overlap ? 1 : attn_tc_splits(p.B, p.T, p.G, p.Hkv, p.L);
     if (NS > 1) n += 1;             // split-attention combine
     n += 1;                         // verification partial merge
   }

@@ -28,7 +28,9 @@
 // loads V, warp 2 allocates TMEM and issues S = Q K^T, warp 3 issues O += P V,
 // warps 4..7 and 8..11 run the softmax and epilogue of tiles 0 and 1.  With
 // fewer (row pair, b, g) CTAs than SMs the key blocks are split into NS equal
-// shares (partials merged by the combine kernel).  Every wait is bounded.
+// shares (partials merged by the combine kernel).  In the fused step's overlap
+// schedule the kernel runs unsplit beside the head projection, on the SMs the
+// projection's grid leaves free.  Every wait is bounded.
 #include <limits.h>
 
 #include "internal.cuh"
@@ -63,6 +65,10 @@ struct AtArgs {
   uint8_t* ws;
   const int32_t* lens;  // [B] per-sequence cache lengths, or null (L for all)
   int Lc;
+  // overlap schedule of the fused step: launched right after the head
+  // projection, whose kernel lets it start only after everything before the
+  // step has completed, so no store waits and the CTAs retire freely
+  int nowait;
 };
 
 __device__ __forceinline__ uint32_t at_sw(int r, int unit) {  // byte offset of 16-byte unit `unit` of row r
@@ -431,7 +437,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (ok && nblk > 0 &&
         !at_wait_warp(&pv_done[2 * t + ((nblk - 1) & 1)], ((nblk - 1) >> 1) & 1u, abort_flag, a.ws, lane))
       ok = false;
-    pdl_wait();
+    if (!a.nowait) pdl_wait();
     tc::fence_after_sync();
     if (ok && warp_live && nblk > 0) {  // TMEM loads by the whole warp, stores by the real rows
       if (a.NS > 1) {
@@ -482,7 +488,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, AT_TMEM_COLS);
   }
-  pdl_wait();  // completes only after the preceding kernel (keeps the stream's order transitive)
+  if (!a.nowait) pdl_wait();  // completes only after the preceding kernel (keeps the stream's order transitive)
 }
 
 // ------------------------------------------------------------------- host --
@@ -545,6 +551,10 @@ int attn_tc_splits(int B, int T, int G, int Hkv, int L) {
 
 bool attn_tc_supported(const Plan& p) { return p.bf16 && p.Dh == AT_DH; }
 
+long long attn_tc_unsplit_ctas(const Plan& p) {
+  return (long long)((p.T * p.G + AT_ROWS - 1) / AT_ROWS) * p.Hkv * p.B;
+}
+
 int launch_attn_combine(const Plan& p, float* part_o, float2* part_ml, int NS, void* out, cudaStream_t st);
 
 int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
@@ -565,7 +575,10 @@ int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void
   a.ws = ws;
   a.lens = lens;
   a.Lc = p.Lc;
-  a.NS = attn_tc_splits(p.B, p.T, p.G, p.Hkv, p.L);
+  // beside the projection the attention has only the SMs the projection
+  // leaves free: no key splits (and no combine launch)
+  a.NS = p.overlap ? 1 : attn_tc_splits(p.B, p.T, p.G, p.Hkv, p.L);
+  a.nowait = p.overlap ? 1 : 0;
   const size_t rows_all = (size_t)p.B * p.Hq * p.T * a.NS;
   a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);
   a.part_ml = reinterpret_cast<float2*>(ws + p.off_attn_part + rows_all * p.Dh * sizeof(float));

@@ -65,6 +65,12 @@ struct HtArgs {
   float* slot;    // [kHeadsTcMaxCtas][2][N][128] partial accumulators
   int* tk_own;    // [kHeadsTcMaxCtas] this kernel's boundary tickets
   int* tk_other;  // the other heads kernel's tickets, cleared here
+  // overlap schedule: the projection lets the next kernel (the tree
+  // attention) start only once its own wait has returned, and each of its CTAs
+  // counts itself into *proj_done when its last output is written; the layer
+  // clears the count
+  int late_trigger;
+  int* proj_done;
   uint8_t* ws;
 };
 
@@ -209,10 +215,14 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  pdl_trigger();
+  if (!a.late_trigger) pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    if (lane != 0 && a.late_trigger) {
+      pdl_wait();
+      pdl_trigger();
+    }
     if (lane == 0) {
       uint32_t g = 0;
       bool ok = true;
@@ -237,6 +247,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
         load_a(sa, &full[i], u0 + i);
       }
       pdl_wait();
+      if (a.late_trigger) pdl_trigger();
       for (int u = u0; u < u1; ++u, ++g) {
         const int s = g % S;
         const uint32_t ph = (g / S) & 1u;
@@ -265,6 +276,10 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
+    if (a.late_trigger) {
+      pdl_wait();
+      pdl_trigger();
+    }
     if (lane == 0) {
       uint32_t g = 0, tl = 0;
       bool ok = true;
@@ -309,10 +324,12 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
     const int etid = threadIdx.x - 64;
     pdl_wait();
+    if (a.late_trigger) pdl_trigger();
     // the other heads kernel has completed (or not started, for the layer):
     // its tickets are reset for its next launch
     for (int i = blockIdx.x * (32 * HT_EPI_WARPS) + etid; i < kHeadsTcMaxCtas; i += gridDim.x * 32 * HT_EPI_WARPS)
       a.tk_other[i] = 0;
+    if (EPI == 0 && blockIdx.x == 0 && etid == 0) *a.proj_done = 0;  // the previous step has completed
     float lv[KM];
     int li[KM];
     ht_reset<KM>(lv, li, KM);
@@ -429,8 +446,13 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  if (EPI == 1 && a.proj_done) __threadfence();  // this thread's outputs, before the count below
   tc::fence_before_sync();
   __syncthreads();
+  if (EPI == 1 && a.proj_done && threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(a.proj_done, 1);
+  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, tmem_cols);
@@ -454,11 +476,18 @@ static void ht_partition(const Plan& p, int rows, HtArgs* a, int* grid) {
   a->nks = (p.H + HT_KB * HT_BK - 1) / (HT_KB * HT_BK);
   a->tps = (rows + HT_M - 1) / HT_M;
   a->U = p.K * a->tps * a->nks;
-  const int cmax = p.sm_count < kHeadsTcMaxCtas ? p.sm_count : kHeadsTcMaxCtas;
+  const int cmax = p.heads_ctas < kHeadsTcMaxCtas ? p.heads_ctas : kHeadsTcMaxCtas;
   int upc = (a->U + cmax - 1) / cmax;
   if (upc < a->nks) upc = a->nks;  // a tile is cut at most once
   a->upc = upc;
   *grid = (a->U + upc - 1) / upc;
+}
+
+int heads_tc_proj_grid(const Plan& p) {
+  HtArgs a{};
+  int grid = 0;
+  ht_partition(p, p.V, &a, &grid);
+  return grid;
 }
 
 template <int EPI, int N, int KM>
@@ -485,6 +514,8 @@ static void ht_common(const Plan& p, uint8_t* ws, HtArgs* a) {
   a->zs = reinterpret_cast<__nv_bfloat16*>(ws + p.off_zs);
   a->slot = reinterpret_cast<float*>(ws + p.off_ht_slot);
   a->ws = ws;
+  a->late_trigger = 0;
+  a->proj_done = nullptr;
 }
 
 int launch_fc_tc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st) {
@@ -495,6 +526,7 @@ int launch_fc_tc(const Plan& p, const void* h, const void* W1, const void* b1, u
   a.b1 = reinterpret_cast<const __nv_bfloat16*>(b1);
   a.tk_own = reinterpret_cast<int*>(ws + p.off_ht_tickets);
   a.tk_other = a.tk_own + kHeadsTcMaxCtas;
+  a.proj_done = reinterpret_cast<int*>(ws) + TICKET_PROJ_DONE;
   int grid = 0;
   ht_partition(p, p.H, &a, &grid);
   if (a.upc > a.tps * a.nks) return (int)cudaErrorInvalidConfiguration;  // a CTA must touch at most 2 heads
@@ -522,6 +554,10 @@ int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t
   a.cand_seg = reinterpret_cast<int*>(ws + p.off_cand_seg);
   a.tk_other = reinterpret_cast<int*>(ws + p.off_ht_tickets);
   a.tk_own = a.tk_other + kHeadsTcMaxCtas;
+  if (p.overlap) {
+    a.late_trigger = 1;
+    a.proj_done = reinterpret_cast<int*>(ws) + TICKET_PROJ_DONE;
+  }
   int grid = 0;
   ht_partition(p, p.V, &a, &grid);
   if (a.upc > a.tps * a.nks) return (int)cudaErrorInvalidConfiguration;  // a CTA must touch at most 2 heads

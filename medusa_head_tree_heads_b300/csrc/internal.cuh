@@ -20,7 +20,8 @@ constexpr int kHeadsTcMaxBatch = 32;  // largest batch of the tensor-core heads 
 
 // ---------------------------------------------------------------- workspace --
 // [0, 256): int32 error word at 0, tickets from word 8 on.
-enum Ticket { TICKET_FC = 8, TICKET_PROJ = 9, TICKET_VERIFY = 10 };
+enum Ticket { TICKET_FC = 8, TICKET_PROJ = 9, TICKET_VERIFY = 10,
+              TICKET_PROJ_DONE = 11 };  // overlap schedule: projection CTAs finished this step
 
 // The candidate tree as tables, filled on the host for the Cartesian tree of
 // the per-depth list sizes or for a caller's explicit tree.  Nodes are in
@@ -47,6 +48,9 @@ struct Plan {
   int topk_n[MEDUSA_MAX_HEADS];  // entries kept per head
   // streaming partitions
   int sm_count;
+  int heads_ctas;  // grid cap of the tensor-core heads kernels
+  int schedule;    // medusa_schedule_t as given
+  bool overlap;    // medusa_step only: tree attention beside the head projection
   int fc_nc, fc_ctiles, pj_nc, pj_ctiles, vf_nc, vf_ctiles;  // columns per CTA, column tiles
   // workspace offsets (bytes)
   size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, off_vtc_part, off_attn_part;
@@ -80,6 +84,8 @@ int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* roo
                       cudaStream_t st);
 int attn_tc_splits(int B, int T, int G, int Hkv, int L);
 bool attn_tc_supported(const Plan& p);
+long long attn_tc_unsplit_ctas(const Plan& p);  // CTAs of the attention without key splits
+int heads_tc_proj_grid(const Plan& p);          // CTAs of the tensor-core head projection
 int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
                         const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st);
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
@@ -161,6 +167,26 @@ inline cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t s
 // first error wins
 __device__ __forceinline__ void set_error(uint8_t* ws, int code) {
   atomicCAS(reinterpret_cast<int*>(ws), 0, code);
+}
+
+// Bounded wait for a count that CTAs of an already running earlier grid raise
+// (each after a fence over its outputs): one thread polls with acquire loads;
+// past `budget_ns` it records MEDUSA_ERR_TIMEOUT and gives up.  The caller
+// makes the rest of its CTA wait on that thread (a barrier).
+__device__ __forceinline__ void wait_count(const int* count, int target, uint64_t budget_ns, uint8_t* ws) {
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+    if (v >= target) return;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > budget_ns) {
+      set_error(ws, MEDUSA_ERR_TIMEOUT);
+      return;
+    }
+  }
 }
 
 // float -> int with the same order (negative floats have their magnitude bits flipped)

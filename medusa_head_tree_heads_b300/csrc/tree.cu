@@ -79,6 +79,10 @@ struct MergeTreeArgs {
   const int* cand_seg;
   int32_t* out_idx;  // [B][K][kmax]
   float* out_val;
+  // overlap schedule: the preceding grid is the tree attention, and the
+  // projection's CTAs each raise this count once their candidates are written
+  const int* proj_done;
+  uint8_t* ws;
 };
 
 __device__ __forceinline__ bool mt_better(float v, int i, float w, int j) { return v > w || (v == w && i < j); }
@@ -91,6 +95,10 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(const __grid_constant__
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
   pdl_wait();  // the candidates come from the projection kernel
+  if (a.proj_done) {  // ... which may still be retiring beside the attention
+    if (threadIdx.x == 0) wait_count(a.proj_done, a.nctas, 20ull * 1000 * 1000, a.ws);
+    __syncthreads();
+  }
   if (warp < ta.K) {
     const int seg = warp;
     int kn = 1;
@@ -116,13 +124,13 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(const __grid_constant__
         const int sl = sl0 + u * 32 + lane;
         const bool in = sl < n_slots;
         const int blk = b_lo + sl / kMaxPieces, pc = sl % kMaxPieces;
-        sg[u] = in ? a.cand_seg[blk * kMaxPieces + pc] : -1;
+        sg[u] = in ? __ldcg(a.cand_seg + blk * kMaxPieces + pc) : -1;
         const size_t base = ((size_t)(blk * kMaxPieces + pc) * ta.B + b) * ta.kmax;
 #pragma unroll
         for (int i = 0; i < KM; ++i) {
           const bool ok = in && i < kn;
-          cv[u][i] = ok ? a.cand_val[base + i] : -INFINITY;
-          ci[u][i] = ok ? a.cand_idx[base + i] : INT_MAX;
+          cv[u][i] = ok ? __ldcg(a.cand_val + base + i) : -INFINITY;
+          ci[u][i] = ok ? __ldcg(a.cand_idx + base + i) : INT_MAX;
         }
       }
 #pragma unroll
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(const __grid_constant__
 }
 
 int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
-                      const medusa_tree_t& t, const uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st) {
+                      const medusa_tree_t& t, uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st) {
   MergeTreeArgs a;
   a.t.td = p.tree;
   a.t.B = p.B;
@@ -207,6 +215,8 @@ int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const i
   a.cand_seg = reinterpret_cast<const int*>(ws + p.off_cand_seg);
   a.out_idx = topk_idx;
   a.out_val = topk_val;
+  a.proj_done = p.overlap ? reinterpret_cast<const int*>(ws) + TICKET_PROJ_DONE : nullptr;
+  a.ws = ws;
   if (p.kmax <= 4) return (int)launch_k(merge_tree_kernel<4>, dim3(p.B), dim3(256), 0, st, true, a);
   if (p.kmax <= 8) return (int)launch_k(merge_tree_kernel<8>, dim3(p.B), dim3(256), 0, st, true, a);
   return (int)launch_k(merge_tree_kernel<MEDUSA_MAX_TOPK>, dim3(p.B), dim3(256), 0, st, true, a);

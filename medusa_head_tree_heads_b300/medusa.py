@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libmedusa.so")
 MAX_DEPTH = 8
 F32, BF16 = 0, 1
 GREEDY, TYPICAL, SAMPLE = 0, 1, 2
+AUTO, SERIAL, OVERLAP = 0, 1, 2  # medusa_schedule_t
 STATUS = {0: "MEDUSA_OK", -1: "MEDUSA_ERR_INVALID_ARG", -2: "MEDUSA_ERR_UNSUPPORTED", -3: "MEDUSA_ERR_CUDA",
           -4: "MEDUSA_ERR_TIMEOUT", -5: "MEDUSA_ERR_DEVICE"}
 
@@ -45,7 +46,8 @@ class Config(ctypes.Structure):
                 ("accept_mode", ctypes.c_int32), ("temperature", ctypes.c_float), ("eps", ctypes.c_float),
                 ("delta", ctypes.c_float), ("tree_nodes", ctypes.c_int32),
                 ("tree_parent", ctypes.POINTER(ctypes.c_int32)), ("tree_rank", ctypes.POINTER(ctypes.c_int32)),
-                ("sample_seed", ctypes.c_uint32 * 2), ("sample_step", ctypes.c_int32)]
+                ("sample_seed", ctypes.c_uint32 * 2), ("sample_step", ctypes.c_int32),
+                ("schedule", ctypes.c_int32)]
 
 
 class Tree(ctypes.Structure):
@@ -126,6 +128,7 @@ def make_config(shape, **over) -> Config:
     seed = getattr(shape, "sample_seed", (0, 0))
     c.sample_seed[0], c.sample_seed[1] = seed
     c.sample_step = getattr(shape, "sample_step", 0)
+    c.schedule = getattr(shape, "schedule", AUTO)
     c.temperature, c.eps, c.delta = shape.temperature, shape.eps, shape.delta
     parent = getattr(shape, "tree_parent", None)
     if parent is not None:  # explicit tree: host arrays kept alive with the config

@@ -64,7 +64,9 @@ def test_workspace_is_modest_at_full_size():
 BAD = [
     (dict(batch=0), -1), (dict(hidden=100), -2), (dict(head_dim=96), -2), (dict(n_kv_heads=3), -1),
     (dict(kv_capacity=10), -1), (dict(dtype=7), -1), (dict(accept_mode=5), -1), (dict(n_heads=9), -2),
-    (dict(depth=6), -2), (dict(temperature=0.0, accept_mode=1), -1),
+    (dict(depth=6), -2), (dict(temperature=0.0, accept_mode=1), -1), (dict(schedule=3), -1),
+    (dict(schedule=M.OVERLAP, dtype=M.F32), -2), (dict(schedule=M.OVERLAP, head_dim=64, n_q_heads=10), -2),
+    (dict(schedule=M.OVERLAP, batch=33), -2),
 ]
 
 
@@ -149,3 +151,17 @@ def test_noalloc_rejects_configs_beyond_its_scratch_on_the_host():
         cfg = M.make_config(synth.SHAPES["7b-mini"], **over)
         r = M.lib().medusa_heads_topk_noalloc(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake, None)
         assert r == -2, (over, r)
+
+
+def test_schedule_launch_counts():
+    """The overlap schedule runs the attention unsplit (no combine launch); AUTO
+    takes it for the batch-1 7B step only (host estimate; 148 SMs assumed
+    without a device)."""
+    def n(name, **over):
+        return M.step_launches(M.make_config(synth.SHAPES[name], **over))
+    assert n("7b-bf16", schedule=M.SERIAL) == 8   # 6 stages + attention combine + verification merge
+    assert n("7b-bf16", schedule=M.OVERLAP) == 7
+    assert n("7b-bf16") == 7 and n("7b-sample") == 7 and n("7b-sparse64") == 7
+    for name in ("13b-bf16", "gqa128k-bf16", "33b-bf16", "7b-mini", "7b-prof"):
+        assert n(name) == n(name, schedule=M.SERIAL), name
+    assert n("tiny-fp32") == n("tiny-fp32", schedule=M.SERIAL)

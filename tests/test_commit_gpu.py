@@ -132,7 +132,8 @@ def test_commit_without_room_changes_nothing():
     assert lens.item() == s.cap - 2
 
 
-def test_two_step_loop_commits_and_chains():
+@pytest.mark.parametrize("schedule", ["serial", "overlap"])
+def test_two_step_loop_commits_and_chains(schedule):
     """Step 1 (planted acceptance, bit-exact with the oracle), commit, next
     inputs, step 2 on the grown per-sequence caches: the committed rows and
     lengths equal the oracle's commit of its own step-1 acceptance, and step
@@ -143,7 +144,7 @@ def test_two_step_loop_commits_and_chains():
     n = U.np_inputs(inp)
     d = {k: v.cuda() for k, v in inp.items()}
     d["k_cache"], d["v_cache"] = d["k_cache"].clone(), d["v_cache"].clone()
-    cfg = M.make_config(s)
+    cfg = M.make_config(s, schedule={"serial": M.SERIAL, "overlap": M.OVERLAP}[schedule])
     ws = M.alloc_workspace(cfg)
     out = M.alloc_outputs(cfg)
     lens = torch.full((s.batch,), s.kv_len, dtype=torch.int32, device="cuda")

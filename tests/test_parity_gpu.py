@@ -41,6 +41,57 @@ def test_step_matches_oracle(name):
         assert int(res["bonus"][b]) == sq["bonus"]
 
 
+# bf16, head dim 128, batch <= 32: shapes the overlap schedule accepts (greedy,
+# typical, sample; sparse and wide trees; no cache; a depth-1 chain)
+OVERLAP_OK = ["7b-mini", "13b-mini", "gqa-mini", "gqa-b16-mini", "sample-mini", "sparse-mini",
+              "sparse-typical-mini", "wide-bf16", "nocache-bf16", "b5-mini", "chain-bf16", "13b-b8-split"]
+
+
+@pytest.mark.parametrize("name", OVERLAP_OK)
+def test_overlap_schedule_matches_oracle(name):
+    """The attention issued beside the head projection (unsplit, no waits),
+    the candidate merge waiting on the projection's completion count: every
+    output against the oracle, as in the serial order."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs(name)
+    ref = O.step(U.np_inputs(inp), s)
+    res = U.gpu_step(s, U.to_device(inp), schedule=M.OVERLAP)
+    U.compare_step(s, res, ref)
+    for b, sq in enumerate(U.plans()[name]["seqs"]):
+        assert int(res["accept_len"][b]) == sq["depth"]
+        assert int(res["bonus"][b]) == sq["bonus"]
+
+
+@pytest.mark.parametrize("name", ["7b-mini", "gqa-b16-mini"])
+def test_overlap_schedule_graph_replays_are_identical(name):
+    """One CUDA graph of the overlap step replayed back to back: the completion
+    count resets itself each step, and every replay gives the integers of an
+    eager serial step bit for bit."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs(name)
+    d = U.to_device(inp)
+    serial = U.gpu_step(s, d, schedule=M.SERIAL)
+    cfg = M.make_config(s, schedule=M.OVERLAP)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_outputs(cfg)
+    io = M.step_io(d, out)
+    M.medusa_step(cfg, io, ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        M.medusa_step(cfg, io, ws)
+    for _ in range(3):
+        for k in ("topk_idx", "node_argmax", "accept_len", "acc_nodes", "bonus"):
+            out[k].fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert M.medusa_get_device_error(ws) == 0
+        for k in ("topk_idx", "node_argmax", "accept_len", "acc_nodes", "acc_tokens", "bonus"):
+            assert torch.equal(out[k].cpu(), serial[k]), k
+        U.assert_close(out["attn_out"].float().cpu().numpy(), serial["attn_out"].float().numpy(), s.dtype,
+                       "attn_out")
+
+
 @pytest.mark.parametrize("name", ["tiny-fp32", "gqa-mini", "33b-mini", "deep-bf16"])
 def test_stage_calls_equal_fused_step(name):
     s, inp = U.planned_inputs(name)
@@ -180,11 +231,14 @@ def _sample_nodes(s, plan, b, rng, extra=4):
     return sorted(set(planted) | set(rand))
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
+@pytest.mark.parametrize("name,schedule", [(n, "auto") for n in FULL] + [("7b-bf16", "serial")])
+def test_full_size_sampled(name, schedule):
+    """Full size in the launch configuration the benchmark times (AUTO: the
+    overlap schedule for the 7B shapes), plus the 7B step in the serial order."""
+    from medusa_head_tree_heads_b300 import medusa as M
     s, inp = U.planned_inputs(name)
     plan = U.plans()[name]
-    res = U.gpu_step(s, U.to_device(inp))
+    res = U.gpu_step(s, U.to_device(inp), schedule={"auto": M.AUTO, "serial": M.SERIAL}[schedule])
     n = U.np_inputs(inp)
     # heads and top-k: every sequence, every head
     z = O.head_hidden(n["h"], n["W1"], n["b1"])

@@ -68,10 +68,11 @@ def to_device(inp: Dict[str, torch.Tensor], device="cuda") -> Dict[str, torch.Te
     return {k: v.to(device) for k, v in inp.items()}
 
 
-def gpu_step(s, dinp: Dict[str, torch.Tensor], fused: bool = True) -> Dict[str, torch.Tensor]:
-    """One step through the C ABI (fused medusa_step, or the four stage calls)."""
+def gpu_step(s, dinp: Dict[str, torch.Tensor], fused: bool = True, **over) -> Dict[str, torch.Tensor]:
+    """One step through the C ABI (fused medusa_step, or the four stage calls);
+    `over` sets config fields (e.g. schedule)."""
     from medusa_head_tree_heads_b300 import medusa as M
-    cfg = M.make_config(s)
+    cfg = M.make_config(s, **over)
     ws = M.alloc_workspace(cfg)
     out = M.alloc_outputs(cfg)
     if fused:
