@@ -77,9 +77,8 @@ typedef enum { MEDUSA_ACCEPT_GREEDY = 0, MEDUSA_ACCEPT_TYPICAL = 1, MEDUSA_ACCEP
  * SERIAL: heads, candidate tree, tree attention, verification, acceptance.
  * OVERLAP: the tree attention runs beside the head projection, on the SMs the
  * projection's grid leaves free (the attention reads no head output); bf16,
- * head dim 128 and B <= 32 only, else MEDUSA_ERR_UNSUPPORTED.  AUTO takes
- * OVERLAP where the attention is short next to the projection's weight stream
- * (a batch-1 7B-class step), else SERIAL. */
+ * head dim 128 and B <= 32 only, else MEDUSA_ERR_UNSUPPORTED.  AUTO is
+ * SERIAL (at the 7B shape the two orders measured the same step time). */
 typedef enum { MEDUSA_SCHEDULE_AUTO = 0, MEDUSA_SCHEDULE_SERIAL = 1, MEDUSA_SCHEDULE_OVERLAP = 2 } medusa_schedule_t;
 
 /* Sizes and options of one step (host memory, read during the call only). */

@@ -206,8 +206,9 @@ void finish_plan(Plan* p) {
   p->sm_count = sm_count();
   // The tensor-core heads kernels stream their weights faster on ~5/6 of the
   // SMs than on all of them (7B: 240 vs 252 us for layer + projection; 13B:
-  // 306 vs 315), and the SMs left over host the tree attention under the
-  // overlap schedule.
+  // 306 vs 315), and on the SMs left over the tree attention's first CTAs
+  // start early and run their key blocks during the projection (7B step: 316
+  // vs 324 us).
   p->heads_ctas = p->sm_count - p->sm_count / 6;
   if (p->heads_ctas < 1) p->heads_ctas = 1;
   p->overlap = false;
@@ -227,21 +228,14 @@ int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* to
 
 static bool aligned16(const void* x) { return x && ((uintptr_t)x & 15u) == 0; }
 
-// medusa_step's schedule (after finish_plan).  AUTO overlaps when the unsplit
-// attention, on the SMs the projection leaves free, is estimated to take at
-// most half the projection's weight stream: per CTA ~15 us fixed plus ~1.3 us
-// per 64-key block (measured on the 7B and 33B shapes), the stream at ~6 TB/s.
+// medusa_step's schedule.  AUTO is the serial order: at the 7B shape the
+// overlap order measured no faster (317.2 vs 316.0 us per step; the attention
+// vanishes from the critical path, but the projection beside it and the
+// verification after it each run longer), and in the serial order the
+// attention already starts on the SMs the heads kernels leave free and waits
+// only to store.
 static bool pick_overlap(const Plan& p) {
-  if (p.schedule == MEDUSA_SCHEDULE_SERIAL) return false;
-  if (!heads_tc_supported(p) || !attn_tc_supported(p)) return false;
-  if (p.schedule == MEDUSA_SCHEDULE_OVERLAP) return true;
-  const int free_sms = p.sm_count - heads_tc_proj_grid(p);
-  if (free_sms < 8) return false;
-  const long long ctas = attn_tc_unsplit_ctas(p);
-  const int nb = (p.Lc + 63) / 64 + (p.T + 63) / 64;
-  const double att_us = (double)((ctas + free_sms - 1) / free_sms) * (15.0 + 1.3 * nb);
-  const double proj_us = (double)p.K * p.V * p.H * 2 / 6.0e6;
-  return att_us <= 0.5 * proj_us;
+  return p.schedule == MEDUSA_SCHEDULE_OVERLAP && heads_tc_supported(p) && attn_tc_supported(p);
 }
 
 static int cuda_status(int e) { return e == 0 ? MEDUSA_OK : MEDUSA_ERR_CUDA; }

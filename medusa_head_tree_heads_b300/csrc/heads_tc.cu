@@ -483,13 +483,6 @@ static void ht_partition(const Plan& p, int rows, HtArgs* a, int* grid) {
   *grid = (a->U + upc - 1) / upc;
 }
 
-int heads_tc_proj_grid(const Plan& p) {
-  HtArgs a{};
-  int grid = 0;
-  ht_partition(p, p.V, &a, &grid);
-  return grid;
-}
-
 template <int EPI, int N, int KM>
 static int ht_launch(const CUtensorMap& tA, const CUtensorMap& tB, HtArgs a, int grid, bool pdl, cudaStream_t st) {
   constexpr size_t stage = (size_t)HT_KB * (HT_M + N) * HT_BK * 2;

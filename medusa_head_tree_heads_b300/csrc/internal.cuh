@@ -84,8 +84,6 @@ int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* roo
                       cudaStream_t st);
 int attn_tc_splits(int B, int T, int G, int Hkv, int L);
 bool attn_tc_supported(const Plan& p);
-long long attn_tc_unsplit_ctas(const Plan& p);  // CTAs of the attention without key splits
-int heads_tc_proj_grid(const Plan& p);          // CTAs of the tensor-core head projection
 int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
                         const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st);
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
