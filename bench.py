@@ -253,6 +253,13 @@ def time_oracle(s, inp, budget_s: float = 20.0) -> dict:
             "seconds": sum(times)}
 
 
+def workload_config(s, parallelism: str) -> dict:
+    """The workload's sizes, shared by both arms' JSON lines."""
+    return {"workload": s.name, "batch": s.batch, "hidden": s.hidden, "vocab": s.vocab, "heads": s.n_heads,
+            "topk": list(s.topk), "tree_nodes": s.n_nodes, "kv_len": s.kv_len, "q_heads": s.n_q_heads,
+            "kv_heads": s.n_kv_heads, "head_dim": s.head_dim, "accept": s.accept, "parallelism": parallelism}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -273,8 +280,7 @@ def run_reference(args, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": s.name, "batch": s.batch, "hidden": s.hidden, "vocab": s.vocab,
-                       "heads": s.n_heads, "topk": list(s.topk), "tree_nodes": s.n_nodes, "kv_len": s.kv_len},
+            "config": workload_config(s, "oracle on the host cores"),
             "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} whole step(s) of {s.name} after {args.warmup} warm-up"},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -421,12 +427,8 @@ def run_medusa(args, world, rank, local):
     line = {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
-            "config": {"workload": s.name, "batch": s.batch, "hidden": s.hidden, "vocab": s.vocab,
-                       "heads": s.n_heads, "topk": list(s.topk), "tree_nodes": s.n_nodes, "kv_len": s.kv_len,
-                       "q_heads": s.n_q_heads, "kv_heads": s.n_kv_heads, "head_dim": s.head_dim,
-                       "accept": s.accept, "parallelism": f"replicas{world}",
-                       "l2": "inputs larger than L2 (no flush)", "accept_len": acc,
-                       "launch": "eager" if args.no_graph else "cuda_graph"},
+            "config": dict(workload_config(s, f"replicas{world}"), l2="inputs larger than L2 (no flush)",
+                           accept_len=acc, launch="eager" if args.no_graph else "cuda_graph"),
             "roofline": roofline,
             "e2e": {"value": round(world / e2e_dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
