@@ -212,6 +212,11 @@ _add(Shape("nocache-bf16", "bf16", 256, 700, 2, 2, (3, 2), 0, 2, 2, 128, "typica
 _add(Shape("wide-bf16", "bf16", 256, 1200, 3, 1, (8, 8, 6), 100, 2, 1, 128, "greedy", ("fixed", 3), 3004))
 _add(Shape("deep-bf16", "bf16", 192, 600, 8, 2, (2, 2, 2, 2, 2, 2, 2, 2), 33, 3, 1, 64, "greedy", ("uniform", 0, 8),
            3005))
+# the per-depth list limit (16 entries): the tensor-core heads and the merged
+# tree at kmax 16, heads deeper than the tree; the fp32 streaming heads and
+# typical acceptance over 16 children per node
+_add(Shape("k16-bf16", "bf16", 256, 1200, 3, 2, (16, 16), 60, 2, 1, 128, "greedy", ("uniform", 0, 2), 3006))
+_add(Shape("k16-f32", "f32", 128, 800, 2, 2, (16, 9), 40, 2, 1, 64, "typical", ("uniform", 0, 2), 3007))
 
 # tensor tags for seed derivation
 _TAG = {"lm_head": 1, "W2": 2, "W1": 3, "b1": 4, "h": 5, "root": 6, "q": 7, "k_tree": 8, "v_tree": 9,

@@ -42,9 +42,9 @@ def test_step_matches_oracle(name):
 
 
 # bf16, head dim 128, batch <= 32: shapes the overlap schedule accepts (greedy,
-# typical, sample; sparse and wide trees; no cache; a depth-1 chain)
+# typical, sample; sparse and wide trees; no cache; a depth-1 chain; 16-entry lists)
 OVERLAP_OK = ["7b-mini", "13b-mini", "gqa-mini", "gqa-b16-mini", "sample-mini", "sparse-mini",
-              "sparse-typical-mini", "wide-bf16", "nocache-bf16", "b5-mini", "chain-bf16", "13b-b8-split"]
+              "sparse-typical-mini", "wide-bf16", "nocache-bf16", "b5-mini", "chain-bf16", "13b-b8-split", "k16-bf16"]
 
 
 @pytest.mark.parametrize("name", OVERLAP_OK)
@@ -92,7 +92,7 @@ def test_overlap_schedule_graph_replays_are_identical(name):
                        "attn_out")
 
 
-@pytest.mark.parametrize("name", ["tiny-fp32", "gqa-mini", "33b-mini", "deep-bf16"])
+@pytest.mark.parametrize("name", ["tiny-fp32", "gqa-mini", "33b-mini", "deep-bf16", "k16-bf16", "k16-f32"])
 def test_stage_calls_equal_fused_step(name):
     s, inp = U.planned_inputs(name)
     d = U.to_device(inp)
