@@ -287,7 +287,8 @@ int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* wo
  * <= 32 with bf16 fused with the top-k candidate merge), 3 tree attention
  * (+ split combine), 4 verification projection (+ partial merge),
  * 5 acceptance.  Under MEDUSA_SCHEDULE_OVERLAP stage 3 is issued before stage
- * 2; the records around each stage keep the stages from overlapping. */
+ * 2 (the results are the same; its stage times may include overlap with the
+ * projection). */
 #define MEDUSA_STEP_KERNELS 6
 int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
                          void* const* events, int32_t n_events);
