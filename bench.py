@@ -305,7 +305,7 @@ def run_medusa(args, world, rank, local):
     def step():
         M.medusa_step(cfg, io, ws)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if not args.no_graph:  # one CUDA graph per step: no host launch gaps between the kernels
@@ -453,7 +453,11 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         # each oracle step takes seconds: keep the whole run within a few minutes
-        args.steps, args.warmup = min(args.steps, 20), min(args.warmup, 2)
+        # (at most 20 timed steps, always 3 warm-up steps)
+        args.steps, args.warmup = min(args.steps, 20), 3
+    else:
+        args.warmup = max(args.warmup, 3)  # at least 3 warm-up steps, reported as run
+    if args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_medusa(args, world, rank, local)

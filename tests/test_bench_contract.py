@@ -1,0 +1,41 @@
+"""bench.py's JSON line on the CPU: the reference arm (the oracle timed on the
+host cores) prints one line with the keys the benchmark contract names, the
+same workload config as the CUDA arm, at least 3 warm-up steps, and nothing on
+ranks other than 0."""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny-fp32", "--steps", "2",
+                        "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    import bench
+    from medusa_head_tree_heads_b300 import synth
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "steps/s"
+    assert d["higher_is_better"] is True and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and abs(d["ms_per_step"] - 1e3 / d["value"]) < 1e-6 * d["ms_per_step"]
+    assert d["data"] == "synthetic" and d["vs_baseline"] is None
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    s = synth.SHAPES["tiny-fp32"]
+    want = bench.workload_config(s, "oracle on the host cores")
+    assert d["config"] == want
+
+
+def test_reference_arm_is_silent_off_rank_0(capsys):
+    import bench
+    args = argparse.Namespace(workload="tiny-fp32", steps=1, warmup=3, gpus=2)
+    bench.run_reference(args, world=2, rank=1)
+    assert capsys.readouterr().out == ""
