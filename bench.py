@@ -58,7 +58,7 @@ def flops(s) -> dict:
 # the SHA-256 of the kernel's source file at capture time: a changed kernel
 # reports null until it is captured again.
 TRAFFIC_CAPTURES = {
-    "7b-bf16": {"source": "medusa_head_tree_heads_b300/csrc/heads_tc.cu", "sha256": "9fcba06e9dbfb81350d3f3346688e0975739357b789ed81d5d5d58c66bcd09e4",
+    "7b-bf16": {"source": "medusa_head_tree_heads_b300/csrc/heads_tc.cu", "sha256": "b229ce57da05357858bc9cc6ed35b62d6496c647002b25edb0d18ab2b69d5f5b",
                 "bytes": 1312646656 + 3930368},
 }
 

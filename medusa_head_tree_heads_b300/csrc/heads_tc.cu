@@ -17,8 +17,10 @@
 // of one head, K-major, read by 3-D TMA boxes with the 128-byte swizzle, so a
 // head's ragged last tile reads zeros), the sequences are N (<= 64).  A work
 // unit is one tile x 128 reduction elements (two 64-wide boxes); each CTA
-// takes a contiguous run of units (stream-K), so every SM streams the same
-// number of weight bytes.  A tile cut by a CTA boundary is finished by
+// takes a contiguous run of units (stream-K), so every CTA streams the same
+// number of weight bytes; the grid is capped at 5/6 of the SMs (measured
+// faster than all of them; the rest host the attention's early CTAs).  A
+// tile cut by a CTA boundary is finished by
 // whichever of its two CTAs arrives second at a per-boundary ticket: both
 // store their partial accumulators, the second adds the other's and runs the
 // epilogue (no CTA ever waits for another).  Warp roles per CTA (one CTA per

@@ -171,8 +171,8 @@ _add(Shape("tiny-fp32-gqa", "f32", 256, 777, 3, 2, (3, 2), 70, 4, 2, 64, "typica
            kv_capacity=75))
 # batched reduced variants for the tensor-core heads (batch 5..32): odd batch,
 # a GQA typical batch of 16, a batch of 32 with half-tile hidden and ragged
-# reduction, and 7B-wide heads whose tile counts make the 148-way work split
-# cut tiles between CTAs in both the head layer and the projection
+# reduction, and 7B-wide heads whose tile counts make the heads' work split
+# (124 CTAs on 148 SMs) cut tiles between CTAs in both the layer and the projection
 _add(Shape("b5-mini", "bf16", 256, 777, 3, 5, (3, 2), 70, 2, 1, 128, "greedy", ("uniform", 0, 2), 2006))
 _add(Shape("gqa-b16-mini", "bf16", 512, 4099, 4, 16, (4, 3, 2, 2), 257, 4, 2, 128, "typical", ("uniform", 0, 4), 2007,
            kv_capacity=260))
