@@ -1,6 +1,9 @@
 """Builds libmedusa.so in-tree with nvcc for sm_103a (B300).
 
     python -m medusa_head_tree_heads_b300.build [--verbose-ptxas]
+
+Each CUDA source compiles to its own object under _build/ (in parallel, one
+nvcc per file), then one nvcc call links the shared library.
 """
 from __future__ import annotations
 
@@ -8,11 +11,14 @@ import glob
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libmedusa.so")
+OBJ = os.path.join(PKG, "..", "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 
 
 def nvcc() -> str:
@@ -27,11 +33,20 @@ def sources():
 
 
 def build(verbose_ptxas: bool = False, out: str = LIB, extra=()) -> str:
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC,-O2",
-           "-cudart", "shared", "--expt-relaxed-constexpr", "-o", out, *extra, *sources()]
-    if verbose_ptxas:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.run(cmd, check=True)
+    os.makedirs(OBJ, exist_ok=True)
+    srcs = sources()
+    objs = [os.path.join(OBJ, os.path.basename(s)[:-3] + ".o") for s in srcs]
+
+    def compile_one(so):
+        src, obj = so
+        cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", "-o", obj, src]
+        if verbose_ptxas:
+            cmd.insert(1, "-Xptxas=-v")
+        subprocess.run(cmd, check=True)
+
+    with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
+        list(ex.map(compile_one, zip(srcs, objs)))
+    subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", out, *objs], check=True)
     return out
 
 

@@ -141,13 +141,15 @@ def test_status_strings():
 
 
 def test_noalloc_rejects_configs_beyond_its_scratch_on_the_host():
-    """The fixed-scratch heads entry point checks the whole stretch of scratch
-    its kernels touch before any launch: at batch 32 the tensor-core heads'
-    buffers lie past 16 MiB (behind the verification partials in the layout)
-    while the candidate slots end below it; both batch 32 and batch 64 are
+    """The fixed-scratch heads entry point checks the heads stage's own
+    scratch against its 16 MiB before any launch.  Batch 32 with two lists
+    of 16 entries needs 2 x 1024 x 4 x 32 x 16 x 4 B = 16 MiB of top-k
+    candidates plus 10.5 MB of cut-tile partials; batch 64 (the CUDA-core heads) with 8 heads of width
+    8192 needs 64 x 8 x 8192 x 4 B = 16.8 MB of fp32 activations.  Both are
     refused with MEDUSA_ERR_UNSUPPORTED and no device call is made."""
     fake = ctypes.c_void_p(4096)  # aligned, never dereferenced: the call stops on the host
-    for over in (dict(batch=32), dict(batch=64, hidden=8192, n_q_heads=64, n_kv_heads=64, n_heads=8)):
+    for over in (dict(batch=32, depth=2, topk=(ctypes.c_int32 * 8)(16, 16, 0, 0, 0, 0, 0, 0)),
+                 dict(batch=64, hidden=8192, n_q_heads=64, n_kv_heads=64, n_heads=8)):
         cfg = M.make_config(synth.SHAPES["7b-mini"], **over)
         r = M.lib().medusa_heads_topk_noalloc(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake, None)
         assert r == -2, (over, r)
