@@ -124,6 +124,31 @@ def _gumbel_one_word(seed, step, node, V):
     return O.gumbel_noise(seed, step, node - node % 4, V)  # word 0 for every node of a counter
 
 
+def _philox(rounds=10, mul=O.PHILOX_MUL, weyl=O.PHILOX_WEYL, bump_first=False, order=(0, 1, 2, 3)):
+    """A Philox4x32 variant with one planted mistake."""
+    U = 0xFFFFFFFF
+
+    def f(c0, c1, c2, c3, k0, k1):
+        c = [np.asarray(x, dtype=np.uint64) for x in (c0, c1, c2, c3)]
+        k0, k1 = np.uint64(k0), np.uint64(k1)
+        for r in range(rounds):
+            if r or bump_first:
+                k0 = (k0 + np.uint64(weyl[0])) & np.uint64(U)
+                k1 = (k1 + np.uint64(weyl[1])) & np.uint64(U)
+            p0 = np.uint64(mul[0]) * c[0]
+            p1 = np.uint64(mul[1]) * c[2]
+            c = [(p1 >> np.uint64(32)) ^ c[1] ^ k0, p1 & np.uint64(U), (p0 >> np.uint64(32)) ^ c[3] ^ k1,
+                 p0 & np.uint64(U)]
+        return [c[i] for i in order]
+    return f
+
+
+def _gumbel_neg_log(seed, step, node, V):
+    # -ln(u): exponential noise, not Gumbel
+    g = O.gumbel_noise(seed, step, node, V)
+    return -np.log(np.exp(-np.exp(-g)))
+
+
 def _attn_scale_dh(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=None, batches=None):
     Dh = q.shape[-1]
     return O.tree_attention(q * (math.sqrt(Dh) / Dh), k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes, batches)
@@ -188,6 +213,13 @@ MUTANTS = [
     ("per-sequence lengths ignored", dict(tree_attention=_attn_uniform_len), P.check_kv_commit),
     ("Gumbel noise sign flipped", dict(gumbel_noise=_gumbel_sign), P.check_gumbel_max),
     ("one Philox word for four nodes", dict(gumbel_noise=_gumbel_one_word), P.check_gumbel_max),
+    ("Philox with nine rounds", dict(philox4x32_10=_philox(rounds=9)), P.check_philox_kat),
+    ("Philox output words swapped", dict(philox4x32_10=_philox(order=(0, 3, 2, 1))), P.check_philox_kat),
+    ("Philox key bumped before round 1", dict(philox4x32_10=_philox(bump_first=True)), P.check_philox_kat),
+    ("Philox Weyl constant off by two", dict(philox4x32_10=_philox(weyl=(0x9E3779B7, 0xBB67AE85))),
+     P.check_philox_kat),
+    ("Philox multipliers exchanged", dict(philox4x32_10=_philox(mul=O.PHILOX_MUL[::-1])), P.check_philox_kat),
+    ("exponential noise instead of Gumbel", dict(gumbel_noise=_gumbel_neg_log), P.check_gumbel_distribution),
 ]
 
 

@@ -411,6 +411,39 @@ def check_philox(M) -> None:
     assert abs(np.mean(flips) - 64) < 3, np.mean(flips)
 
 
+def check_philox_kat(M) -> None:
+    """Philox4x32-10 reproduces the generator's published known-answer
+    vectors (fixture tests/golden/philox4x32_10_kat.txt: the Random123
+    library's test file for the SC'11 generator), word for word: a dropped
+    or extra round, a wrong multiplier or Weyl constant, a key bumped before
+    the first round or output words in another order all change them."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert len(rows) == 3
+    for r in rows:
+        c = [np.uint64(int(x, 16)) for x in r[0:4]]
+        k0, k1 = int(r[4], 16), int(r[5], 16)
+        want = [int(x, 16) for x in r[6:10]]
+        got = [int(np.asarray(w).ravel()[0]) for w in M.philox4x32_10(*c, k0, k1)]
+        assert got == want, (r, ["%08x" % g for g in got])
+
+
+def check_gumbel_distribution(M) -> None:
+    """The noise is standard Gumbel: over 2^14 vocabulary rows of one node the
+    empirical CDF stays within the Kolmogorov-Smirnov bound (p ~ 1e-3) of
+    exp(-exp(-g)); its mean is the Euler-Mascheroni constant and its
+    variance pi^2/6 (within 5 standard errors)."""
+    n = 1 << 14
+    g = np.sort(M.gumbel_noise((5, 6), 3, 7, n))
+    cdf = np.exp(-np.exp(-g))
+    emp_hi = np.arange(1, n + 1) / n
+    emp_lo = np.arange(0, n) / n
+    ks = max(np.max(emp_hi - cdf), np.max(cdf - emp_lo))
+    assert ks < 1.95 / math.sqrt(n), ks
+    assert abs(g.mean() - 0.5772156649015329) < 5 * math.sqrt(math.pi ** 2 / 6 / n), g.mean()
+    assert abs(g.var() - math.pi ** 2 / 6) < 5 * 2.2 / math.sqrt(n), g.var()
+
+
 def check_gumbel_max(M) -> None:
     """Gumbel-max draws follow softmax(logit / temperature): over 40000 steps
     of a 5-token vocabulary the draw frequencies pass a chi-square test (4
@@ -481,7 +514,8 @@ def check_silu(M) -> None:
 CHECKS = [check_zero_init, check_head_vs_torch, check_topk, check_tree_2x3, check_tree_invariants,
           check_attention_paths, check_attention_single_node, check_verify, check_greedy_lossless,
           check_typical_special_cases, check_plans, check_bf16_rounding, check_silu, check_explicit_tree,
-          check_typical_shallow_tie, check_ragged_lengths, check_kv_commit, check_philox, check_gumbel_max]
+          check_typical_shallow_tie, check_ragged_lengths, check_kv_commit, check_philox, check_gumbel_max,
+          check_philox_kat, check_gumbel_distribution]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)

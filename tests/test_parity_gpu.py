@@ -285,10 +285,16 @@ def test_full_size_sampled(name, schedule):
                 assert g == r, (b, i)
             else:  # an unplanted node: the GPU's choice must tie the best within rounding
                 lg = float(o_st[j] @ O.decode(lm[g]))
+                # the bound scales with the best score; a sampled score adds
+                # Gumbel noise of order 1, so its best can sit near 0 while the
+                # rounding of the logit part does not shrink with it: there the
+                # scale is at least 1
+                scale = abs(st["maxlogit"][j])
                 if sample:
                     lg = lg / s.temperature + float(O.gumbel_noise(s.sample_seed, s.sample_step, ids[j],
                                                                    s.vocab)[g])
-                assert st["maxlogit"][j] - lg <= 2e-3 * max(1.0, abs(st["maxlogit"][j])), (b, i, g, r)
+                    scale = max(1.0, scale)
+                assert st["maxlogit"][j] - lg <= 2e-3 * scale, (b, i, g, r)
         if typical:
             U.assert_close(res["node_lse"][b, nodes].numpy(), st["lse"], s.dtype, "lse")
             U.assert_close(res["node_entropy"][b, nodes].numpy(), st["entropy"], s.dtype, "entropy")
