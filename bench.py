@@ -234,9 +234,26 @@ def oracle_inputs(inp):
     return out
 
 
-def time_oracle(s, inp, budget_s: float = 20.0) -> dict:
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def time_oracle(s, inp, budget_s: float = 20.0, single_thread: bool = True) -> dict:
     """The oracle as it stands, on this host's cores: whole steps until the
-    time budget is used (at least one)."""
+    time budget is used (at least one), with the BLAS library on every core;
+    then one whole step with it held to one thread."""
     from oracle import medusa_oracle as O
     n = oracle_inputs(inp)
     times = []
@@ -247,10 +264,18 @@ def time_oracle(s, inp, budget_s: float = 20.0) -> dict:
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_all > budget_s:
             break
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": len(times) / sum(times), "unit": "steps/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(times)} whole step(s) of {s.name} (numpy float64, BLAS on all cores)",
-            "seconds": sum(times)}
+    res = {"value": len(times) / sum(times), "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
+           "sample": f"{len(times)} whole step(s) of {s.name} (numpy float64, BLAS on all cores)",
+           "seconds": sum(times), "cpu_model": cpu_model()}
+    if single_thread:
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=1):
+            t0 = time.perf_counter()
+            O.step(n, s)
+            dt = time.perf_counter() - t0
+        res["single_thread"] = {"value": 1.0 / dt, "unit": "steps/s", "cores": 1,
+                                "sample": f"1 whole step of {s.name} (BLAS held to one thread)"}
+    return res
 
 
 def workload_config(s, parallelism: str) -> dict:
@@ -276,13 +301,14 @@ def run_reference(args, world, rank):
         O.step(n, s)
     dt = time.perf_counter() - t0
     v = args.steps / dt
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = host_cores()
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(s, "oracle on the host cores"),
             "cpu_baseline": {"value": v, "unit": "steps/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{args.steps} whole step(s) of {s.name} after {args.warmup} warm-up"},
+                             "sample": f"{args.steps} whole step(s) of {s.name} after {args.warmup} warm-up",
+                             "cpu_model": cpu_model()},
             "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -451,12 +477,11 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    args.warmup = max(args.warmup, 3)  # at least 3 warm-up steps, reported as run
     if args.impl == "reference":
         # each oracle step takes seconds: keep the whole run within a few minutes
-        # (at most 20 timed steps, always 3 warm-up steps)
-        args.steps, args.warmup = min(args.steps, 20), 3
-    else:
-        args.warmup = max(args.warmup, 3)  # at least 3 warm-up steps, reported as run
+        # (at most 20 timed steps, reported as run)
+        args.steps = min(args.steps, 20)
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:

@@ -186,7 +186,14 @@ int medusa_tree_size(const medusa_config_t* cfg, int32_t* n_nodes, int32_t* n_le
  *   topk_idx[b][k][r], topk_val[b][k][r]: rank r of head k, descending logit,
  *   ties to the lower token id; kmax = max_d k_d; head k (0-based) keeps
  *   k_{k+1} entries when k < D, else 1; unused entries are -1 / -inf.
- * h [B][H], W1 [K][H][H], b1 [K][H], W2 [K][V][H]. */
+ * h [B][H], W1 [K][H][H], b1 [K][H], W2 [K][V][H].
+ * Kernels: bf16 batches of at most 32 sequences run both head matrices on the
+ * tensor cores (z kept as a bf16 hi/lo pair, about 16 significant bits);
+ * larger bf16 batches and every fp32 config stream the weights through the
+ * CUDA cores (fp32 z and accumulation).  The results agree within the
+ * stated tolerances either way; only the speed differs (the CUDA-core path
+ * runs at 2B multiply-adds per weight element and falls below the memory
+ * bound as B grows). */
 int medusa_heads_topk(const medusa_config_t* cfg, const void* h, const void* W1, const void* b1,
                       const void* W2, int32_t* topk_idx, float* topk_val, void* workspace, void* stream);
 

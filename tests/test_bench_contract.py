@@ -13,6 +13,30 @@ import sys
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+def _reference_line(warmup: int) -> dict:
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny-fp32", "--steps", "2",
+                        "--warmup", str(warmup)], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [x for x in r.stdout.splitlines() if x.strip()]
+    assert len(lines) == 1
+    return json.loads(lines[0])
+
+
+def test_reference_arm_honours_the_warmup_it_is_given():
+    assert _reference_line(5)["warmup"] == 5
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    import bench
+    from medusa_head_tree_heads_b300 import synth
+    s = synth.SHAPES["tiny-fp32"]
+    inp = synth.make_inputs(s, synth.load_plans()[s.name])
+    cb = bench.time_oracle(s, inp, budget_s=0.0)
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["cpu_model"]
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0 and st["unit"] == "steps/s"
+
+
 def test_reference_arm_prints_one_contract_line():
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny-fp32", "--steps", "2",
                         "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
@@ -28,6 +52,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["data"] == "synthetic" and d["vs_baseline"] is None
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["cpu_model"]
     assert d["e2e"] == {"value": d["value"], "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     s = synth.SHAPES["tiny-fp32"]
     want = bench.workload_config(s, "oracle on the host cores")
