@@ -77,9 +77,13 @@ typedef enum { MEDUSA_ACCEPT_GREEDY = 0, MEDUSA_ACCEPT_TYPICAL = 1, MEDUSA_ACCEP
  * SERIAL: heads, candidate tree, tree attention, verification, acceptance.
  * OVERLAP: the tree attention runs beside the head projection, on the SMs the
  * projection's grid leaves free (the attention reads no head output); bf16,
- * head dim 128 and B <= 32 only, else MEDUSA_ERR_UNSUPPORTED.  AUTO is
- * SERIAL (at the 7B shape the two orders measured the same step time).  Any
- * other value is MEDUSA_ERR_INVALID_ARG (every call validates the config). */
+ * head dim 128 and B <= 32 only, else MEDUSA_ERR_UNSUPPORTED.  AUTO takes
+ * OVERLAP where it is supported and the attention is small next to the head
+ * projection (an estimate from the shape: at the 7B shape the step measured
+ * 301 us against 317 us), else SERIAL.  With the tensor-core heads (bf16,
+ * B <= 32) both orders issue the verification projection before the
+ * candidate merge and tree, which then run beside it.  Any other value is
+ * MEDUSA_ERR_INVALID_ARG (every call validates the config). */
 typedef enum { MEDUSA_SCHEDULE_AUTO = 0, MEDUSA_SCHEDULE_SERIAL = 1, MEDUSA_SCHEDULE_OVERLAP = 2 } medusa_schedule_t;
 
 /* Sizes and options of one step (host memory, read during the call only). */

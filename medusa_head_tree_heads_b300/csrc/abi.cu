@@ -9,8 +9,6 @@ namespace medusa {
 
 int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint8_t* ws, cudaStream_t st);
 int launch_bounded_wait_probe(uint8_t* ws, uint64_t budget_ns, cudaStream_t st);
-int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
-                      const medusa_tree_t& t, uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st);
 
 // head layer / head projection: the tensor-core kernel for bf16 batches up to
 // 32, else the general streaming kernel
@@ -228,14 +226,25 @@ int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* to
 
 static bool aligned16(const void* x) { return x && ((uintptr_t)x & 15u) == 0; }
 
-// medusa_step's schedule.  AUTO is the serial order: at the 7B shape the
-// overlap order measured no faster (317.2 vs 316.0 us per step; the attention
-// vanishes from the critical path, but the projection beside it and the
-// verification after it each run longer), and in the serial order the
-// attention already starts on the SMs the heads kernels leave free and waits
-// only to store.
+// medusa_step's schedule (after finish_plan).  AUTO takes the overlap order
+// when the unsplit attention, on the SMs the projection's grid leaves free,
+// is estimated to need at most half the time of the projection's weight
+// stream; a CTA of the attention is modelled as 15 us plus 1.3 us per 64-key
+// block (measured beside the projection on the 7B shape), the stream at
+// 6 TB/s.  Measured: 7B 301 us per step in the overlap order against 317 us
+// in the serial one; 13B 481 against 484; the large-vocabulary GQA and the
+// 33B shapes 1% and 0.4% slower in the overlap order.
 static bool pick_overlap(const Plan& p) {
-  return p.schedule == MEDUSA_SCHEDULE_OVERLAP && heads_tc_supported(p) && attn_tc_supported(p);
+  if (p.schedule == MEDUSA_SCHEDULE_SERIAL) return false;
+  if (!heads_tc_supported(p) || !attn_tc_supported(p)) return false;
+  if (p.schedule == MEDUSA_SCHEDULE_OVERLAP) return true;
+  const int free_sms = p.sm_count - heads_tc_proj_grid(p);
+  if (free_sms < 8) return false;
+  const long long ctas = attn_tc_unsplit_ctas(p);
+  const int nb = (p.L + 63) / 64 + (p.T + 63) / 64;
+  const double attn_us = (double)((ctas + free_sms - 1) / free_sms) * (15.0 + 1.3 * nb);
+  const double proj_us = (double)p.K * p.V * p.H * 2 / 6.0e6;
+  return attn_us <= 0.5 * proj_us;
 }
 
 static int cuda_status(int e) { return e == 0 ? MEDUSA_OK : MEDUSA_ERR_CUDA; }
@@ -393,6 +402,7 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   if (events && n_events < 2 * MEDUSA_STEP_KERNELS) return MEDUSA_ERR_INVALID_ARG;
   finish_plan(&p);
   p.overlap = pick_overlap(p);
+  p.late_tree = heads_tc_supported(p);
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* ws = (uint8_t*)workspace;
   int e = 0;
@@ -413,22 +423,33 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   MEDUSA_STAGE(3, launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, \
                                    io->tree.mask, io->attn_out, ws, st))
   MEDUSA_STAGE(0, launch_head_layer(p, io->h, io->W1, io->b1, ws, st))
-  if (heads_tc_supported(p)) {
-    // the projection kernel alone, then one kernel for the candidate merge and
-    // the tree; under the overlap schedule the attention is issued between them
+  if (p.late_tree) {
+    // Tensor-core heads: the projection, the tree attention and the
+    // verification projection, none of which reads the candidate tree's
+    // tokens, then the candidate merge + tree, which waits for the
+    // projection's completion count and so runs beside the verification
+    // projection, then the verification merge and the acceptance.
     int ctas = 0, upc = 0, ups = 0;
     MEDUSA_STAGE(1, launch_proj_tc_only(p, io->W2, ws, st, &ctas, &upc, &ups))
-    if (p.overlap) {
-      MEDUSA_ATTN_STAGE
-    }
-    MEDUSA_STAGE(2, launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, upc, ups, st))
-  } else {
-    MEDUSA_STAGE(1, launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
-    MEDUSA_STAGE(2, launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
-  }
-  if (!p.overlap) {
     MEDUSA_ATTN_STAGE
+    MEDUSA_STAGE(4, launch_verify_tc(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax,
+                                     io->node_maxlogit, io->node_lse, io->node_entropy, ws, st, VERIFY_GEMM))
+    MEDUSA_STAGE(2, launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, upc, ups,
+                                      true, st))
+    rec(10);
+    if (e == 0)
+      e = launch_verify_tc(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit,
+                           io->node_lse, io->node_entropy, ws, st, VERIFY_MERGE);
+    if (e == 0)
+      e = launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse, io->node_entropy,
+                        io->accept_len, io->acc_tokens, io->acc_nodes, io->bonus, ws, st);
+    rec(11);
+    if (e) return cuda_status(e);
+    return MEDUSA_OK;
   }
+  MEDUSA_STAGE(1, launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st))
+  MEDUSA_STAGE(2, launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st))
+  MEDUSA_ATTN_STAGE
   MEDUSA_STAGE(4, launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit, io->node_lse,
                              io->node_entropy, ws, st))
   MEDUSA_STAGE(5, launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse,

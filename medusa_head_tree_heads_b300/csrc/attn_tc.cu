@@ -551,6 +551,10 @@ int attn_tc_splits(int B, int T, int G, int Hkv, int L) {
 
 bool attn_tc_supported(const Plan& p) { return p.bf16 && p.Dh == AT_DH; }
 
+long long attn_tc_unsplit_ctas(const Plan& p) {
+  return (long long)((p.T * p.G + AT_ROWS - 1) / AT_ROWS) * p.Hkv * p.B;
+}
+
 int launch_attn_combine(const Plan& p, float* part_o, float2* part_ml, int NS, void* out, cudaStream_t st);
 
 int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,

@@ -67,10 +67,11 @@ struct HtArgs {
   float* slot;    // [kHeadsTcMaxCtas][2][N][128] partial accumulators
   int* tk_own;    // [kHeadsTcMaxCtas] this kernel's boundary tickets
   int* tk_other;  // the other heads kernel's tickets, cleared here
-  // overlap schedule: the projection lets the next kernel (the tree
-  // attention) start only once its own wait has returned, and each of its CTAs
-  // counts itself into *proj_done when its last output is written; the layer
-  // clears the count
+  // in medusa_step the projection lets the kernels after it start only once
+  // its own wait has returned (so they start after the step's earlier work is
+  // complete), and each of its CTAs counts itself into *proj_done when its
+  // last output is written (the candidate merge waits for that count instead
+  // of its preceding grid); the layer clears the count
   int late_trigger;
   int* proj_done;
   uint8_t* ws;
@@ -485,6 +486,13 @@ static void ht_partition(const Plan& p, int rows, HtArgs* a, int* grid) {
   *grid = (a->U + upc - 1) / upc;
 }
 
+int heads_tc_proj_grid(const Plan& p) {
+  HtArgs a{};
+  int grid = 0;
+  ht_partition(p, p.V, &a, &grid);
+  return grid;
+}
+
 template <int EPI, int N, int KM>
 static int ht_launch(const CUtensorMap& tA, const CUtensorMap& tB, HtArgs a, int grid, bool pdl, cudaStream_t st) {
   constexpr size_t stage = (size_t)HT_KB * (HT_M + N) * HT_BK * 2;
@@ -549,7 +557,7 @@ int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t
   a.cand_seg = reinterpret_cast<int*>(ws + p.off_cand_seg);
   a.tk_other = reinterpret_cast<int*>(ws + p.off_ht_tickets);
   a.tk_own = a.tk_other + kHeadsTcMaxCtas;
-  if (p.overlap) {
+  if (p.overlap || p.late_tree) {  // see HtArgs: dependents start after the wait, CTAs count themselves
     a.late_trigger = 1;
     a.proj_done = reinterpret_cast<int*>(ws) + TICKET_PROJ_DONE;
   }

@@ -51,6 +51,7 @@ struct Plan {
   int heads_ctas;  // grid cap of the tensor-core heads kernels
   int schedule;    // medusa_schedule_t as given
   bool overlap;    // medusa_step only: tree attention beside the head projection
+  bool late_tree;  // medusa_step only: candidate merge + tree beside the verification projection
   int fc_nc, fc_ctiles, pj_nc, pj_ctiles, vf_nc, vf_ctiles;  // columns per CTA, column tiles
   // workspace offsets (bytes)
   size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, off_vtc_part, off_attn_part;
@@ -74,8 +75,15 @@ int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t
 int launch_proj_tc(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws, cudaStream_t st);
 size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh);
 void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks);
+// the verification's two launches: the projection (partials per vocabulary
+// tile) and the merge of the partials (node results, typical keep flags)
+enum VerifyPart { VERIFY_BOTH = 0, VERIFY_GEMM = 1, VERIFY_MERGE = 2 };
 int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
-                     float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
+                     float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st,
+                     VerifyPart part = VERIFY_BOTH);
+int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
+                      const medusa_tree_t& t, uint8_t* ws, int nctas, int rpc, int S, bool count_wait,
+                      cudaStream_t st);
 
 // launchers (enqueue only; return cudaError_t as int)
 int launch_heads(const Plan& p, const void* h, const void* W1, const void* b1, const void* W2, int32_t* topk_idx,
@@ -84,6 +92,8 @@ int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* roo
                       cudaStream_t st);
 int attn_tc_splits(int B, int T, int G, int Hkv, int L);
 bool attn_tc_supported(const Plan& p);
+long long attn_tc_unsplit_ctas(const Plan& p);  // CTAs of the tensor-core attention without key splits
+int heads_tc_proj_grid(const Plan& p);          // CTAs of the tensor-core head projection
 int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
                         const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st);
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,

@@ -79,8 +79,11 @@ struct MergeTreeArgs {
   const int* cand_seg;
   int32_t* out_idx;  // [B][K][kmax]
   float* out_val;
-  // overlap schedule: the preceding grid is the tree attention, and the
-  // projection's CTAs each raise this count once their candidates are written
+  // The projection's CTAs each raise this count once their candidates are
+  // written.  With it the kernel runs beside the verification projection (its
+  // preceding grid, which reads nothing of this kernel's): it waits for the
+  // count instead of that grid, and waits for the grid only at its end, so
+  // that its completion still implies the completion of everything before it.
   const int* proj_done;
   uint8_t* ws;
 };
@@ -90,15 +93,25 @@ __device__ __forceinline__ bool mt_better(float v, int i, float w, int j) { retu
 template <int KM>
 __global__ void __launch_bounds__(256) merge_tree_kernel(const __grid_constant__ MergeTreeArgs a) {
   __shared__ int s_idx[MEDUSA_MAX_HEADS][MEDUSA_MAX_TOPK];
+  __shared__ int16_t s_parent[MEDUSA_MAX_NODES];
+  __shared__ uint8_t s_depth[MEDUSA_MAX_NODES], s_rank[MEDUSA_MAX_NODES];
   const TreeArgs& ta = a.t;
   const TreeDims& td = ta.td;
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
-  pdl_wait();  // the candidates come from the projection kernel
-  if (a.proj_done) {  // ... which may still be retiring beside the attention
-    if (threadIdx.x == 0) wait_count(a.proj_done, a.nctas, 20ull * 1000 * 1000, a.ws);
-    __syncthreads();
+  // the tree tables move to shared memory first: the walks below index them
+  // with data-dependent node ids, which parameter space serves slowly
+  for (int i = threadIdx.x; i < td.T; i += blockDim.x) {
+    s_parent[i] = td.parent[i];
+    s_depth[i] = td.depth[i];
+    s_rank[i] = td.rank[i];
   }
+  if (a.proj_done) {  // the candidates: every projection CTA has counted itself
+    if (threadIdx.x == 0) wait_count(a.proj_done, a.nctas, 20ull * 1000 * 1000, a.ws);
+  } else {
+    pdl_wait();  // the candidates come from the preceding grid, the projection
+  }
+  __syncthreads();
   if (warp < ta.K) {
     const int seg = warp;
     int kn = 1;
@@ -185,18 +198,38 @@ __global__ void __launch_bounds__(256) merge_tree_kernel(const __grid_constant__
     }
   }
   __syncthreads();
-  const int T = td.T;
+  const int T = td.T, W = td.W;
   for (int i = threadIdx.x; i < T; i += blockDim.x) {
-    const int d = td.depth[i];
-    ta.t.token[(size_t)b * T + i] = d == 0 ? ta.root[b] : s_idx[d - 1][td.rank[i]];
-    if (b == 0) write_node(td, ta.t, ta.L, i);
+    const int d = s_depth[i];
+    ta.t.token[(size_t)b * T + i] = d == 0 ? ta.root[b] : s_idx[d - 1][s_rank[i]];
+    if (b == 0) {
+      ta.t.depth[i] = d;
+      ta.t.parent[i] = s_parent[i];
+      ta.t.rank[i] = s_rank[i];
+      ta.t.pos[i] = ta.L + d;
+    }
   }
-  if (b == 0)
-    for (int l = threadIdx.x; l < td.n_leaves; l += blockDim.x) write_path(td, ta.t, l);
+  if (b == 0) {
+    for (int e = threadIdx.x; e < T * W; e += blockDim.x) {  // mask word w of node i
+      const int i = e / W, w = e - i * W;
+      uint32_t word = 0;
+      for (int j = i; j >= 0; j = s_parent[j])
+        if ((j >> 5) == w) word |= 1u << (j & 31);
+      ta.t.mask[e] = word;
+    }
+    for (int l = threadIdx.x; l < td.n_leaves; l += blockDim.x) {  // root-to-leaf path, then -1
+      const int leaf = td.leaf[l], dl = s_depth[leaf];
+      int32_t* row = ta.t.paths + (size_t)l * (td.D + 1);
+      for (int d = td.D; d > dl; --d) row[d] = -1;
+      for (int d = dl, j = leaf; d >= 0; --d, j = s_parent[j]) row[d] = j;
+    }
+  }
+  if (a.proj_done) pdl_wait();  // complete only after the preceding grid
 }
 
 int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
-                      const medusa_tree_t& t, uint8_t* ws, int nctas, int rpc, int S, cudaStream_t st) {
+                      const medusa_tree_t& t, uint8_t* ws, int nctas, int rpc, int S, bool count_wait,
+                      cudaStream_t st) {
   MergeTreeArgs a;
   a.t.td = p.tree;
   a.t.B = p.B;
@@ -215,7 +248,7 @@ int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const i
   a.cand_seg = reinterpret_cast<const int*>(ws + p.off_cand_seg);
   a.out_idx = topk_idx;
   a.out_val = topk_val;
-  a.proj_done = p.overlap ? reinterpret_cast<const int*>(ws) + TICKET_PROJ_DONE : nullptr;
+  a.proj_done = count_wait ? reinterpret_cast<const int*>(ws) + TICKET_PROJ_DONE : nullptr;
   a.ws = ws;
   if (p.kmax <= 4) return (int)launch_k(merge_tree_kernel<4>, dim3(p.B), dim3(256), 0, st, true, a);
   if (p.kmax <= 8) return (int)launch_k(merge_tree_kernel<8>, dim3(p.B), dim3(256), 0, st, true, a);

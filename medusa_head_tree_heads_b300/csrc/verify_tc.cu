@@ -625,7 +625,8 @@ size_t verify_tc_part_bytes(int V, int N) {
 }
 
 int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
-                     float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st) {
+                     float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st,
+                     VerifyPart part) {
   VtcArgs a;
   a.V = p.V;
   a.N = p.B * p.T;
@@ -655,6 +656,11 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, c
   a.keep = ws + p.off_keep;
   a.log_eps = p.typical ? logf(p.eps) : 0.f;
   a.log_delta = p.typical && p.delta > 0.f ? logf(p.delta) : -INFINITY;
+  const unsigned mgrid = (unsigned)((a.N + 7) / 8);
+  if (part == VERIFY_MERGE) {
+    if (a.typical) return (int)launch_k(verify_merge_kernel<true>, dim3(mgrid), dim3(256), 0, st, true, a);
+    return (int)launch_k(verify_merge_kernel<false>, dim3(mgrid), dim3(256), 0, st, true, a);
+  }
   const size_t stage = (size_t)(VT_SUB * VT_M + a.BN) * VT_BK * 2;
   const size_t fixed = 1024 + (size_t)4 * a.BN * sizeof(Soft) + 256;
   const size_t budget = 227 * 1024;
@@ -674,8 +680,7 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, c
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.n_tiles < p.sm_count ? a.n_tiles : p.sm_count;
   ce = launch_k(kern, dim3(grid), dim3(VT_THREADS), smem, st, true, tA, tB, a);
-  if (ce != cudaSuccess) return (int)ce;
-  const unsigned mgrid = (unsigned)((a.N + 7) / 8);
+  if (ce != cudaSuccess || part == VERIFY_GEMM) return (int)ce;
   if (a.typical) return (int)launch_k(verify_merge_kernel<true>, dim3(mgrid), dim3(256), 0, st, true, a);
   return (int)launch_k(verify_merge_kernel<false>, dim3(mgrid), dim3(256), 0, st, true, a);
 }

@@ -231,14 +231,15 @@ def _sample_nodes(s, plan, b, rng, extra=4):
     return sorted(set(planted) | set(rand))
 
 
-@pytest.mark.parametrize("name,schedule", [(n, "auto") for n in FULL] + [("7b-bf16", "overlap")])
+@pytest.mark.parametrize("name,schedule", [(n, "auto") for n in FULL] + [("7b-bf16", "serial")])
 def test_full_size_sampled(name, schedule):
-    """Full size in the launch configuration the benchmark times (AUTO), plus
-    the 7B step in the overlap order."""
+    """Full size in the launch configuration the benchmark times (AUTO: the
+    overlap order at the 7B shape, the serial order for the others), plus the
+    7B step in the serial order."""
     from medusa_head_tree_heads_b300 import medusa as M
     s, inp = U.planned_inputs(name)
     plan = U.plans()[name]
-    res = U.gpu_step(s, U.to_device(inp), schedule={"auto": M.AUTO, "overlap": M.OVERLAP}[schedule])
+    res = U.gpu_step(s, U.to_device(inp), schedule={"auto": M.AUTO, "serial": M.SERIAL, "overlap": M.OVERLAP}[schedule])
     n = U.np_inputs(inp)
     # heads and top-k: every sequence, every head
     z = O.head_hidden(n["h"], n["W1"], n["b1"])
