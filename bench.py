@@ -450,6 +450,10 @@ def run_medusa(args, world, rank, local):
     e2e_dt = reduce_max((time.perf_counter() - t0) / args.steps, world)
     assert res_host["accept_len"].tolist() == planted
 
+    loop = None
+    if s.name == DEFAULT_WORKLOAD and not args.no_loop:
+        loop = decode_loop_figures(args)
+
     line = {"metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
@@ -459,10 +463,46 @@ def run_medusa(args, world, rank, local):
             "e2e": {"value": round(world / e2e_dt, 2), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * M.step_launches(cfg), "clocks": clk.summary()}
+    if loop is not None:
+        line["decode_loop"] = loop
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(s, inp, budget_s=args.cpu_budget)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def decode_loop_figures(args, name: str = "toy-7b") -> dict:
+    """Rounds of decoding over the 7B-shaped table backbone (the stage calls
+    of the library, the commit of the kept branch and the next inputs, with
+    the backbone's table lookups between tree and attention), captured as one
+    CUDA graph of all rounds that starts by restoring the initial caches:
+    tokens per round and tokens per second."""
+    from medusa_head_tree_heads_b300 import decode_loop
+    t = synth.TOYS[name]
+    loop = decode_loop.DecodeLoop(t, synth.make_toy(t))
+    loop.run()  # warm-up (and the kernels' first-launch set-up)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        loop.reset()
+        loop.run()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = 5
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / reps
+    tokens = loop.tokens()
+    return {"workload": name, "rounds": t.rounds, "batch": t.batch, "tokens": tokens,
+            "tokens_per_round": round(tokens / (t.rounds * t.batch), 3),
+            "ms_per_round": round(sec / t.rounds * 1e3, 4), "tokens_per_s": round(tokens / sec, 1),
+            "launch": "one CUDA graph of all rounds (eager stage calls, no fused step)",
+            "heads": "synthetic, right per (head, token) with probability " + str(list(t.head_acc))}
 
 
 def main():
@@ -475,6 +515,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--no-loop", action="store_true", help="skip the multi-round decoding figures")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     args.warmup = max(args.warmup, 3)  # at least 3 warm-up steps, reported as run

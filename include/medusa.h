@@ -71,8 +71,21 @@ typedef enum { MEDUSA_F32 = 0, MEDUSA_BF16 = 1 } medusa_dtype_t;
  * node's choice is a draw from its distribution at the temperature (Gumbel-max
  * with counter-based noise, see medusa_verify_accept); a candidate equal to
  * its parent's draw is kept, so the accepted tokens follow the base model's
- * sampling distribution (bf16 only). */
-typedef enum { MEDUSA_ACCEPT_GREEDY = 0, MEDUSA_ACCEPT_TYPICAL = 1, MEDUSA_ACCEPT_SAMPLE = 2 } medusa_accept_t;
+ * sampling distribution (bf16 only).  This is rejection sampling against the
+ * base model over the tree's fixed candidates ("Tetes de decodage Medusa":
+ * exact rejection sampling keeps the base model's distribution): trying the
+ * children in rank order, each accepted with its probability renormalised
+ * over the tokens not yet rejected, and drawing the bonus from the rest, emits
+ * the same distribution; one draw per node decides all of it at once.
+ * TYPICAL_SAMPLE: typical acceptance whose bonus token is that draw at the
+ * last kept node instead of the top choice (bf16 only; not with vocabulary
+ * shards). */
+typedef enum {
+  MEDUSA_ACCEPT_GREEDY = 0,
+  MEDUSA_ACCEPT_TYPICAL = 1,
+  MEDUSA_ACCEPT_SAMPLE = 2,
+  MEDUSA_ACCEPT_TYPICAL_SAMPLE = 3
+} medusa_accept_t;
 /* Launch order of medusa_step (the results are the same bits either way).
  * SERIAL: heads, candidate tree, tree attention, verification, acceptance.
  * OVERLAP: the tree attention runs beside the head projection, on the SMs the
@@ -101,7 +114,7 @@ typedef struct {
   int32_t kv_capacity;             /* Lc >= L: cache rows allocated per sequence */
   int32_t dtype;                   /* medusa_dtype_t of weights/activations */
   int32_t accept_mode;             /* medusa_accept_t */
-  float temperature;               /* typical: softmax temperature (> 0) */
+  float temperature;               /* typical, sample: softmax temperature (> 0) */
   float eps;                       /* typical: threshold cap */
   float delta;                     /* typical: threshold scale, thr = min(eps, delta*exp(-H)) */
   /* Optional explicit candidate tree ("Medusa Heads", "Attenzione sull'albero
@@ -116,13 +129,21 @@ typedef struct {
   int32_t tree_nodes;
   const int32_t* tree_parent;
   const int32_t* tree_rank;
-  /* SAMPLE mode: the noise of vocabulary row v at node n = b*T + i is drawn
+  /* SAMPLE, TYPICAL_SAMPLE: the noise of vocabulary row v at node n = b*T + i is drawn
    * from Philox4x32-10 with key (sample_seed[0], sample_seed[1]) and counter
    * (v, n / 4, sample_step, 0), word n % 4; a new step needs a new
    * sample_step (or seed). */
   uint32_t sample_seed[2];
   int32_t sample_step;
   int32_t schedule; /* medusa_schedule_t, read by medusa_step and medusa_step_launches */
+  /* Vocabulary shard (medusa_shard_partial only; see there): this call's W2
+   * holds rows [vocab_begin, vocab_begin + vocab_rows) of every head, as
+   * [K][vocab_rows][H], and its lm_head the same rows, as [vocab_rows][H];
+   * token ids stay global (0 .. vocab - 1).  vocab_rows = 0: the whole
+   * vocabulary, which every other entry point requires (else
+   * MEDUSA_ERR_INVALID_ARG).  Needs max_d k_d <= vocab_rows. */
+  int32_t vocab_begin;
+  int32_t vocab_rows;
 } medusa_config_t;
 
 /* Candidate tree, device arrays allocated by the caller (sizes from
@@ -309,6 +330,48 @@ int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io,
  * current device (the kernels chosen depend on the shape and the SM count);
  * negative medusa_status_t on an invalid config.  Host-only. */
 int medusa_step_launches(const medusa_config_t* cfg);
+
+/* Vocabulary-sharded step over several GPUs (one process per GPU; arXiv
+ * 2401.10774, abstract: the step is memory-bound, so at batch 1 only a split
+ * of the weights lowers the bytes each GPU reads).  GPU s of G holds rows
+ * [vocab_begin, vocab_begin + vocab_rows) of every head projection and of
+ * lm_head (cfg->vocab_begin / cfg->vocab_rows; the shards tile 0 .. vocab-1
+ * in rank order).  A step is:
+ *   medusa_shard_partial   on every GPU, writes its record
+ *   (the caller)           all-gathers the records into one device buffer,
+ *                          rank order, records back to back
+ *   medusa_shard_finish    on every GPU, the same results as medusa_step
+ * The top-k lists over the whole vocabulary are the top-k of the union of
+ * the shards' lists; a node's argmax, maximum, log-partition and entropy
+ * combine exactly from per-shard states; a child's typical-acceptance score
+ * comes from the shard holding its token's row.  Host-only; 0 when the config
+ * names no shard (vocab_rows = 0) or is invalid. */
+size_t medusa_shard_record_bytes(const medusa_config_t* cfg);
+
+/* This GPU's part of the step: heads and per-head top-k over its rows,
+ * the sequence-independent tree arrays (parent, depth, rank, pos, mask,
+ * paths: written into io->tree), tree attention of every node (io->attn_out,
+ * replicated on every GPU; io->kv_lens as in medusa_step) and the
+ * verification over its rows.  record (device, medusa_shard_record_bytes,
+ * 16-byte aligned): int32 header {vocab_begin, vocab_rows, B*T, kmax}, the
+ * shard's top-k values and global ids [B][K][kmax], per node the state
+ * (max score, sum e, sum e*t, argmax id bits) with t = (score - max) /
+ * temperature (typical; e = exp t), and for typical acceptance the scores
+ * lm_head[id] . o_node of the shard's candidates of each node's child depth
+ * [B*T][kmax].  io->W2 is [K][vocab_rows][H], io->lm_head [vocab_rows][H]; the
+ * other inputs as in medusa_step; io's top-k, node and acceptance outputs are
+ * not written.  A config without a shard is MEDUSA_ERR_INVALID_ARG. */
+int medusa_shard_partial(const medusa_config_t* cfg, const medusa_step_io_t* io, void* record, void* workspace,
+                         void* stream);
+
+/* The combination: records = n_shards records back to back (device).  Writes
+ * io's top-k lists (global), the tree's tokens and arrays, node_argmax,
+ * node_maxlogit, (typical) node_lse / node_entropy and the acceptance
+ * outputs, identical on every GPU.  Records that do not tile the vocabulary
+ * in order set MEDUSA_ERR_DEVICE in the workspace error word.  Reads no
+ * weight. */
+int medusa_shard_finish(const medusa_config_t* cfg, const medusa_step_io_t* io, const void* records,
+                        int32_t n_shards, void* workspace, void* stream);
 
 /* Checks, on the current device, the bounded-wait path every kernel of the
  * library uses: one CTA waits on an mbarrier that nothing completes; after

@@ -22,8 +22,6 @@ int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* to
 int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                      cudaStream_t st);
 
-int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
-                       float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 int launch_verify(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
                   float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, const medusa_tree_t& t,
@@ -53,10 +51,12 @@ int make_plan(const medusa_config_t* c, Plan* p) {
     return MEDUSA_ERR_INVALID_ARG;
   if (c->dtype != MEDUSA_F32 && c->dtype != MEDUSA_BF16) return MEDUSA_ERR_INVALID_ARG;
   if (c->accept_mode != MEDUSA_ACCEPT_GREEDY && c->accept_mode != MEDUSA_ACCEPT_TYPICAL &&
-      c->accept_mode != MEDUSA_ACCEPT_SAMPLE)
+      c->accept_mode != MEDUSA_ACCEPT_SAMPLE && c->accept_mode != MEDUSA_ACCEPT_TYPICAL_SAMPLE)
     return MEDUSA_ERR_INVALID_ARG;
   if (c->accept_mode == MEDUSA_ACCEPT_SAMPLE && !(c->temperature > 0.f)) return MEDUSA_ERR_INVALID_ARG;
-  if (c->accept_mode == MEDUSA_ACCEPT_SAMPLE && c->dtype != MEDUSA_BF16) return MEDUSA_ERR_UNSUPPORTED;
+  if ((c->accept_mode == MEDUSA_ACCEPT_SAMPLE || c->accept_mode == MEDUSA_ACCEPT_TYPICAL_SAMPLE) &&
+      c->dtype != MEDUSA_BF16)
+    return MEDUSA_ERR_UNSUPPORTED;
   if (c->schedule != MEDUSA_SCHEDULE_AUTO && c->schedule != MEDUSA_SCHEDULE_SERIAL &&
       c->schedule != MEDUSA_SCHEDULE_OVERLAP)
     return MEDUSA_ERR_INVALID_ARG;
@@ -71,11 +71,18 @@ int make_plan(const medusa_config_t* c, Plan* p) {
     return MEDUSA_ERR_INVALID_ARG;
   if ((long long)c->n_heads * c->vocab > (1LL << 30) || (long long)c->n_heads * c->hidden > (1LL << 30))
     return MEDUSA_ERR_UNSUPPORTED;
-  if (c->accept_mode == MEDUSA_ACCEPT_TYPICAL && !(c->temperature > 0.f && c->eps > 0.f && c->delta >= 0.f))
+  if ((c->accept_mode == MEDUSA_ACCEPT_TYPICAL || c->accept_mode == MEDUSA_ACCEPT_TYPICAL_SAMPLE) &&
+      !(c->temperature > 0.f && c->eps > 0.f && c->delta >= 0.f))
+    return MEDUSA_ERR_INVALID_ARG;
+  if (c->vocab_rows < 0 || c->vocab_begin < 0 || (c->vocab_rows == 0 && c->vocab_begin != 0) ||
+      (long long)c->vocab_begin + c->vocab_rows > c->vocab)
     return MEDUSA_ERR_INVALID_ARG;
   p->B = c->batch;
   p->H = c->hidden;
   p->V = c->vocab;
+  p->Vs = c->vocab_rows ? c->vocab_rows : c->vocab;
+  p->v0 = c->vocab_begin;
+  p->sharded = c->vocab_rows > 0;
   p->K = c->n_heads;
   p->D = c->depth;
   p->Hq = c->n_q_heads;
@@ -85,8 +92,9 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   p->L = c->kv_len;
   p->Lc = c->kv_capacity;
   p->bf16 = c->dtype == MEDUSA_BF16;
-  p->typical = c->accept_mode == MEDUSA_ACCEPT_TYPICAL;
+  p->typical = c->accept_mode == MEDUSA_ACCEPT_TYPICAL || c->accept_mode == MEDUSA_ACCEPT_TYPICAL_SAMPLE;
   p->sample = c->accept_mode == MEDUSA_ACCEPT_SAMPLE;
+  p->sample_bonus = c->accept_mode == MEDUSA_ACCEPT_TYPICAL_SAMPLE;
   p->seed[0] = c->sample_seed[0];
   p->seed[1] = c->sample_seed[1];
   p->step = c->sample_step;
@@ -100,7 +108,7 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   p->kmax = 1;
   for (int d = 1; d <= p->D; ++d) {
     const int k = c->topk[d - 1];
-    if (k < 1 || k > MEDUSA_MAX_TOPK || k > p->V) return MEDUSA_ERR_UNSUPPORTED;
+    if (k < 1 || k > MEDUSA_MAX_TOPK || k > p->Vs) return MEDUSA_ERR_UNSUPPORTED;
     if (k > p->kmax) p->kmax = k;
   }
   int T = 0;
@@ -181,7 +189,7 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   p->off_vf_idx = o;
   o = align_up(o + n_vf * sizeof(int), 256);
   p->off_vtc_part = o;
-  if (p->bf16) o = align_up(o + verify_tc_part_bytes(p->V, p->B * p->T), 256);
+  if (p->bf16) o = align_up(o + verify_tc_part_bytes(p->Vs, p->B * p->T), 256);
   p->off_attn_part = o;
   if (p->bf16) o = align_up(o + attn_part_bytes(p->B, p->T, p->G, p->Hkv, p->L, p->Dh), 256);
   p->off_zs = p->off_ht_slot = p->off_ht_tickets = o;
@@ -195,6 +203,13 @@ int make_plan(const medusa_config_t* c, Plan* p) {
   }
   p->off_keep = o;
   o = align_up(o + (size_t)p->B * p->T, 256);
+  p->off_draw_part = p->off_draw = o;
+  if (p->sample_bonus) {
+    p->off_draw_part = o;
+    o = align_up(o + verify_tc_part_bytes(p->Vs, p->B * p->T) / 2, 256);  // float2 per (vocab tile, node)
+    p->off_draw = o;
+    o = align_up(o + (size_t)p->B * p->T * sizeof(int32_t), 256);
+  }
   p->total = o;
   return MEDUSA_OK;
 }
@@ -243,7 +258,7 @@ static bool pick_overlap(const Plan& p) {
   const long long ctas = attn_tc_unsplit_ctas(p);
   const int nb = (p.L + 63) / 64 + (p.T + 63) / 64;
   const double attn_us = (double)((ctas + free_sms - 1) / free_sms) * (15.0 + 1.3 * nb);
-  const double proj_us = (double)p.K * p.V * p.H * 2 / 6.0e6;
+  const double proj_us = (double)p.K * p.Vs * p.H * 2 / 6.0e6;
   return attn_us <= 0.5 * proj_us;
 }
 
@@ -283,7 +298,7 @@ int medusa_heads_topk(const medusa_config_t* cfg, const void* h, const void* W1,
   int s = make_plan(cfg, &p);
   if (s != MEDUSA_OK) return s;
   if (!aligned16(h) || !aligned16(W1) || !aligned16(b1) || !aligned16(W2) || !topk_idx || !topk_val ||
-      !aligned16(workspace))
+      !aligned16(workspace) || p.sharded)
     return MEDUSA_ERR_INVALID_ARG;
   finish_plan(&p);
   cudaStream_t st = (cudaStream_t)stream;
@@ -367,7 +382,7 @@ int medusa_verify_accept(const medusa_config_t* cfg, const void* attn_out, const
   int s = make_plan(cfg, &p);
   if (s != MEDUSA_OK) return s;
   if (!aligned16(attn_out) || !aligned16(lm_head) || !node_argmax || !node_maxlogit || !accept_len ||
-      !acc_tokens || !acc_nodes || !bonus || !aligned16(workspace))
+      !acc_tokens || !acc_nodes || !bonus || !aligned16(workspace) || p.sharded)
     return MEDUSA_ERR_INVALID_ARG;
   if (p.typical && (!node_lse || !node_entropy)) return MEDUSA_ERR_INVALID_ARG;
   if ((s = check_tree(p, tree)) != MEDUSA_OK) return s;
@@ -393,7 +408,7 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
       !aligned16(io->lm_head) || !io->root_token || !aligned16(io->q) || !aligned16(io->k_tree) ||
       !aligned16(io->v_tree) || !io->topk_idx || !io->topk_val || !aligned16(io->attn_out) || !io->node_argmax ||
       !io->node_maxlogit || !io->accept_len || !io->acc_tokens || !io->acc_nodes || !io->bonus ||
-      !aligned16(workspace))
+      !aligned16(workspace) || p.sharded)
     return MEDUSA_ERR_INVALID_ARG;
   if ((p.L > 0 || (io->kv_lens && p.Lc > 0)) && (!aligned16(io->k_cache) || !aligned16(io->v_cache)))
     return MEDUSA_ERR_INVALID_ARG;
@@ -483,6 +498,7 @@ int medusa_step_launches(const medusa_config_t* cfg) {
   Plan p;
   int s = make_plan(cfg, &p);
   if (s != MEDUSA_OK) return s;
+  if (p.sharded) return MEDUSA_ERR_INVALID_ARG;
   finish_plan(&p);
   p.overlap = pick_overlap(p);
   int n = 6;                        // one launch per stage

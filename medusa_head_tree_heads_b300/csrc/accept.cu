@@ -19,8 +19,6 @@
 
 namespace medusa {
 
-int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
-                       float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st);
 
 struct AcceptArgs {
   int B, T, D, NL, V, H;
@@ -35,6 +33,7 @@ struct AcceptArgs {
   const float* node_lse;
   const float* node_entropy;
   const uint8_t* child_keep;  // typical keep flags from the verification merge, or null (computed here)
+  const int32_t* bonus_src;   // [B][T] the token the bonus takes at the last kept node (node_argmax, or a draw)
   int32_t *accept_len, *acc_tokens, *acc_nodes, *bonus;
   uint8_t* ws;
 };
@@ -116,7 +115,7 @@ __global__ void __launch_bounds__(256) accept_kernel(AcceptArgs a) {
   }
   if (threadIdx.x == 0) {
     a.accept_len[b] = n;
-    a.bonus[b] = a.node_argmax[(size_t)b * a.T + path[n]];
+    a.bonus[b] = a.bonus_src[(size_t)b * a.T + path[n]];
   }
 }
 
@@ -142,7 +141,8 @@ int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, cons
   a.node_argmax = node_argmax;
   a.node_lse = node_lse;
   a.node_entropy = node_entropy;
-  a.child_keep = p.typical && p.bf16 ? ws + p.off_keep : nullptr;
+  a.child_keep = p.typical && (p.bf16 || p.sharded) ? ws + p.off_keep : nullptr;
+  a.bonus_src = p.sample_bonus ? reinterpret_cast<const int32_t*>(ws + p.off_draw) : node_argmax;
   a.accept_len = accept_len;
   a.acc_tokens = acc_tokens;
   a.acc_nodes = acc_nodes;

@@ -67,8 +67,11 @@ struct AtArgs {
   int Lc;
   // overlap schedule of the fused step: launched right after the head
   // projection, whose kernel lets it start only after everything before the
-  // step has completed, so no store waits and the CTAs retire freely
+  // step has completed, so no store waits and the CTAs retire freely; each
+  // CTA counts itself into *done_count once its outputs are written (the
+  // verification projection waits for that count, not for this grid)
   int nowait;
+  int* done_count;
 };
 
 __device__ __forceinline__ uint32_t at_sw(int r, int unit) {  // byte offset of 16-byte unit `unit` of row r
@@ -482,8 +485,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  if (a.done_count) __threadfence();  // this thread's outputs, before the count below
   tc::fence_before_sync();
   __syncthreads();
+  if (a.done_count && threadIdx.x == 0) atomicAdd(a.done_count, 1);
   if (warp == 2) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, AT_TMEM_COLS);
@@ -579,6 +584,7 @@ int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void
   // leaves free: no key splits (and no combine launch)
   a.NS = p.overlap ? 1 : attn_tc_splits(p.B, p.T, p.G, p.Hkv, p.L);
   a.nowait = p.overlap ? 1 : 0;
+  a.done_count = p.overlap ? reinterpret_cast<int*>(ws) + TICKET_ATTN_DONE : nullptr;
   const size_t rows_all = (size_t)p.B * p.Hq * p.T * a.NS;
   a.part_o = reinterpret_cast<float*>(ws + p.off_attn_part);
   a.part_ml = reinterpret_cast<float2*>(ws + p.off_attn_part + rows_all * p.Dh * sizeof(float));

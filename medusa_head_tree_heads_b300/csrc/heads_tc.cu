@@ -58,6 +58,7 @@ struct HtArgs {
   __nv_bfloat16* zs;        // [K][NZ][H]: row 2b = z_hi of sequence b, 2b+1 = z_lo
   int NZ;
   // projection
+  int id_off;  // token id of local row 0 (a vocabulary shard's first row)
   int kmax;
   int topk_n[MEDUSA_MAX_HEADS];
   float* cand_val;  // [grid][kMaxPieces][B][kmax]
@@ -74,6 +75,7 @@ struct HtArgs {
   // of its preceding grid); the layer clears the count
   int late_trigger;
   int* proj_done;
+  int* attn_done;  // layer: the tree attention's completion count, cleared with proj_done
   uint8_t* ws;
 };
 
@@ -332,7 +334,10 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
     // its tickets are reset for its next launch
     for (int i = blockIdx.x * (32 * HT_EPI_WARPS) + etid; i < kHeadsTcMaxCtas; i += gridDim.x * 32 * HT_EPI_WARPS)
       a.tk_other[i] = 0;
-    if (EPI == 0 && blockIdx.x == 0 && etid == 0) *a.proj_done = 0;  // the previous step has completed
+    if (EPI == 0 && blockIdx.x == 0 && etid == 0) {  // the previous step has completed
+      *a.proj_done = 0;
+      *a.attn_done = 0;
+    }
     float lv[KM];
     int li[KM];
     ht_reset<KM>(lv, li, KM);
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
         for (int b = 0; b < N / 2; ++b) {
           if (b >= a.B) break;
           const float v = valid ? acc[2 * b] + acc[2 * b + 1] : -INFINITY;
-          const int r = valid ? row : INT_MAX;
+          const int r = valid ? a.id_off + row : INT_MAX;
           float tv = __shfl_sync(0xffffffffu, lv[KM - 1], b);
           int ti = __shfl_sync(0xffffffffu, li[KM - 1], b);
           unsigned pass = __ballot_sync(0xffffffffu, valid && better(v, r, tv, ti));
@@ -432,7 +437,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
             const unsigned top = __ballot_sync(0xffffffffu, in && key == kmx);
             const int w = __ffs(top) - 1;  // lowest lane = lowest row among equal values
             const float wv = __shfl_sync(0xffffffffu, v, w);
-            if (lane == b) ht_insert<KM>(lv, li, wv, row0 + w);
+            if (lane == b) ht_insert<KM>(lv, li, wv, a.id_off + row0 + w);
             pass &= ~(1u << w);
             tv = __shfl_sync(0xffffffffu, lv[KM - 1], b);
             ti = __shfl_sync(0xffffffffu, li[KM - 1], b);
@@ -489,7 +494,7 @@ static void ht_partition(const Plan& p, int rows, HtArgs* a, int* grid) {
 int heads_tc_proj_grid(const Plan& p) {
   HtArgs a{};
   int grid = 0;
-  ht_partition(p, p.V, &a, &grid);
+  ht_partition(p, p.Vs, &a, &grid);
   return grid;
 }
 
@@ -530,6 +535,7 @@ int launch_fc_tc(const Plan& p, const void* h, const void* W1, const void* b1, u
   a.tk_own = reinterpret_cast<int*>(ws + p.off_ht_tickets);
   a.tk_other = a.tk_own + kHeadsTcMaxCtas;
   a.proj_done = reinterpret_cast<int*>(ws) + TICKET_PROJ_DONE;
+  a.attn_done = reinterpret_cast<int*>(ws) + TICKET_ATTN_DONE;
   int grid = 0;
   ht_partition(p, p.H, &a, &grid);
   if (a.upc > a.tps * a.nks) return (int)cudaErrorInvalidConfiguration;  // a CTA must touch at most 2 heads
@@ -549,7 +555,8 @@ int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t
                         int* ups) {
   HtArgs a{};
   ht_common(p, ws, &a);
-  a.rows = p.V;
+  a.rows = p.Vs;
+  a.id_off = p.v0;
   a.kmax = p.kmax;
   for (int k = 0; k < MEDUSA_MAX_HEADS; ++k) a.topk_n[k] = p.topk_n[k];
   a.cand_val = reinterpret_cast<float*>(ws + p.off_cand_val);
@@ -562,14 +569,14 @@ int launch_proj_tc_only(const Plan& p, const void* W2, uint8_t* ws, cudaStream_t
     a.proj_done = reinterpret_cast<int*>(ws) + TICKET_PROJ_DONE;
   }
   int grid = 0;
-  ht_partition(p, p.V, &a, &grid);
+  ht_partition(p, p.Vs, &a, &grid);
   if (a.upc > a.tps * a.nks) return (int)cudaErrorInvalidConfiguration;  // a CTA must touch at most 2 heads
   *ctas = grid;
   *upc = a.upc;
   *ups = a.tps * a.nks;
   const int n = ht_n_proj(p.B);
   CUtensorMap tA, tB;
-  int e = make_tmap_bf16_3d(&tA, W2, p.K, p.V, p.H, HT_M);
+  int e = make_tmap_bf16_3d(&tA, W2, p.K, p.Vs, p.H, HT_M);
   if (e) return e;
   e = make_tmap_bf16(&tB, a.zs, p.K * n, p.H, n);
   if (e) return e;

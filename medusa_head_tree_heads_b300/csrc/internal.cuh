@@ -21,7 +21,8 @@ constexpr int kHeadsTcMaxBatch = 32;  // largest batch of the tensor-core heads 
 // ---------------------------------------------------------------- workspace --
 // [0, 256): int32 error word at 0, tickets from word 8 on.
 enum Ticket { TICKET_FC = 8, TICKET_PROJ = 9, TICKET_VERIFY = 10,
-              TICKET_PROJ_DONE = 11 };  // overlap schedule: projection CTAs finished this step
+              TICKET_PROJ_DONE = 11,    // medusa_step: projection CTAs finished this step
+              TICKET_ATTN_DONE = 12 };  // overlap schedule: tree attention CTAs finished this step
 
 // The candidate tree as tables, filled on the host for the Cartesian tree of
 // the per-depth list sizes or for a caller's explicit tree.  Nodes are in
@@ -40,7 +41,9 @@ struct TreeDims {
 struct Plan {
   // sizes
   int B, H, V, K, D, kmax, T, NL, W, Hq, Hkv, G, Dh, L, Lc;
+  int Vs, v0;  // vocabulary rows this call holds (W2 per head, lm_head) and the id of its first row
   bool bf16, typical, sample;
+  bool sample_bonus;  // typical acceptance whose bonus is a draw (MEDUSA_ACCEPT_TYPICAL_SAMPLE)
   float temperature, eps, delta;
   uint32_t seed[2];
   int step;
@@ -52,11 +55,13 @@ struct Plan {
   int schedule;    // medusa_schedule_t as given
   bool overlap;    // medusa_step only: tree attention beside the head projection
   bool late_tree;  // medusa_step only: candidate merge + tree beside the verification projection
+  bool sharded;    // the config names a vocabulary shard (vocab_rows > 0)
   int fc_nc, fc_ctiles, pj_nc, pj_ctiles, vf_nc, vf_ctiles;  // columns per CTA, column tiles
   // workspace offsets (bytes)
   size_t off_z, off_cand_val, off_cand_idx, off_cand_seg, off_vf_part, off_vf_idx, off_vtc_part, off_attn_part;
   size_t off_zs, off_ht_slot, off_ht_tickets;  // tensor-core heads: z pairs, cut-tile partials, tickets
   size_t off_keep;  // [B][T] uint8 typical-acceptance keep flags written by the verification merge
+  size_t off_draw_part, off_draw;  // typical with a sampled bonus: per-tile draws [n_vt][B*T] float2, draws [B*T]
   size_t total;
 };
 
@@ -76,14 +81,37 @@ int launch_proj_tc(const Plan& p, const void* W2, int32_t* topk_idx, float* topk
 size_t attn_part_bytes(int B, int T, int G, int Hkv, int L, int Dh);
 void attn_split_shape(int B, int T, int G, int Hkv, int L, int* NS, int* chunk_blks);
 // the verification's two launches: the projection (partials per vocabulary
-// tile) and the merge of the partials (node results, typical keep flags)
-enum VerifyPart { VERIFY_BOTH = 0, VERIFY_GEMM = 1, VERIFY_MERGE = 2 };
+// tile) and the merge of the partials (node results, typical keep flags; or,
+// for a vocabulary shard, the merged state per node into shard_out)
+enum VerifyPart { VERIFY_BOTH = 0, VERIFY_GEMM = 1, VERIFY_MERGE = 2, VERIFY_SHARD = 3 };
 int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
                      float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st,
-                     VerifyPart part = VERIFY_BOTH);
+                     VerifyPart part = VERIFY_BOTH, float4* shard_out = nullptr);
 int launch_merge_tree(const Plan& p, int32_t* topk_idx, float* topk_val, const int32_t* root,
                       const medusa_tree_t& t, uint8_t* ws, int nctas, int rpc, int S, bool count_wait,
                       cudaStream_t st);
+
+// fp32 (or bf16 beyond the tensor-core kernels) verification on the CUDA
+// cores; with soft_out the merged state per node goes there instead of the
+// node results (a vocabulary shard)
+int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
+                       float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st,
+                       float4* soft_out = nullptr);
+
+// Exchange record of one vocabulary shard (medusa_shard_partial writes it,
+// medusa_shard_finish reads n of them back to back); offsets in bytes, every
+// section 16-byte aligned:
+//   0         int32 header {vocab_begin, vocab_rows, B*T, kmax}
+//   off_val   float [B][K][kmax]  the shard's per-head top-k values (-inf pad)
+//   off_idx   int32 [B][K][kmax]  their global token ids (-1 pad)
+//   off_node  float4 [B*T]        per node: max score, sum e, sum e*t (typical),
+//                                 argmax id bits (see shard_node_states)
+//   off_cdot  float [B*T][kmax]   typical only: lm_head[idx] . o_node for the
+//                                 shard's candidates of the node's child depth
+struct ShardRecord {
+  size_t off_val, off_idx, off_node, off_cdot, bytes;
+};
+ShardRecord shard_record_layout(const Plan& p);
 
 // launchers (enqueue only; return cudaError_t as int)
 int launch_heads(const Plan& p, const void* h, const void* W1, const void* b1, const void* W2, int32_t* topk_idx,
@@ -196,6 +224,10 @@ __device__ __forceinline__ void wait_count(const int* count, int target, uint64_
     }
   }
 }
+
+// Makes the data an acquire (wait_count) has seen visible to the reads of the
+// async proxy (TMA loads) that follow in this thread.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // float -> int with the same order (negative floats have their magnitude bits flipped)
 __device__ __forceinline__ int order_key(float x) {

@@ -98,7 +98,8 @@ extern "C" int medusa_heads_topk_noalloc(const medusa_config_t* cfg, const void*
   Plan p;
   int s = make_plan(cfg, &p);
   if (s != MEDUSA_OK) return s;
-  if (!al16(h) || !al16(W1) || !al16(b1) || !al16(W2) || !topk_idx || !topk_val) return MEDUSA_ERR_INVALID_ARG;
+  if (!al16(h) || !al16(W1) || !al16(b1) || !al16(W2) || !topk_idx || !topk_val || p.sharded)
+    return MEDUSA_ERR_INVALID_ARG;
   const bool tc = heads_tc_supported(p);
   if (heads_only_layout(&p) > kNoAllocScratchBytes) return MEDUSA_ERR_UNSUPPORTED;
   uint8_t* ws = nullptr;

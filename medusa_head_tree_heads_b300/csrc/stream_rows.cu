@@ -59,6 +59,8 @@ struct RowArgs {
   float* node_maxlogit;
   float* node_lse;
   float* node_entropy;
+  float4* soft_out;  // a vocabulary shard: the merged state (max, sum e, sum e*t, argmax bits) per column instead
+  int id_off;        // EPI_TOPK / EPI_VERIFY: token id of local row 0
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -297,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 2) stream_rows_kernel(RowArgs a) {
           } else if (EPI == EPI_TOPK) {
             rowbuf[c * kRowBuf + (r - r0)] = acc[c];
           } else {
-            soft_push(soft, acc[c], j, typical, a.inv_temp);
+            soft_push(soft, acc[c], a.id_off + j, typical, a.inv_temp);
           }
         }
       }
@@ -311,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 2) stream_rows_kernel(RowArgs a) {
         float lv[KMAX];
         int li[KMAX];
         list_reset(lv, li);
-        for (int e = lane; e < r1 - r0; e += 32) list_insert(lv, li, kn, rowbuf[c * kRowBuf + e], r0 + e - seg * a.S);
+        for (int e = lane; e < r1 - r0; e += 32)
+          list_insert(lv, li, kn, rowbuf[c * kRowBuf + e], a.id_off + r0 + e - seg * a.S);
         const size_t base = ((size_t)(cta * kMaxPieces + piece) * a.C + (c0 + c)) * a.kmax;
         warp_select(lv, li, kn, a.kmax, a.cand_val + base, a.cand_idx + base, INT_MAX);
       }
@@ -374,7 +377,9 @@ __global__ void __launch_bounds__(kThreads, 2) stream_rows_kernel(RowArgs a) {
         t.mi = __shfl_xor_sync(0xffffffffu, m.mi, o);
         m = soft_merge(m, t, typical, a.inv_temp);
       }
-      if (lane == 0) {
+      if (lane == 0 && a.soft_out) {
+        a.soft_out[c] = make_float4(m.m, m.z, m.s, __int_as_float(m.mi));
+      } else if (lane == 0) {
         a.node_argmax[c] = m.mi;
         a.node_maxlogit[c] = m.m;
         if (typical) {
@@ -516,8 +521,9 @@ int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* to
   a.x = ws + p.off_z;
   a.x_cs = (long long)p.K * p.H;
   a.x_ss = p.H;
-  a.R = p.K * p.V;
-  a.S = p.V;
+  a.R = p.K * p.Vs;
+  a.S = p.Vs;
+  a.id_off = p.v0;
   a.H = p.H;
   a.C = p.B;
   a.nseg = p.K;
@@ -535,14 +541,17 @@ int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* to
 }
 
 int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
-                       float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st) {
+                       float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st,
+                       float4* soft_out) {
   RowArgs a{};
   a.W = lm_head;
   a.x = attn_out;
   a.x_cs = p.H;
   a.x_ss = 0;
-  a.R = p.V;
-  a.S = p.V;
+  a.R = p.Vs;
+  a.S = p.Vs;
+  a.id_off = p.v0;
+  a.soft_out = soft_out;
   a.H = p.H;
   a.C = p.B * p.T;
   a.nseg = 1;

@@ -51,8 +51,8 @@ __global__ void tree_build_kernel(const __grid_constant__ TreeArgs a) {
   const int gid = blockIdx.x * blockDim.x + threadIdx.x;
   const int T = td.T;
   pdl_trigger();
-  if (gid < a.B * T) {
-    pdl_wait();  // the top-k lists come from the previous kernel
+  pdl_wait();  // the top-k lists come from the previous kernel, which may also still read the tree
+  if (gid < a.B * T && a.topk_idx) {  // (no lists: the sequence-independent arrays only)
     const int b = gid / T, i = gid - b * T;
     const int d = td.depth[i];
     const int tok = d == 0 ? a.root[b] : a.topk_idx[((size_t)b * a.K + (d - 1)) * a.kmax + td.rank[i]];

@@ -49,7 +49,14 @@ constexpr uint32_t VT_TMEM_COLS = 512;
 constexpr uint64_t VT_WAIT_NS = 20ull * 1000 * 1000;  // 20 ms per wait
 
 struct VtcArgs {
-  int V, N, H, BN, n_vt, n_nt, n_tiles, nk, stages;
+  int V, N, H, BN, n_vt, n_nt, n_tiles, nk, stages;  // V: lm_head rows this call holds
+  int id_off;  // token id of lm_head row 0 (a vocabulary shard's first row)
+  // overlap schedule of the fused step: the node operand is complete once
+  // *node_ready reaches node_target (the tree attention's CTAs count
+  // themselves); the producer waits for that instead of the preceding grid,
+  // which cannot complete before the head projection it runs beside
+  const int* node_ready;
+  int node_target;
   uint32_t idesc;
   int typical;
   int sample;  // node choice = argmax of s / temperature + Gumbel noise
@@ -71,6 +78,12 @@ struct VtcArgs {
   const __nv_bfloat16* lm_head;     // [V][H]
   uint8_t* keep;                    // [B][T]
   float log_eps, log_delta;
+  float4* shard_out;  // a vocabulary shard: the merged state per node (max, sum e, sum e*t, argmax bits)
+  // typical acceptance with a sampled bonus (MODE 3): per (vocab tile, node)
+  // the best perturbed score s / temperature + g and its id, merged into
+  // draw[node]
+  float2* draw_part;  // [n_vt][N]
+  int32_t* draw;      // [N]
 };
 
 struct Soft {
@@ -156,8 +169,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return true;
 }
 
-// MODE: 0 greedy, 1 typical, 2 sample (a compile-time choice, so each
-// instance carries only its own epilogue)
+// MODE: 0 greedy, 1 typical, 2 sample, 3 typical with a sampled bonus (a
+// compile-time choice, so each instance carries only its own epilogue)
 template <int MODE>
 __global__ void __launch_bounds__(VT_THREADS, 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -168,7 +181,8 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
   const uint32_t bytesA1 = VT_M * VT_BK * 2, bytesA = VT_SUB * bytesA1, bytesB = (uint32_t)a.BN * VT_BK * 2;
   const uint32_t stage_bytes = bytesA + bytesB;
   Soft* red = reinterpret_cast<Soft*>(smem + (size_t)S * stage_bytes);  // [4][BN]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 4 * a.BN);
+  float2* red2 = reinterpret_cast<float2*>(red + 4 * a.BN);               // MODE 3: [4][BN] draws
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red2 + (MODE == 3 ? 4 * a.BN : 0));
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -179,7 +193,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
   volatile int* ep_ok = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr bool typical = MODE == 1;
+  constexpr bool typical = MODE == 1 || MODE == 3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -221,7 +235,12 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
         for (int h = 0; h < VT_SUB; ++h)
           tc::tma_load_2d(sa + h * bytesA1, &tmA, &full[kb], kb * VT_BK, (vt * VT_SUB + h) * VT_M);
       }
-      pdl_wait();  // the node operand is the previous kernel's output
+      if (a.node_ready) {  // the node operand: every attention CTA has counted itself
+        wait_count(a.node_ready, a.node_target, VT_WAIT_NS, a.ws);
+        fence_proxy_async_global();
+      } else {
+        pdl_wait();  // the node operand is the previous kernel's output
+      }
       for (int t = blockIdx.x; t < a.n_tiles && ok; t += gridDim.x) {
         const int vt = t / a.n_nt, nt = t - vt * a.n_nt;
         for (int kb = 0; kb < a.nk; ++kb, ++g) {
@@ -328,15 +347,44 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
             float zs[16], ss[16];
             float my_m = -INFINITY;
             int my_i = INT_MAX;
+            float dr_m = -INFINITY;  // MODE 3: this lane's column (lane < 16) of the draw
+            int dr_i = INT_MAX;
+            uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float x0 = ok0 ? v[0][j] : -INFINITY;
               const float x1 = ok1 ? v[1][j] : -INFINITY;
+              if constexpr (MODE == 3) {
+                // the bonus draw: s / temperature + Gumbel noise, keyed as in the
+                // sampling mode (one Philox call per row and 4 node columns)
+                if ((j & 3) == 0) {
+                  const uint32_t nc = (uint32_t)(nt * a.BN + (ch0 + c) * 16 + j) >> 2;
+                  w0 = philox4x32_10(make_uint4((uint32_t)(a.id_off + row0), nc, (uint32_t)a.step, 0u), a.seed0,
+                                     a.seed1);
+                  w1 = philox4x32_10(make_uint4((uint32_t)(a.id_off + row0 + VT_M), nc, (uint32_t)a.step, 0u),
+                                     a.seed0, a.seed1);
+                }
+                const uint32_t u0 = (j & 3) == 0 ? w0.x : (j & 3) == 1 ? w0.y : (j & 3) == 2 ? w0.z : w0.w;
+                const uint32_t u1 = (j & 3) == 0 ? w1.x : (j & 3) == 1 ? w1.y : (j & 3) == 2 ? w1.z : w1.w;
+                const float y0 = ok0 ? x0 * a.inv_temp + gumbel24(u0) : -INFINITY;
+                const float y1 = ok1 ? x1 * a.inv_temp + gumbel24(u1) : -INFINITY;
+                const bool one_d = y1 > y0;
+                const int dkey = order_key(one_d ? y1 : y0);
+                int dmax;
+                asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(dmax) : "r"(dkey));
+                const uint32_t dr = ok0 ? (uint32_t)(a.id_off + (one_d ? row0 + VT_M : row0)) : 0xffffffffu;
+                uint32_t drmin;
+                asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(drmin) : "r"(dkey == dmax ? dr : 0xffffffffu));
+                if (lane == j && drmin != 0xffffffffu) {
+                  dr_m = order_key_inv(dmax);
+                  dr_i = (int)drmin;
+                }
+              }
               const bool one = x1 > x0;  // equal values keep half 0 (the lower row)
               const int key = order_key(one ? x1 : x0);
               int kmax;
               asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(kmax) : "r"(key));
-              const uint32_t r = ok0 ? (uint32_t)(one ? row0 + VT_M : row0) : 0xffffffffu;
+              const uint32_t r = ok0 ? (uint32_t)(a.id_off + (one ? row0 + VT_M : row0)) : 0xffffffffu;
               uint32_t rmin;
               asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(rmin) : "r"(key == kmax ? r : 0xffffffffu));
               const float mj = order_key_inv(kmax);
@@ -375,6 +423,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
               o.s = my_i == INT_MAX ? 0.f : ss[0];
               red[q * a.BN + (ch0 + c) * 16 + (lane >> 1)] = o;
             }
+            if (MODE == 3 && lane < 16) red2[q * a.BN + (ch0 + c) * 16 + lane] = make_float2(dr_m, __int_as_float(dr_i));
           }
         } else {
           // greedy: per column, the best of this thread's two rows, then a
@@ -411,7 +460,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
                 const uint32_t n0 = (uint32_t)(nt * a.BN + (ch0 + cp + c) * 16);
 #pragma unroll
                 for (int h = 0; h < VT_SUB; ++h) {
-                  const uint32_t row = (uint32_t)(row0 + h * VT_M);
+                  const uint32_t row = (uint32_t)(a.id_off + row0 + h * VT_M);  // the global token id
 #pragma unroll
                   for (int j4 = 0; j4 < 16; j4 += 4) {
                     const uint4 w = philox4x32_10(make_uint4(row, (n0 + j4) >> 2, (uint32_t)a.step, 0u), a.seed0,
@@ -429,7 +478,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
                 const float x1 = ok1 ? v[1][c][j] : -INFINITY;
                 const bool one = x1 > x0;  // equal values keep half 0 (the lower row)
                 const float x = one ? x1 : x0;
-                const uint32_t r = ok0 ? (uint32_t)(one ? row0 + VT_M : row0) : 0xffffffffu;
+                const uint32_t r = ok0 ? (uint32_t)(a.id_off + (one ? row0 + VT_M : row0)) : 0xffffffffu;
                 const int key = order_key(x);
                 int kmax;
                 asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(kmax) : "r"(key));
@@ -458,6 +507,14 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
           Soft m = red[col];
           for (int w = 1; w < 4; ++w) m = soft_join(m, red[w * a.BN + col], typical, a.inv_temp);
           a.part[(size_t)vt * a.N + n] = make_float4(m.m, m.z, m.s, __int_as_float(m.i));
+          if constexpr (MODE == 3) {  // the draw: the larger perturbed score, ties to the lower id
+            float2 d = red2[col];
+            for (int w = 1; w < 4; ++w) {
+              const float2 o = red2[w * a.BN + col];
+              if (better(o.x, __float_as_int(o.y), d.x, __float_as_int(d.y))) d = o;
+            }
+            a.draw_part[(size_t)vt * a.N + n] = d;
+          }
         }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -503,6 +560,31 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const __grid_constant
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = soft_join(m, shfl_soft(m, o), TYPICAL, a.inv_temp);
+  if (a.shard_out) {  // the state itself: shards are combined after their exchange
+    if (lane == 0) a.shard_out[n] = make_float4(m.m, m.z, m.s, __int_as_float(m.i));
+    return;
+  }
+  if (TYPICAL && a.draw_part) {  // the bonus draw of this node: best perturbed score over the vocab tiles
+    float dm = -INFINITY;
+    int di = INT_MAX;
+    for (int vt = lane; vt < a.n_vt; vt += 32) {
+      const float2 d = a.draw_part[(size_t)vt * a.N + n];
+      if (better(d.x, __float_as_int(d.y), dm, di)) {
+        dm = d.x;
+        di = __float_as_int(d.y);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, dm, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, di, o);
+      if (better(om, oi, dm, di)) {
+        dm = om;
+        di = oi;
+      }
+    }
+    if (lane == 0) a.draw[n] = di;
+  }
   const float lz = logf(m.z);
   const float lse = m.m * a.inv_temp + lz, ent = lz - m.s / m.z;
   if (lane == 0) {
@@ -626,13 +708,14 @@ size_t verify_tc_part_bytes(int V, int N) {
 
 int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, const int32_t* token, int32_t* node_argmax,
                      float* node_maxlogit, float* node_lse, float* node_entropy, uint8_t* ws, cudaStream_t st,
-                     VerifyPart part) {
+                     VerifyPart part, float4* shard_out) {
   VtcArgs a;
-  a.V = p.V;
+  a.V = p.Vs;
+  a.id_off = p.v0;
   a.N = p.B * p.T;
   a.H = p.H;
   verify_tc_shape(a.N, &a.BN, &a.n_nt);
-  a.n_vt = (p.V + VT_SUB * VT_M - 1) / (VT_SUB * VT_M);
+  a.n_vt = (p.Vs + VT_SUB * VT_M - 1) / (VT_SUB * VT_M);
   a.n_tiles = a.n_vt * a.n_nt;
   a.nk = p.H / VT_BK;
   a.idesc = tc::idesc_bf16_f32(VT_M, a.BN);
@@ -643,6 +726,8 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, c
   a.step = p.step;
   a.inv_temp = (p.typical || p.sample) ? 1.f / p.temperature : 1.f;
   a.part = reinterpret_cast<float4*>(ws + p.off_vtc_part);
+  a.node_ready = p.overlap ? reinterpret_cast<const int*>(ws) + TICKET_ATTN_DONE : nullptr;
+  a.node_target = p.overlap ? (int)attn_tc_unsplit_ctas(p) : 0;
   a.node_argmax = node_argmax;
   a.node_maxlogit = node_maxlogit;
   a.node_lse = node_lse;
@@ -654,15 +739,18 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, c
   a.attn_out = reinterpret_cast<const __nv_bfloat16*>(attn_out);
   a.lm_head = reinterpret_cast<const __nv_bfloat16*>(lm_head);
   a.keep = ws + p.off_keep;
+  a.shard_out = part == VERIFY_SHARD ? shard_out : nullptr;
+  a.draw_part = p.sample_bonus ? reinterpret_cast<float2*>(ws + p.off_draw_part) : nullptr;
+  a.draw = p.sample_bonus ? reinterpret_cast<int32_t*>(ws + p.off_draw) : nullptr;
   a.log_eps = p.typical ? logf(p.eps) : 0.f;
   a.log_delta = p.typical && p.delta > 0.f ? logf(p.delta) : -INFINITY;
   const unsigned mgrid = (unsigned)((a.N + 7) / 8);
-  if (part == VERIFY_MERGE) {
+  if (part == VERIFY_MERGE || part == VERIFY_SHARD) {
     if (a.typical) return (int)launch_k(verify_merge_kernel<true>, dim3(mgrid), dim3(256), 0, st, true, a);
     return (int)launch_k(verify_merge_kernel<false>, dim3(mgrid), dim3(256), 0, st, true, a);
   }
   const size_t stage = (size_t)(VT_SUB * VT_M + a.BN) * VT_BK * 2;
-  const size_t fixed = 1024 + (size_t)4 * a.BN * sizeof(Soft) + 256;
+  const size_t fixed = 1024 + (size_t)4 * a.BN * (sizeof(Soft) + (p.sample_bonus ? sizeof(float2) : 0)) + 256;
   const size_t budget = 227 * 1024;
   int S = (int)((budget - fixed) / stage);
   if (S > 8) S = 8;
@@ -670,12 +758,13 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, c
   a.stages = S;
   const size_t smem = fixed + (size_t)S * stage;
   CUtensorMap tA, tB;
-  int e = make_tmap_bf16(&tA, lm_head, p.V, p.H, VT_M);
+  int e = make_tmap_bf16(&tA, lm_head, p.Vs, p.H, VT_M);
   if (e) return e;
   e = make_tmap_bf16(&tB, attn_out, a.N, p.H, a.BN);
   if (e) return e;
   void (*kern)(CUtensorMap, CUtensorMap, VtcArgs) =
-      a.typical ? verify_tc_kernel<1> : (a.sample ? verify_tc_kernel<2> : verify_tc_kernel<0>);
+      p.sample_bonus ? verify_tc_kernel<3>
+                     : (a.typical ? verify_tc_kernel<1> : (a.sample ? verify_tc_kernel<2> : verify_tc_kernel<0>));
   cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.n_tiles < p.sm_count ? a.n_tiles : p.sm_count;

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libmedusa.so")
 
 MAX_DEPTH = 8
 F32, BF16 = 0, 1
-GREEDY, TYPICAL, SAMPLE = 0, 1, 2
+GREEDY, TYPICAL, SAMPLE, TYPICAL_SAMPLE = 0, 1, 2, 3
 AUTO, SERIAL, OVERLAP = 0, 1, 2  # medusa_schedule_t
 STATUS = {0: "MEDUSA_OK", -1: "MEDUSA_ERR_INVALID_ARG", -2: "MEDUSA_ERR_UNSUPPORTED", -3: "MEDUSA_ERR_CUDA",
           -4: "MEDUSA_ERR_TIMEOUT", -5: "MEDUSA_ERR_DEVICE"}
@@ -28,7 +28,7 @@ EXPORTS = ("medusa_workspace_bytes", "medusa_tree_size", "medusa_heads_topk", "m
            "medusa_tree_attn", "medusa_verify_accept", "medusa_step", "medusa_step_profiled",
            "medusa_step_launches", "medusa_get_device_error", "medusa_status_string",
            "medusa_heads_topk_noalloc", "medusa_check_bounded_wait", "medusa_tree_attn_lens", "medusa_kv_commit",
-           "medusa_next_inputs")
+           "medusa_next_inputs", "medusa_shard_record_bytes", "medusa_shard_partial", "medusa_shard_finish")
 STEP_KERNELS = ("head_layer", "head_proj_topk", "tree_build", "tree_attn", "verify_proj", "accept")
 
 
@@ -47,7 +47,7 @@ class Config(ctypes.Structure):
                 ("delta", ctypes.c_float), ("tree_nodes", ctypes.c_int32),
                 ("tree_parent", ctypes.POINTER(ctypes.c_int32)), ("tree_rank", ctypes.POINTER(ctypes.c_int32)),
                 ("sample_seed", ctypes.c_uint32 * 2), ("sample_step", ctypes.c_int32),
-                ("schedule", ctypes.c_int32)]
+                ("schedule", ctypes.c_int32), ("vocab_begin", ctypes.c_int32), ("vocab_rows", ctypes.c_int32)]
 
 
 class Tree(ctypes.Structure):
@@ -90,10 +90,14 @@ def lib() -> ctypes.CDLL:
         L.medusa_step_launches.argtypes = [cfgp]
         L.medusa_heads_topk_noalloc.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp]
         L.medusa_check_bounded_wait.argtypes = [vp, ctypes.c_int32, vp]
+        L.medusa_shard_record_bytes.argtypes = [cfgp]
+        L.medusa_shard_record_bytes.restype = ctypes.c_size_t
+        L.medusa_shard_partial.argtypes = [cfgp, ctypes.POINTER(StepIO), vp, vp, vp]
+        L.medusa_shard_finish.argtypes = [cfgp, ctypes.POINTER(StepIO), vp, ctypes.c_int32, vp, vp]
         L.medusa_status_string.argtypes = [ctypes.c_int]
         L.medusa_status_string.restype = ctypes.c_char_p
         for f in EXPORTS:
-            if f not in ("medusa_workspace_bytes", "medusa_status_string"):
+            if f not in ("medusa_workspace_bytes", "medusa_status_string", "medusa_shard_record_bytes"):
                 getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -124,7 +128,8 @@ def make_config(shape, **over) -> Config:
     c.kv_len = shape.kv_len
     c.kv_capacity = shape.kv_capacity if shape.kv_capacity else shape.kv_len
     c.dtype = F32 if shape.dtype == "f32" else BF16
-    c.accept_mode = {"greedy": GREEDY, "typical": TYPICAL, "sample": SAMPLE}[shape.accept]
+    c.accept_mode = {"greedy": GREEDY, "typical": TYPICAL, "sample": SAMPLE,
+                     "typical-sample": TYPICAL_SAMPLE}[shape.accept]
     seed = getattr(shape, "sample_seed", (0, 0))
     c.sample_seed[0], c.sample_seed[1] = seed
     c.sample_step = getattr(shape, "sample_step", 0)
@@ -277,6 +282,21 @@ def medusa_step_profiled(cfg: Config, io: StepIO, ws, events, stream=None) -> No
                                                               _stream(stream), arr, len(events)))
 
 
+def shard_record_bytes(cfg: Config) -> int:
+    """Bytes of one vocabulary shard's exchange record (0 if the config names no shard)."""
+    return int(lib().medusa_shard_record_bytes(ctypes.byref(cfg)))
+
+
+def medusa_shard_partial(cfg: Config, io: StepIO, record, ws, stream=None) -> None:
+    _check("medusa_shard_partial", lib().medusa_shard_partial(ctypes.byref(cfg), ctypes.byref(io), _p(record),
+                                                              _p(ws), _stream(stream)))
+
+
+def medusa_shard_finish(cfg: Config, io: StepIO, records, n_shards: int, ws, stream=None) -> None:
+    _check("medusa_shard_finish", lib().medusa_shard_finish(ctypes.byref(cfg), ctypes.byref(io), _p(records),
+                                                            n_shards, _p(ws), _stream(stream)))
+
+
 def medusa_get_device_error(ws, stream=None) -> int:
     code = ctypes.c_int32()
     _check("medusa_get_device_error", lib().medusa_get_device_error(_p(ws), ctypes.byref(code), _stream(stream)))
@@ -285,6 +305,11 @@ def medusa_get_device_error(ws, stream=None) -> int:
 
 def medusa_check_bounded_wait(ws, budget_us: int, stream=None) -> None:
     _check("medusa_check_bounded_wait", lib().medusa_check_bounded_wait(_p(ws), budget_us, _stream(stream)))
+
+
+def step_launches_raw(cfg: Config) -> int:
+    """medusa_step_launches as returned (a negative status on a bad config)."""
+    return int(lib().medusa_step_launches(ctypes.byref(cfg)))
 
 
 def step_launches(cfg: Config) -> int:

@@ -61,7 +61,7 @@ class Shape:
     n_q_heads: int
     n_kv_heads: int
     head_dim: int
-    accept: str  # "greedy", "typical" or "sample"
+    accept: str  # "greedy", "typical", "sample" or "typical-sample"
     planted: Tuple  # ("fixed", d) or ("uniform", lo, hi)
     seed: int
     kv_capacity: int = 0  # cache rows per sequence; 0 means kv_len
@@ -200,6 +200,9 @@ _add(Shape("sample-sparse-mini", "bf16", 256, 777, 4, 3, (4, 3, 2, 2), 70, 2, 1,
            2014, sparse_nodes=24, temperature=0.3, sample_seed=(7, 11), sample_step=3))
 _add(Shape("7b-sample", "bf16", 4096, 32000, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "sample", ("fixed", 3),
            1007, full_size=True))
+# typical acceptance whose bonus token is drawn (the GQA reduced shapes)
+_add(Shape("typical-sample-mini", "bf16", 512, 4099, 4, 2, (4, 3, 2, 2), 257, 4, 2, 128, "typical-sample",
+           ("uniform", 0, 4), 2015, kv_capacity=260, sample_seed=(21, 22), sample_step=5))
 # profiling case: the 7B shapes with a quarter-sized vocabulary (still far
 # larger than L2) so that counter replays stay small
 _add(Shape("7b-prof", "bf16", 4096, 8192, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3), 4001,
@@ -330,3 +333,143 @@ PLANS_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file
 def load_plans(path: str = PLANS_PATH) -> dict:
     with open(path) as f:
         return json.load(f)
+
+
+# ----------------------------------------------------------------------------
+# Toy backbone for multi-round decoding.
+#
+# The decode step's inputs around the path (the tree's queries, keys and
+# values, the next hidden state) come from a base model.  For a loop of many
+# rounds a stand-in model is needed whose greedy continuation is known and
+# whose heads are right part of the time.  This toy draws, per token x:
+#   u[x, g]  a random unit vector per kv group g, key K[x, g] = a * u[x, g] and
+#            query Q[x, h] = a * u[x, h // G] with a^2 / sqrt(Dh) = 30, so every
+#            token attends almost only to its own key (a cache key scores ~N(0, 2)
+#            against it),
+#   Vt[x, g] a random N(0, 1) value, so the hidden state at token x is close
+#            to hv[x] = [Vt[x, h // G] for each q head h] (length H);
+# a random cyclic permutation pi of the vocabulary is the greedy continuation:
+#   lm_head[pi(x)] = hv[x] / |hv[x]|;
+# heads (W1 = b1 = 0, so z = h) with row W2_d[pi^(d+1)(x)] = +hv[x] / |hv[x]|
+# when head d is right about x (probability head_acc[d], drawn per (d, x)), else
+# -hv[x] / |hv[x]| (the true token then scores lowest and leaves the list).
+# These are random draws and row arrangements only: none of the step's
+# arithmetic happens here.
+
+
+@dataclasses.dataclass(frozen=True)
+class ToyShape:
+    """A toy backbone and the loop run on it (field names as in Shape, so the
+    same config builder applies)."""
+
+    name: str
+    hidden: int
+    vocab: int
+    n_heads: int
+    batch: int
+    topk: Tuple[int, ...]
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    kv_len: int  # cache rows before the first round
+    rounds: int
+    head_acc: Tuple[float, ...]  # per head depth: chance that the head is right about a token
+    seed: int
+    dtype: str = "bf16"
+    accept: str = "greedy"
+    temperature: float = 0.7
+    eps: float = 0.3
+    delta: float = 0.09
+
+    @property
+    def depth(self) -> int:
+        return len(self.topk)
+
+    @property
+    def kv_capacity(self) -> int:
+        """Room for every round's commit (at most depth + 1 rows per round)."""
+        return self.kv_len + self.rounds * (self.depth + 1)
+
+    cap = kv_capacity
+
+    @property
+    def n_nodes(self) -> int:
+        total, level = 1, 1
+        for k in self.topk:
+            level *= k
+            total += level
+        return total
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+TOYS: Dict[str, ToyShape] = {}
+for _t in (
+    ToyShape("toy-mini", 256, 997, 4, 3, (3, 2, 2, 1), 2, 1, 128, 40, 12, (0.9, 0.8, 0.7, 0.6), 5001),
+    ToyShape("toy-gqa-mini", 512, 1201, 4, 2, (4, 3, 2), 4, 2, 128, 70, 10, (0.85, 0.7, 0.55, 0.4), 5002),
+    ToyShape("toy-7b", 4096, 32000, 5, 1, (4, 3, 2, 2, 1), 32, 32, 128, 1024, 64, (0.9, 0.8, 0.7, 0.6, 0.5),
+             5003),
+):
+    TOYS[_t.name] = _t
+
+_TOY_TAG = {"perm": 1, "u": 2, "v": 3, "right": 4, "cache_k": 5, "cache_v": 6, "root": 7}
+
+
+def _toy_seed(t: ToyShape, tag: str, index: int = 0) -> int:
+    return (t.seed * 1_000_003 + _TOY_TAG[tag] * 7_919 + index * 104_729) & 0x7FFF_FFFF_FFFF_FFFF
+
+
+def make_toy(t: ToyShape) -> Dict[str, torch.Tensor]:
+    """The toy's tables, weights and first-round inputs (CPU tensors):
+    Qtab [V,Hq,Dh], Ktab / Vtab [V,Hkv,Dh], lm_head [V,H], W1 [K,H,H], b1 [K,H],
+    W2 [K,V,H], k_cache / v_cache [B,cap,Hkv,Dh] (the first kv_len rows drawn,
+    the rest zero), kv_lens [B], root_token [B], h [B,H] (the hidden state whose
+    greedy continuation is the root), perm [V] (pi) and right [K,V] (1 where
+    head k is right about a token)."""
+    V, H, K, B = t.vocab, t.hidden, t.n_heads, t.batch
+    Hq, Hkv, Dh = t.n_q_heads, t.n_kv_heads, t.head_dim
+    G = Hq // Hkv
+    dt = t.torch_dtype
+    g = torch.Generator().manual_seed(_toy_seed(t, "perm"))
+    order = torch.randperm(V, generator=g)
+    perm = torch.empty(V, dtype=torch.int64)
+    perm[order] = torch.roll(order, -1)  # one cycle through every token
+    u = _randn((V, Hkv, Dh), _toy_seed(t, "u"))
+    u = u / u.norm(dim=-1, keepdim=True)
+    a = math.sqrt(30.0 * math.sqrt(Dh))
+    Ktab = (a * u).to(dt)
+    Qtab = (a * u).repeat_interleave(G, dim=1).to(dt)
+    Vtab = _randn((V, Hkv, Dh), _toy_seed(t, "v")).to(dt)
+    hv = Vtab.to(torch.float32).repeat_interleave(G, dim=1).reshape(V, H)
+    unit = hv / hv.norm(dim=-1, keepdim=True)
+    lm = torch.empty((V, H), dtype=torch.float32)
+    lm[perm] = unit
+    W2 = torch.empty((K, V, H), dtype=dt)
+    right_all = torch.zeros((K, V), dtype=torch.int8)
+    step = perm.clone()  # pi^(d+1)
+    for d in range(K):
+        step = perm[step] if d > 0 else perm[perm]
+        acc = t.head_acc[d] if d < len(t.head_acc) else 0.0
+        right = torch.rand(V, generator=torch.Generator().manual_seed(_toy_seed(t, "right", d))) < acc
+        right_all[d] = right.to(torch.int8)
+        rows = torch.where(right[:, None], unit, -unit)
+        W2d = torch.empty((V, H), dtype=torch.float32)
+        W2d[step] = rows
+        W2[d] = W2d.to(dt)
+    cap = t.kv_capacity
+    kc = torch.zeros((B, cap, Hkv, Dh), dtype=dt)
+    vc = torch.zeros((B, cap, Hkv, Dh), dtype=dt)
+    for b in range(B):
+        kc[b, :t.kv_len] = _randn((t.kv_len, Hkv, Dh), _toy_seed(t, "cache_k", b)).to(dt)
+        vc[b, :t.kv_len] = _randn((t.kv_len, Hkv, Dh), _toy_seed(t, "cache_v", b)).to(dt)
+    gr = torch.Generator().manual_seed(_toy_seed(t, "root"))
+    root = torch.randint(0, V, (B,), generator=gr, dtype=torch.int64)
+    inv = torch.empty(V, dtype=torch.int64)
+    inv[perm] = torch.arange(V)
+    h = hv[inv[root]].to(dt)
+    return {"Qtab": Qtab, "Ktab": Ktab, "Vtab": Vtab, "lm_head": lm.to(dt), "W1": torch.zeros((K, H, H), dtype=dt),
+            "b1": torch.zeros((K, H), dtype=dt), "W2": W2, "k_cache": kc, "v_cache": vc,
+            "kv_lens": torch.full((B,), t.kv_len, dtype=torch.int32), "root_token": root.to(torch.int32), "h": h,
+            "perm": perm.to(torch.int32), "right": right_all}

@@ -39,6 +39,9 @@ design notes):
       is the argmax at the last accepted node.
   R8  the attention output is rounded to its storage type (bf16 or fp32)
       before the verification projection reads it.
+  R15 typical acceptance with a sampled bonus: the acceptance as R7, the
+      bonus token drawn from softmax(logits / temperature) at the last kept
+      node with the sampling mode's Gumbel-max draw (same noise keying).
 """
 from __future__ import annotations
 
@@ -394,6 +397,39 @@ def accept_greedy(tree: Tree, tokens_b: np.ndarray, argmax_b: np.ndarray):
     return len(toks), toks, nodes, int(argmax_b[cur])
 
 
+def accept_rejection(tree: Tree, tokens_b: np.ndarray, probs, uniform):
+    """Rejection sampling against the base model over the tree's fixed
+    candidates [P2: exact rejection sampling verifies the candidates against
+    the base model's distribution, so the output keeps that distribution]:
+    at the current node its children are tried in rank order; child i's token
+    is accepted with its base probability renormalised over the tokens not
+    yet rejected, p(t_i) / (1 - sum_{j<i} p(t_j)) (a candidate of probability
+    one is the whole remaining mass); if one is accepted the walk continues
+    from it, else the bonus token is drawn from p with the rejected tokens
+    removed.  ``probs(node)`` is the base distribution at a node (length V),
+    ``uniform()`` a draw from U(0, 1).  Returns (length, tokens, nodes incl.
+    root, bonus)."""
+    cur, nodes, toks = 0, [0], []
+    while True:
+        p = np.array(probs(cur), dtype=np.float64)
+        rest = 1.0
+        nxt = None
+        for c in tree.children[cur]:
+            t = int(tokens_b[c])
+            if rest > 0 and uniform() * rest < p[t]:
+                nxt = c
+                break
+            rest -= p[t]
+            p[t] = 0.0
+        if nxt is None:
+            q = p / p.sum()
+            bonus = int(np.searchsorted(np.cumsum(q), uniform() * q.sum(), side="right"))
+            return len(toks), toks, nodes, min(bonus, len(q) - 1)
+        nodes.append(nxt)
+        toks.append(int(tokens_b[nxt]))
+        cur = nxt
+
+
 def accept_typical(tree: Tree, tokens_b: np.ndarray, argmax_b: np.ndarray, keep_edge):
     """Typical acceptance (R7): ``keep_edge(parent, child)`` says whether the
     child's token clears its parent's entropy-tied threshold; the longest
@@ -444,6 +480,124 @@ def next_inputs(attn_out_stored, acc_nodes, accept_len, bonus):
     return h, np.array([int(x) for x in bonus], dtype=np.int32)
 
 
+# ------------------------------------------------------ vocabulary shards --
+# The step is memory-bound [P3, abstract], so at batch 1 only a split of the
+# weights cuts the bytes each GPU reads: shard s holds vocabulary rows
+# [v0, v1) of every head projection and of lm_head, computes what those rows
+# give, and the shards' small partial results are combined.  These functions
+# state that split on the CPU: what one shard computes, and the combination,
+# whose result must equal the unsplit step.
+
+def shard_topk(z: np.ndarray, W2_shard, v0: int, topk: Sequence[int]):
+    """One shard's per-head top-k (R5, R6) over its rows: W2_shard [K,Vs,H]
+    holds rows v0 .. v0+Vs-1 of every head.  Token ids are global (local row
+    + v0; ties still go to the lower id).  Returns idx [B,K,kmax] (pad -1),
+    val [B,K,kmax] (pad -inf)."""
+    idx, val = topk_lists(head_logits(z, W2_shard), topk)
+    return np.where(idx >= 0, idx + v0, -1).astype(np.int32), val
+
+
+def merge_topk(parts: Sequence, topk: Sequence[int]):
+    """Global per-head top-k from the shards' lists [(idx, val), ...]: the
+    union of the candidates, again by descending value, ties to the lower
+    id; also the (shard, rank in that shard's list) each entry came from."""
+    B, K, kmax = parts[0][0].shape
+    idx = np.full((B, K, kmax), -1, dtype=np.int32)
+    val = np.full((B, K, kmax), -np.inf)
+    src = np.full((B, K, kmax, 2), -1, dtype=np.int32)
+    for b in range(B):
+        for k in range(K):
+            n = topk[k] if k < len(topk) else 1
+            cand = [(-float(pv[b, k, j]), int(pi[b, k, j]), si, j) for si, (pi, pv) in enumerate(parts)
+                    for j in range(kmax) if pi[b, k, j] >= 0]
+            cand.sort()
+            for r, (nv, t, si, j) in enumerate(cand[:n]):
+                idx[b, k, r], val[b, k, r], src[b, k, r] = t, -nv, (si, j)
+    return idx, val, src
+
+
+def shard_node_states(o_stored: np.ndarray, lm_shard, v0: int, temperature: Optional[float] = None):
+    """One shard's scores of every node over its lm_head rows, reduced to a
+    state that combines across shards: the maximum m and its (global, lowest)
+    id, and with a temperature T, z = sum_v exp(t_v) and s = sum_v exp(t_v) t_v
+    with t_v = (logit_v - m) / T (so log-partition = m / T + ln z, entropy =
+    ln z - s / z).  Returns arrays m, i, z, s over the nodes."""
+    L = o_stored @ decode(lm_shard).T  # [N, Vs]
+    m = L.max(axis=1)
+    i = np.argmax(L, axis=1) + v0  # first maximum = lowest id
+    if temperature is None:
+        return {"m": m, "i": i, "z": np.ones_like(m), "s": np.zeros_like(m)}
+    t = (L - m[:, None]) / temperature
+    e = np.exp(t)
+    return {"m": m, "i": i, "z": e.sum(axis=1), "s": (e * t).sum(axis=1)}
+
+
+def merge_node_states(parts: Sequence[Dict[str, np.ndarray]], temperature: Optional[float] = None):
+    """Combination of the shards' node states: the larger maximum wins (ties
+    to the lower id); with a temperature each shard's sums are brought to the
+    common maximum, z = sum_s z_s e^(d_s) and s = sum_s e^(d_s) (s_s + z_s d_s)
+    with d_s = (m_s - m) / T.  Returns argmax, maxlogit and (with T) lse and
+    entropy, as verify_stats names them."""
+    m = np.max(np.stack([p["m"] for p in parts]), axis=0)
+    i = np.full(m.shape, np.iinfo(np.int64).max)
+    for p in parts:
+        i = np.where(p["m"] == m, np.minimum(i, p["i"]), i)
+    res = {"argmax": i, "maxlogit": m}
+    if temperature is not None:
+        z = np.zeros_like(m)
+        ss = np.zeros_like(m)
+        for p in parts:
+            d = (p["m"] - m) / temperature
+            z += p["z"] * np.exp(d)
+            ss += np.exp(d) * (p["s"] + p["z"] * d)
+        res["lse"] = m / temperature + np.log(z)
+        res["entropy"] = np.log(z) - ss / z
+    return res
+
+
+# ------------------------------------------------------- rounds of decoding --
+
+def decode_rounds(toy: Dict[str, np.ndarray], shape, rounds: int) -> Dict[str, list]:
+    """Round after round of Medusa decoding over a table backbone [P1,
+    "Attenzione sull'albero e accettazione": the kept branch is appended and
+    the next round starts from it].  A round: heads and top-k on the hidden
+    state, the candidate tree, the tree's queries / keys / values looked up
+    per token in the backbone's tables (Qtab [V,Hq,Dh], Ktab / Vtab
+    [V,Hkv,Dh]), tree attention over each sequence's grown cache, greedy
+    verification and acceptance, then the commit of the kept branch (root
+    first) and the next inputs (hidden state of the last kept node, the bonus
+    as the next root).  ``toy`` holds numpy arrays (bf16 as uint16 bit
+    patterns) as synth.make_toy lays them out.  Returns per round the root,
+    accept_len, acc_tokens, acc_nodes and bonus of every sequence."""
+    topk = list(shape.topk)
+    tree = Tree(topk)
+    kc, vc = toy["k_cache"], toy["v_cache"]
+    lens = [int(x) for x in toy["kv_lens"]]
+    h, root = toy["h"], [int(x) for x in toy["root_token"]]
+    out = {k: [] for k in ("root", "accept_len", "acc_tokens", "acc_nodes", "bonus")}
+    for _ in range(rounds):
+        z = head_hidden(h, toy["W1"], toy["b1"])
+        idx, _ = topk_lists(head_logits(z, toy["W2"]), topk)
+        tok = tree.tokens(idx, root)
+        B, T = tok.shape
+        q, kt, vt = toy["Qtab"][tok], toy["Ktab"][tok], toy["Vtab"][tok]
+        o = round_to_storage(tree_attention(q, kt, vt, kc, vc, lens, tree.mask), shape.dtype)
+        am = verify_stats(o.reshape(B * T, -1), toy["lm_head"])["argmax"].reshape(B, T)
+        acc = [accept_greedy(tree, tok[b], am[b]) for b in range(B)]
+        n = [a[0] for a in acc]
+        nodes = [a[2] for a in acc]
+        out["root"].append(list(root))
+        out["accept_len"].append(n)
+        out["acc_tokens"].append([a[1] for a in acc])
+        out["acc_nodes"].append(nodes)
+        out["bonus"].append([a[3] for a in acc])
+        kc, vc, lens = kv_commit(kc, vc, kt, vt, nodes, n, lens)
+        lens = [int(x) for x in lens]
+        h, root = next_inputs(o, nodes, n, [a[3] for a in acc])
+        root = [int(x) for x in root]
+    return out
+
+
 # -------------------------------------------------------------- whole step --
 
 def step(inp: Dict[str, np.ndarray], shape, nodes_only: Optional[Dict[int, Sequence[int]]] = None) -> Dict:
@@ -467,7 +621,7 @@ def step(inp: Dict[str, np.ndarray], shape, nodes_only: Optional[Dict[int, Seque
                             shape.kv_len, tree.mask, nodes=nb, batches=[b])
         o[b] = ob[b]
     o_st = round_to_storage(o, shape.dtype)
-    typical = shape.accept == "typical"
+    typical = shape.accept in ("typical", "typical-sample")
     flat = o_st.reshape(B * T, H)
     rows = None
     if nodes_only is not None:
@@ -481,6 +635,12 @@ def step(inp: Dict[str, np.ndarray], shape, nodes_only: Optional[Dict[int, Seque
            "attn_out": o_st, "argmax": argmax, "maxlogit": stats["maxlogit"].reshape(B, T),
            "second": stats["second"].reshape(B, T), "lse": stats["lse"].reshape(B, T), "entropy": stats["entropy"].reshape(B, T),
            "accept_len": [], "acc_tokens": [], "acc_nodes": [], "bonus": []}
+    if shape.accept == "typical-sample":  # R15: the bonus is a draw from the base distribution
+        draws = sample_stats(flat, inp["lm_head"], shape.temperature, shape.sample_seed, shape.sample_step,
+                             rows=rows)
+        res["draw"] = draws["argmax"].reshape(B, T)
+        res["draw_max"] = draws["maxlogit"].reshape(B, T)
+        res["draw_second"] = draws["second"].reshape(B, T)
     for b in range(B):
         if typical:
             def keep(p, c, b=b):
@@ -491,6 +651,8 @@ def step(inp: Dict[str, np.ndarray], shape, nodes_only: Optional[Dict[int, Seque
                 thr = typical_threshold(stats["entropy"][b * T + p], shape.eps, shape.delta)
                 return math.exp(lp) > thr
             n, tk, nd, bonus = accept_typical(tree, tok[b], argmax[b], keep)
+            if shape.accept == "typical-sample":
+                bonus = int(res["draw"][b, nd[-1]])
         else:
             n, tk, nd, bonus = accept_greedy(tree, tok[b], argmax[b])
         res["accept_len"].append(n)

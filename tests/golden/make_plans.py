@@ -152,9 +152,14 @@ def build_plan(s: synth.Shape, log=print) -> dict:
         assert res["accept_len"][b] == sq["depth"], (s.name, b, res["accept_len"][b], sq["depth"])
         assert res["acc_tokens"][b] == sq["tokens"], (s.name, b)
         assert res["acc_nodes"][b] == sq["nodes"], (s.name, b)
+        if s.accept == "typical-sample":  # the bonus is the draw at the last kept node: keep it, with its margin
+            last = sq["nodes"][-1]
+            dm, d2 = res["draw_max"][b, last], res["draw_second"][b, last]
+            assert dm - d2 >= REL_NODE[s.dtype] * max(1.0, abs(dm)), (s.name, b, "draw margin")
+            sq["bonus"] = int(res["bonus"][b])
         assert res["bonus"][b] == sq["bonus"], (s.name, b)
         assert [int(x) for x in res["topk_idx"][b].ravel()] == [int(x) for x in topk_idx[b].ravel()]
-        if s.accept == "typical":
+        if s.accept in ("typical", "typical-sample"):
             flat = res["attn_out"].reshape(B * T, -1)
             for p in sq["nodes"]:
                 thr = O.typical_threshold(res["entropy"][b, p], s.eps, s.delta)

@@ -169,3 +169,44 @@ def test_schedule_launch_counts():
         assert n(name) == n(name, schedule=M.OVERLAP), name
     for name in ("13b-bf16", "gqa128k-bf16", "33b-bf16", "tiny-fp32", "33b-b32-mini"):
         assert n(name) == n(name, schedule=M.SERIAL), name
+
+
+def test_vocabulary_shard_configs_on_the_host():
+    """Shard ranges are validated before any launch: a range past the
+    vocabulary or an offset without rows is MEDUSA_ERR_INVALID_ARG, fewer rows
+    than the longest top-k list MEDUSA_ERR_UNSUPPORTED; a shard config is
+    refused by the unsharded entry points and an unsharded one by the shard
+    entry points; the record size follows the layout of the header (16 bytes
+    of header, then lists, node states and, for typical acceptance, the
+    candidates' scores, each section 16-byte aligned)."""
+    fake = ctypes.c_void_p(4096)  # aligned, never dereferenced: every call below stops on the host
+    s = synth.SHAPES["7b-mini"]
+    bad = [(dict(vocab_begin=s.vocab - 10, vocab_rows=11), -1), (dict(vocab_begin=5, vocab_rows=0), -1),
+           (dict(vocab_begin=0, vocab_rows=3), -2)]
+    for over, code in bad:
+        cfg = M.make_config(s, **over)
+        assert M.lib().medusa_workspace_bytes(ctypes.byref(cfg)) == 0, over
+        T = ctypes.c_int32()
+        assert M.lib().medusa_tree_size(ctypes.byref(cfg), ctypes.byref(T), None, None) == code, over
+    shard = M.make_config(s, vocab_begin=1000, vocab_rows=1001)
+    io = M.StepIO()
+    assert M.lib().medusa_step(ctypes.byref(shard), ctypes.byref(io), fake, None) == -1
+    assert M.lib().medusa_heads_topk(ctypes.byref(shard), fake, fake, fake, fake, fake, fake, fake, None) == -1
+    assert M.lib().medusa_heads_topk_noalloc(ctypes.byref(shard), fake, fake, fake, fake, fake, fake, None) == -1
+    assert M.step_launches_raw(shard) == -1
+    whole = M.make_config(s)
+    assert M.shard_record_bytes(whole) == 0
+    assert M.lib().medusa_shard_partial(ctypes.byref(whole), ctypes.byref(io), fake, fake, None) == -1
+    assert M.lib().medusa_shard_finish(ctypes.byref(whole), ctypes.byref(io), fake, 2, fake, None) == -1
+    assert M.lib().medusa_shard_finish(ctypes.byref(shard), ctypes.byref(io), fake, 0, fake, None) == -1
+    B, K, kmax, T = s.batch, s.n_heads, max(s.topk), s.n_nodes
+    up = lambda x: (x + 15) // 16 * 16
+    lists = up(16 + B * K * kmax * 4)
+    lists = up(lists + B * K * kmax * 4)
+    assert M.shard_record_bytes(shard) == up(lists + B * T * 16)
+    g = synth.SHAPES["gqa-mini"]
+    tg = M.make_config(g, vocab_begin=0, vocab_rows=2000)
+    B, K, kmax, T = g.batch, g.n_heads, max(g.topk), g.n_nodes
+    lists = up(16 + B * K * kmax * 4)
+    lists = up(lists + B * K * kmax * 4)
+    assert M.shard_record_bytes(tg) == up(up(lists + B * T * 16) + B * T * kmax * 4)

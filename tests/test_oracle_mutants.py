@@ -149,6 +149,37 @@ def _gumbel_neg_log(seed, step, node, V):
     return -np.log(np.exp(-np.exp(-g)))
 
 
+def _rounds_root_hidden(toy, shape, rounds):
+    # each round starts from the root's hidden state instead of the last kept node's
+    B = toy["h"].shape[0]
+    orig = O.next_inputs
+    O.next_inputs = lambda o, nodes, n, bonus: orig(o, [[nd[0]] * (len(nd)) for nd in nodes], [0] * B, bonus)
+    try:
+        return O.decode_rounds(toy, shape, rounds)
+    finally:
+        O.next_inputs = orig
+
+
+def _rejection_unnormalised(tree, tokens_b, probs, uniform):
+    # accepts child i with p(t_i) instead of renormalising after earlier rejections
+    cur, nodes, toks = 0, [0], []
+    while True:
+        p = np.array(probs(cur), dtype=np.float64)
+        nxt = None
+        for c in tree.children[cur]:
+            t = int(tokens_b[c])
+            if uniform() < p[t]:
+                nxt = c
+                break
+            p[t] = 0.0
+        if nxt is None:
+            q = p / p.sum()
+            return len(toks), toks, nodes, min(int(np.searchsorted(np.cumsum(q), uniform(), side="right")), len(q) - 1)
+        nodes.append(nxt)
+        toks.append(int(tokens_b[nxt]))
+        cur = nxt
+
+
 def _attn_scale_dh(q, k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes=None, batches=None):
     Dh = q.shape[-1]
     return O.tree_attention(q * (math.sqrt(Dh) / Dh), k_tree, v_tree, k_cache, v_cache, kv_len, mask, nodes, batches)
@@ -193,6 +224,20 @@ def _threshold_no_exp(entropy, eps, delta):
     return min(eps, delta * entropy)
 
 
+def _check_rounds(M):
+    from tests import test_decode_loop as L
+    t, toy = L._toy_np("toy-mini")
+    hist = M.decode_rounds(toy, t, t.rounds)
+    inv = np.argsort(toy["perm"])
+    for r in range(t.rounds):
+        for b in range(t.batch):
+            x = int(inv[hist["root"][r][b]])
+            n = 0
+            while n < t.depth and toy["right"][n][x]:
+                n += 1
+            assert hist["accept_len"][r][b] == n
+
+
 MUTANTS = [
     ("head drops the residual", dict(head_hidden=_no_residual), P.check_zero_init),
     ("head drops the bias", dict(head_hidden=_no_bias), P.check_head_vs_torch),
@@ -220,6 +265,9 @@ MUTANTS = [
      P.check_philox_kat),
     ("Philox multipliers exchanged", dict(philox4x32_10=_philox(mul=O.PHILOX_MUL[::-1])), P.check_philox_kat),
     ("exponential noise instead of Gumbel", dict(gumbel_noise=_gumbel_neg_log), P.check_gumbel_distribution),
+    ("rounds restart from the root's hidden state", dict(decode_rounds=_rounds_root_hidden), _check_rounds),
+    ("rejection without renormalising", dict(accept_rejection=_rejection_unnormalised),
+     P.check_rejection_sampling_is_lossless),
 ]
 
 

@@ -470,7 +470,7 @@ def check_plans(M) -> None:
     """On every reduced workload the oracle realises the planted acceptance."""
     plans = synth.load_plans()
     for name in ["tiny-fp32", "tiny-fp32-gqa", "7b-mini", "13b-mini", "gqa-mini", "33b-mini", "sparse-mini",
-                 "sparse-typical-mini", "sparse-f32", "sample-mini", "sample-sparse-mini"]:
+                 "sparse-typical-mini", "sparse-f32", "sample-mini", "sample-sparse-mini", "typical-sample-mini"]:
         s = synth.SHAPES[name]
         inp = {k: to_np(v) for k, v in synth.make_inputs(s, plans[name]).items()}
         res = M.step(inp, s)
@@ -521,3 +521,65 @@ CHECKS = [check_zero_init, check_head_vs_torch, check_topk, check_tree_2x3, chec
 @pytest.mark.parametrize("check", CHECKS, ids=lambda c: c.__name__)
 def test_oracle_pin(check):
     check(O)
+
+
+def _sampling_tree_case():
+    """A 2x2 tree over a 5-token vocabulary with fixed base distributions per
+    node, and the exact distribution of what sequential sampling emits."""
+    V = 5
+    tree_topk = (2, 2)
+    rng = np.random.default_rng(3)
+    T = 1 + 2 + 4
+    P = rng.dirichlet(np.ones(V) * 0.8, size=T)
+    tokens = np.array([0, 1, 3, 2, 4, 0, 3])  # root, depth-1 children, depth-2 children
+    return V, tree_topk, P, tokens
+
+
+def _exact_emission(tree, tokens, P):
+    """P(accepted tokens + bonus) for plain sequential sampling from the base
+    distributions: draw at the current node; a draw equal to a child's token
+    moves there, any other draw ends the walk as the bonus."""
+    out = {}
+
+    def walk(node, pref, pr):
+        for x in range(P.shape[1]):
+            kid = [c for c in tree.children[node] if tokens[c] == x]
+            if kid:
+                walk(kid[0], pref + (x,), pr * P[node, x])
+            else:
+                out[pref + ("bonus", x)] = out.get(pref + ("bonus", x), 0.0) + pr * P[node, x]
+
+    walk(0, (), 1.0)
+    return out
+
+
+def check_rejection_sampling_is_lossless(M) -> None:
+    """Both sampling verifications emit what sequential sampling from the base
+    model emits: the rejection walk over the fixed candidates and the
+    Gumbel-max draw per node with a candidate kept when it equals its
+    parent's draw (the library's sampling mode).  Over 30000 trials each, the
+    emitted (tokens, bonus) frequencies pass a chi-square test against the
+    exact distribution computed by enumeration (bound at p ~ 1e-4)."""
+    V, topk, P, tokens = _sampling_tree_case()
+    tree = M.Tree(topk)
+    exact = _exact_emission(tree, tokens, P)
+    keys = sorted(exact, key=str)
+    n = 30000
+    rng = np.random.default_rng(11)
+    counts_r = {k: 0 for k in keys}
+    counts_g = {k: 0 for k in keys}
+    for trial in range(n):
+        k, toks, _, bonus = M.accept_rejection(tree, tokens, lambda node: P[node], rng.random)
+        counts_r[tuple(toks) + ("bonus", bonus)] += 1
+        g = -np.log(-np.log(rng.random((tree.T, V))))
+        draw = np.argmax(np.log(P) + g, axis=1)
+        k, toks, _, bonus = M.accept_greedy(tree, tokens, draw)  # keep a child equal to its parent's draw
+        counts_g[tuple(toks) + ("bonus", bonus)] += 1
+    dof = len(keys) - 1
+    bound = dof + 4.3 * math.sqrt(2 * dof)
+    for counts in (counts_r, counts_g):
+        chi2 = sum((counts[k] - n * exact[k]) ** 2 / (n * exact[k]) for k in keys)
+        assert chi2 < bound, (chi2, bound)
+
+
+CHECKS.append(check_rejection_sampling_is_lossless)

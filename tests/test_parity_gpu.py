@@ -44,7 +44,8 @@ def test_step_matches_oracle(name):
 # bf16, head dim 128, batch <= 32: shapes the overlap schedule accepts (greedy,
 # typical, sample; sparse and wide trees; no cache; a depth-1 chain; 16-entry lists)
 OVERLAP_OK = ["7b-mini", "13b-mini", "gqa-mini", "gqa-b16-mini", "sample-mini", "sparse-mini",
-              "sparse-typical-mini", "wide-bf16", "nocache-bf16", "b5-mini", "chain-bf16", "13b-b8-split", "k16-bf16"]
+              "sparse-typical-mini", "wide-bf16", "nocache-bf16", "b5-mini", "chain-bf16", "13b-b8-split", "k16-bf16",
+              "typical-sample-mini"]
 
 
 @pytest.mark.parametrize("name", OVERLAP_OK)
@@ -106,7 +107,7 @@ def test_stage_calls_equal_fused_step(name):
                 assert torch.equal(a[k][t], b[k][t]), t
         elif a[k].dtype in (torch.int32, torch.int64):
             assert torch.equal(a[k], b[k]), k
-        elif k not in ("node_lse", "node_entropy") or s.accept == "typical":
+        elif k not in ("node_lse", "node_entropy") or s.accept in ("typical", "typical-sample"):
             U.assert_close(a[k].float().numpy(), b[k].float().numpy(), s.dtype, k)
 
 

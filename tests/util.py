@@ -118,7 +118,7 @@ def compare_step(s, res: Dict, ref: Dict, check_all_nodes: bool = True) -> None:
         assert_close(got_o, ref["attn_out"], s.dtype, "attn_out")
         np.testing.assert_array_equal(res["node_argmax"].numpy(), ref["argmax"], err_msg="node_argmax")
         assert_close(res["node_maxlogit"].numpy(), ref["maxlogit"], s.dtype, "node_maxlogit")
-        if s.accept == "typical":
+        if s.accept in ("typical", "typical-sample"):
             assert_close(res["node_lse"].numpy(), ref["lse"], s.dtype, "node_lse")
             assert_close(res["node_entropy"].numpy(), ref["entropy"], s.dtype, "node_entropy")
     # acceptance: bit-exact
