@@ -403,21 +403,35 @@ def run_medusa(args, world, rank, local):
     # buffer sets pipeline the copies with the steps: step n+1's inputs upload
     # on an upload stream while step n computes, and the host waits for step n's
     # result while step n+1 runs (each step still copies in and reads out).
+    # A step's inputs travel as one packed buffer (each tensor at a 256-byte
+    # aligned offset): one host-to-device copy per step.
     step_in = ["h", "root_token", "q", "k_tree", "v_tree"]
-    host_in = {k: inp[k].pin_memory() for k in step_in}
+    offs, nbytes = {}, 0
+    for k in step_in:
+        offs[k] = nbytes
+        nbytes = (nbytes + inp[k].numel() * inp[k].element_size() + 255) // 256 * 256
+    host_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    for k in step_in:
+        n_k = inp[k].numel() * inp[k].element_size()
+        host_in[offs[k]:offs[k] + n_k].copy_(inp[k].contiguous().view(-1).view(torch.uint8))
+
+    def views(buf):
+        return {k: buf[offs[k]:offs[k] + inp[k].numel() * inp[k].element_size()].view(inp[k].dtype).view(inp[k].shape)
+                for k in step_in}
+
     step_out = ["accept_len", "acc_tokens", "bonus"]
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()  # one stream each way: an upload never queues behind a readback
     sets = []
     for j in range(2):
+        packed = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         d_j = dict(dinp)
-        for k in step_in:
-            d_j[k] = torch.empty_like(dinp[k])
+        d_j.update(views(packed))
         o_j = M.alloc_outputs(cfg)
-        sets.append({"in": d_j, "out": o_j, "io": M.step_io(d_j, o_j), "ws": M.alloc_workspace(cfg),
+        sets.append({"packed": packed, "out": o_j, "io": M.step_io(d_j, o_j), "ws": M.alloc_workspace(cfg),
                      "host_out": {k: torch.empty(o_j[k].shape, dtype=o_j[k].dtype).pin_memory() for k in step_out},
                      "ev_in": torch.cuda.Event(), "ev_done": torch.cuda.Event(), "ev_out": torch.cuda.Event()})
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    h2d = nbytes
     d2h = sum(v.numel() * v.element_size() for v in sets[0]["host_out"].values())
 
     def e2e_run(n_steps):
@@ -426,8 +440,7 @@ def run_medusa(args, world, rank, local):
             b = sets[n % 2]
             with torch.cuda.stream(up):
                 up.wait_event(b["ev_done"])  # the set's previous step has finished with its inputs
-                for k in step_in:
-                    b["in"][k].copy_(host_in[k], non_blocking=True)
+                b["packed"].copy_(host_in, non_blocking=True)
                 b["ev_in"].record(up)
             comp.wait_event(b["ev_in"])
             M.medusa_step(cfg, b["io"], b["ws"], comp)
@@ -505,6 +518,69 @@ def decode_loop_figures(args, name: str = "toy-7b") -> dict:
             "heads": "synthetic, right per (head, token) with probability " + str(list(t.head_acc))}
 
 
+def run_vocab_shards(args, world, rank, local):
+    """The vocabulary-sharded step: rank r holds rows of W2 and lm_head for
+    shard r of `world`; every step is medusa_shard_partial, one all-gather of
+    the records (NCCL), medusa_shard_finish.  One step runs on all ranks at
+    once, so value = steps/s of the job (strong scaling: the work per step is
+    fixed as the rank count grows)."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    from medusa_head_tree_heads_b300 import shards as SH
+    torch.cuda.set_device(local)
+    s = synth.SHAPES[args.workload]
+    plan = synth.load_plans()[s.name]
+    inp = synth.make_inputs(s, plan)
+    v0, v1 = SH.bounds(s.vocab, world)[rank]
+    W2s, lms = SH.shard_weights(inp.pop("W2"), inp.pop("lm_head"), v0, v1)
+    dinp = {k: v.cuda() for k, v in inp.items()}
+    dinp["W2"], dinp["lm_head"] = W2s.cuda(), lms.cuda()
+    del W2s, lms
+    st = SH.ShardedStep(s, world, rank)
+    out = M.alloc_outputs(st.cfg)
+    io = M.step_io(dinp, out)
+
+    def step():
+        st.partial(io)
+        if world > 1:
+            SH.exchange(st.record, st.records)
+        else:
+            st.records[0].copy_(st.record)
+        st.finish(io)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert M.medusa_get_device_error(st.ws) == 0
+    acc = out["accept_len"].cpu().tolist()
+    assert acc == [q["depth"] for q in plan["seqs"]], acc
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        ev0.record()
+        for _ in range(args.steps):
+            step()
+        ev1.record()
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = reduce_max(ev0.elapsed_time(ev1) / args.steps, world)
+    byts = algorithmic_bytes(s)
+    shard_bytes = byts["step"] - (s.n_heads + 1) * (s.vocab - (v1 - v0)) * s.hidden * (2 if s.dtype == "bf16" else 4)
+    peaks = measured_peaks()
+    line = {"metric": METRIC, "value": round(1e3 / ms, 2), "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
+            "config": dict(workload_config(s, f"vocab-sharded x{world}"), l2="inputs larger than L2 (no flush)",
+                           accept_len=acc, launch="eager, one all-gather per step"),
+            "roofline": {"bound": "hbm", "kernel": "whole sharded step (rank 0)", "unit": "GB/s",
+                         "achieved": round(shard_bytes / (ms * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                         "frac": round(shard_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peaks["source"], "algorithmic_bytes": shard_bytes},
+            "gpu_launches": None, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -516,6 +592,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--no-loop", action="store_true", help="skip the multi-round decoding figures")
+    ap.add_argument("--vocab-shards", action="store_true",
+                    help="split W2 / lm_head rows over the ranks (one all-gather per step) instead of replicas")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     args.warmup = max(args.warmup, 3)  # at least 3 warm-up steps, reported as run
@@ -525,6 +603,8 @@ def main():
         args.steps = min(args.steps, 20)
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.vocab_shards:
+        run_vocab_shards(args, world, rank, local)
     else:
         run_medusa(args, world, rank, local)
     if world > 1:

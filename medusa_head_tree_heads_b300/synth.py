@@ -207,6 +207,10 @@ _add(Shape("typical-sample-mini", "bf16", 512, 4099, 4, 2, (4, 3, 2, 2), 257, 4,
 # larger than L2) so that counter replays stay small
 _add(Shape("7b-prof", "bf16", 4096, 8192, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "greedy", ("fixed", 3), 4001,
            full_size=True))
+# profiling case of the tensor-bound verification: the GQA workload's batch,
+# tree and widths with a 32000-row vocabulary (lm_head 262 MB, still past L2)
+_add(Shape("gqa-prof", "bf16", 4096, 32000, 4, 16, (4, 3, 2, 2), 1024, 32, 8, 128, "typical", ("uniform", 0, 4), 4002,
+           full_size=True))
 # edge cases: a chain tree (the mask is causal), a root-only tree, an empty
 # cache, the widest tree under the 512-node limit, and the deepest tree
 _add(Shape("chain-bf16", "bf16", 256, 999, 3, 2, (1, 1, 1), 64, 2, 2, 128, "greedy", ("uniform", 0, 3), 3001))
