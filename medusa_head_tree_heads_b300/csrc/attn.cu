@@ -8,19 +8,20 @@
 //   o = sum_j softmax_j(q . k_j / sqrt(Dh)) v_j,
 //   j over cache rows [0, L) and tree nodes j with bit j of the node's mask row.
 //
-// CUDA-core version: a CTA owns 32 query rows of one (b, g) and streams all
-// of that group's keys through shared memory in tiles of 32 (cache tiles
-// unmasked, tree tiles masked by one mask word per row and tile), with an
-// fp32 online softmax per row in registers.  Rows of one (b, g) sit in
-// adjacent CTAs so that the group's K/V tiles are served from L2 after the
-// first read.  No split of the key range, so no partial results and no
-// combine step.
+// CUDA-core version: a CTA owns up to 16 query rows of one (b, g); its 8
+// warps split the group's keys (cache tiles, then tree tiles masked by the
+// rows' mask words) between them, tile w, w + 8, ... for warp w, each warp
+// keeping an fp32 online softmax per row over its own tiles in registers and
+// its own K/V tile in shared memory (no CTA-wide barrier in the key loop).
+// The 8 partial states of every row are joined at the end through shared
+// memory.  No partial results leave the CTA, so no combine launch.  A tile is
+// 32 keys for head dim 64 (lane = key) and 16 keys for head dim 128.
 #include "internal.cuh"
 
 namespace medusa {
 
-constexpr int AT_ROWS = 32;  // query rows per CTA (4 per warp)
-constexpr int AT_KT = 32;    // keys per tile
+constexpr int AF_ROWS = 16;   // query rows per CTA
+constexpr int AF_WARPS = 8;
 
 struct AttnArgs {
   const void *q, *kt, *vt, *kc, *vc;
@@ -32,38 +33,45 @@ struct AttnArgs {
   uint8_t* ws;
 };
 
-template <typename TT, int DH>
-__global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
-  constexpr int DPL = DH / 32;  // dims per lane
-  extern __shared__ float4 at_smem[];
-  float(*qs)[DH] = reinterpret_cast<float(*)[DH]>(at_smem);                     // [AT_ROWS][DH]
-  float(*ks)[DH + 1] = reinterpret_cast<float(*)[DH + 1]>(&qs[AT_ROWS][0]);     // [AT_KT][DH+1]
-  float(*vs)[DH] = reinterpret_cast<float(*)[DH]>(&ks[AT_KT][0]);              // [AT_KT][DH]
-  __shared__ uint32_t mw[AT_ROWS];
+template <int DH>
+constexpr int af_keys() { return DH == 64 ? 32 : 16; }
+template <int DH>
+constexpr size_t af_smem_floats() {  // queries + per warp one K tile (padded rows) and one V tile
+  return (size_t)AF_ROWS * DH + (size_t)AF_WARPS * af_keys<DH>() * (2 * DH + 1);
+}
 
+template <typename TT, int DH>
+__global__ void __launch_bounds__(AF_WARPS * 32) tree_attn_kernel(AttnArgs a) {
+  constexpr int DPL = DH / 32;      // output dims per lane
+  constexpr int KT = af_keys<DH>();  // keys per tile
+  extern __shared__ float4 at_smem[];
+  float* qs = reinterpret_cast<float*>(at_smem);  // [AF_ROWS][DH]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* ks = qs + AF_ROWS * DH + (size_t)warp * KT * (2 * DH + 1);  // this warp's [KT][DH + 1]
+  float* vs = ks + KT * (DH + 1);                                     // this warp's [KT][DH]
   const int g = blockIdx.y, b = blockIdx.z;
-  const int row0 = blockIdx.x * AT_ROWS;
+  const int row0 = blockIdx.x * AF_ROWS;
   const int nrows = a.T * a.G;
   const TT* Q = reinterpret_cast<const TT*>(a.q);
   pdl_trigger();
   pdl_wait();
 
   // queries of this CTA, pre-scaled so that exp2 gives the softmax weights
-  for (int e = threadIdx.x; e < AT_ROWS * DH; e += blockDim.x) {
+  for (int e = threadIdx.x; e < AF_ROWS * DH; e += blockDim.x) {
     const int rr = e / DH, d = e - rr * DH;
     const int r = row0 + rr;
     float v = 0.f;
     if (r < nrows) {
-      const int i = r / a.G, h = g * a.G + (r - (r / a.G) * a.G);
+      const int i = r / a.G, h = g * a.G + (r - i * a.G);
       v = to_f32(Q[(((size_t)b * a.T + i) * a.Hq + h) * DH + d]) * a.qscale;
     }
-    qs[rr][d] = v;
+    qs[e] = v;
   }
+  __syncthreads();
 
-  float m[4], l[4], acc[4][DPL];
+  float m[AF_ROWS], l[AF_ROWS], acc[AF_ROWS][DPL];
 #pragma unroll
-  for (int rr = 0; rr < 4; ++rr) {
+  for (int rr = 0; rr < AF_ROWS; ++rr) {
     m[rr] = -INFINITY;
     l[rr] = 0.f;
 #pragma unroll
@@ -71,45 +79,36 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
   }
 
   const int Lb = seq_len(a.lens, b, a.L, a.Lc, a.ws);
-  const int n_cache_tiles = (Lb + AT_KT - 1) / AT_KT;
-  const int n_tree_tiles = (a.T + AT_KT - 1) / AT_KT;
-  for (int tile = 0; tile < n_cache_tiles + n_tree_tiles; ++tile) {
+  const int n_cache_tiles = (Lb + KT - 1) / KT;
+  const int n_tree_tiles = (a.T + KT - 1) / KT;
+  const int key = lane % KT;  // the key this lane scores (lanes past KT repeat, their scores are dropped)
+  for (int tile = warp; tile < n_cache_tiles + n_tree_tiles; tile += AF_WARPS) {
     const bool is_tree = tile >= n_cache_tiles;
-    const int k0 = is_tree ? (tile - n_cache_tiles) * AT_KT : tile * AT_KT;
-    const int nk = is_tree ? min(AT_KT, a.T - k0) : min(AT_KT, Lb - k0);
-    __syncthreads();
-    for (int e = threadIdx.x; e < AT_KT * DH; e += blockDim.x) {
+    const int k0 = is_tree ? (tile - n_cache_tiles) * KT : tile * KT;
+    const int nk = is_tree ? min(KT, a.T - k0) : min(KT, Lb - k0);
+    __syncwarp();
+    for (int e = lane; e < KT * DH; e += 32) {
       const int j = e / DH, d = e - j * DH;
       float kv = 0.f, vv = 0.f;
       if (j < nk) {
-        if (is_tree) {
-          const size_t o = (((size_t)b * a.T + k0 + j) * a.Hkv + g) * DH + d;
-          kv = to_f32(reinterpret_cast<const TT*>(a.kt)[o]);
-          vv = to_f32(reinterpret_cast<const TT*>(a.vt)[o]);
-        } else {
-          const size_t o = (((size_t)b * a.Lc + k0 + j) * a.Hkv + g) * DH + d;
-          kv = to_f32(reinterpret_cast<const TT*>(a.kc)[o]);
-          vv = to_f32(reinterpret_cast<const TT*>(a.vc)[o]);
-        }
+        const size_t o = is_tree ? (((size_t)b * a.T + k0 + j) * a.Hkv + g) * DH + d
+                                 : (((size_t)b * a.Lc + k0 + j) * a.Hkv + g) * DH + d;
+        kv = to_f32(reinterpret_cast<const TT*>(is_tree ? a.kt : a.kc)[o]);
+        vv = to_f32(reinterpret_cast<const TT*>(is_tree ? a.vt : a.vc)[o]);
       }
-      ks[j][d] = kv;
-      vs[j][d] = vv;
+      ks[j * (DH + 1) + d] = kv;
+      vs[j * DH + d] = vv;
     }
-    if (is_tree && threadIdx.x < AT_ROWS) {
-      const int r = row0 + threadIdx.x;
-      mw[threadIdx.x] = r < nrows ? a.mask[(size_t)(r / a.G) * a.W + (k0 >> 5)] : 0u;
-    }
-    __syncthreads();
-
+    __syncwarp();
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int lr = warp * 4 + rr;
-      if (row0 + lr >= nrows) continue;
+    for (int rr = 0; rr < AF_ROWS; ++rr) {
+      const int r = row0 + rr;
+      if (r >= nrows) break;
       float s = 0.f;
 #pragma unroll 16
-      for (int d = 0; d < DH; ++d) s = fmaf(qs[lr][d], ks[lane][d], s);
-      bool ok = lane < nk;
-      if (is_tree) ok = ok && ((mw[lr] >> lane) & 1u);
+      for (int d = 0; d < DH; ++d) s = fmaf(qs[rr * DH + d], ks[key * (DH + 1) + d], s);
+      bool ok = lane < KT && key < nk;
+      if (is_tree) ok = ok && ((a.mask[(size_t)(r / a.G) * a.W + ((k0 + key) >> 5)] >> ((k0 + key) & 31)) & 1u);
       s = ok ? s : -INFINITY;
       const float mt = warp_max(s);
       if (mt == -INFINITY) continue;  // nothing visible in this tile
@@ -123,21 +122,44 @@ __global__ void __launch_bounds__(256) tree_attn_kernel(AttnArgs a) {
       for (int j = 0; j < nk; ++j) {
         const float pj = __shfl_sync(0xffffffffu, p, j);
 #pragma unroll
-        for (int t = 0; t < DPL; ++t) acc[rr][t] = fmaf(pj, vs[j][lane + 32 * t], acc[rr][t]);
+        for (int t = 0; t < DPL; ++t) acc[rr][t] = fmaf(pj, vs[j * DH + lane + 32 * t], acc[rr][t]);
       }
     }
   }
 
+  // join the warps' states of every row: m* = max m_w,
+  // o = sum_w 2^(m_w - m*) acc_w / sum_w 2^(m_w - m*) l_w
+  __syncthreads();
+  float* pm = qs + AF_ROWS * DH;          // [AF_WARPS][AF_ROWS] (reuses the tiles' space)
+  float* pl = pm + AF_WARPS * AF_ROWS;    // [AF_WARPS][AF_ROWS]
+  float* pa = pl + AF_WARPS * AF_ROWS;    // [AF_WARPS][AF_ROWS][DH]
+#pragma unroll
+  for (int rr = 0; rr < AF_ROWS; ++rr) {
+    if (lane == 0) {
+      pm[warp * AF_ROWS + rr] = m[rr];
+      pl[warp * AF_ROWS + rr] = l[rr];
+    }
+#pragma unroll
+    for (int t = 0; t < DPL; ++t) pa[((size_t)warp * AF_ROWS + rr) * DH + lane + 32 * t] = acc[rr][t];
+  }
+  __syncthreads();
   TT* O = reinterpret_cast<TT*>(a.out);
-#pragma unroll
-  for (int rr = 0; rr < 4; ++rr) {
-    const int r = row0 + warp * 4 + rr;
+  for (int e = threadIdx.x; e < AF_ROWS * DH; e += blockDim.x) {
+    const int rr = e / DH, d = e - rr * DH;
+    const int r = row0 + rr;
     if (r >= nrows) continue;
+    float ms = -INFINITY;
+    for (int w = 0; w < AF_WARPS; ++w) ms = fmaxf(ms, pm[w * AF_ROWS + rr]);
+    float num = 0.f, den = 0.f;
+    for (int w = 0; w < AF_WARPS; ++w) {
+      const float mw = pm[w * AF_ROWS + rr];
+      if (mw == -INFINITY) continue;  // this warp saw no visible key of the row
+      const float f = exp2f(mw - ms);
+      num = fmaf(f, pa[((size_t)w * AF_ROWS + rr) * DH + d], num);
+      den = fmaf(f, pl[w * AF_ROWS + rr], den);
+    }
     const int i = r / a.G, h = g * a.G + (r - i * a.G);
-    const float inv = 1.f / l[rr];
-#pragma unroll
-    for (int t = 0; t < DPL; ++t)
-      O[((size_t)b * a.T + i) * a.H + (size_t)h * DH + lane + 32 * t] = from_f32<TT>(acc[rr][t] * inv);
+    O[((size_t)b * a.T + i) * a.H + (size_t)h * DH + d] = from_f32<TT>(num / den);
   }
 }
 
@@ -167,14 +189,17 @@ int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* v
   a.qscale = 1.4426950408889634f / sqrtf((float)p.Dh);
   a.lens = lens;
   a.ws = ws;
-  dim3 grid((p.T * p.G + AT_ROWS - 1) / AT_ROWS, p.Hkv, p.B);
-  const size_t smem = (size_t)(AT_ROWS * p.Dh + AT_KT * (p.Dh + 1) + AT_KT * p.Dh) * sizeof(float);
+  dim3 grid((p.T * p.G + AF_ROWS - 1) / AF_ROWS, p.Hkv, p.B);
+  // the key tiles' space also holds the warps' final states ([8][16] m and l, [8][16][Dh] o)
+  const size_t tiles = p.Dh == 128 ? af_smem_floats<128>() : af_smem_floats<64>();
+  const size_t join = (size_t)AF_ROWS * p.Dh + 2 * AF_WARPS * AF_ROWS + (size_t)AF_WARPS * AF_ROWS * p.Dh;
+  const size_t smem = (tiles > join ? tiles : join) * sizeof(float);
   void (*k)(AttnArgs);
   if (p.bf16) k = p.Dh == 128 ? tree_attn_kernel<__nv_bfloat16, 128> : tree_attn_kernel<__nv_bfloat16, 64>;
   else k = p.Dh == 128 ? tree_attn_kernel<float, 128> : tree_attn_kernel<float, 64>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_k(k, grid, dim3(256), smem, st, true, a);
+  return (int)launch_k(k, grid, dim3(AF_WARPS * 32), smem, st, true, a);
 }
 
 }  // namespace medusa

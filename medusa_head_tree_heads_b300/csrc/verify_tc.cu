@@ -391,8 +391,9 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
               const bool any = rmin != 0xffffffffu;
               const float t0 = ok0 && any ? (x0 - mj) * a.inv_temp : 0.f;
               const float t1 = ok1 && any ? (x1 - mj) * a.inv_temp : 0.f;
-              const float e0 = ok0 && any ? expf(t0) : 0.f;
-              const float e1 = ok1 && any ? expf(t1) : 0.f;
+              // one hardware exp2 per element (exp2f), t stays in natural units for the sums
+              const float e0 = ok0 && any ? exp2f(t0 * 1.4426950408889634f) : 0.f;
+              const float e1 = ok1 && any ? exp2f(t1 * 1.4426950408889634f) : 0.f;
               zs[j] = e0 + e1;
               ss[j] = e0 * t0 + e1 * t1;
               if ((lane >> 1) == j) {  // this lane ends up holding column j

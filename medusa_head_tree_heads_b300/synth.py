@@ -200,8 +200,8 @@ _add(Shape("sample-sparse-mini", "bf16", 256, 777, 4, 3, (4, 3, 2, 2), 70, 2, 1,
            2014, sparse_nodes=24, temperature=0.3, sample_seed=(7, 11), sample_step=3))
 _add(Shape("7b-sample", "bf16", 4096, 32000, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 128, "sample", ("fixed", 3),
            1007, full_size=True))
-# typical acceptance whose bonus token is drawn (the GQA reduced shapes)
-_add(Shape("typical-sample-mini", "bf16", 512, 4099, 4, 2, (4, 3, 2, 2), 257, 4, 2, 128, "typical-sample",
+# typical acceptance whose bonus token is drawn (the GQA reduced shapes; 4 x 89 nodes take two node tiles)
+_add(Shape("typical-sample-mini", "bf16", 512, 4099, 4, 4, (4, 3, 2, 2), 257, 4, 2, 128, "typical-sample",
            ("uniform", 0, 4), 2015, kv_capacity=260, sample_seed=(21, 22), sample_step=5))
 # profiling case: the 7B shapes with a quarter-sized vocabulary (still far
 # larger than L2) so that counter replays stay small
@@ -210,6 +210,9 @@ _add(Shape("7b-prof", "bf16", 4096, 8192, 5, 1, (4, 3, 2, 2, 1), 1024, 32, 32, 1
 # profiling case of the tensor-bound verification: the GQA workload's batch,
 # tree and widths with a 32000-row vocabulary (lm_head 262 MB, still past L2)
 _add(Shape("gqa-prof", "bf16", 4096, 32000, 4, 16, (4, 3, 2, 2), 1024, 32, 8, 128, "typical", ("uniform", 0, 4), 4002,
+           full_size=True))
+# profiling case of the tensor-bound attention: the 33B workload with 4 sequences
+_add(Shape("33b-prof", "bf16", 6656, 32000, 5, 4, (4, 3, 2, 2, 2), 8192, 52, 52, 128, "greedy", ("uniform", 0, 5), 4003,
            full_size=True))
 # edge cases: a chain tree (the mask is causal), a root-only tree, an empty
 # cache, the widest tree under the 512-node limit, and the deepest tree
