@@ -17,8 +17,8 @@
 // (one per SM):
 //   warp 0      TMA producer (one thread), S-stage smem ring
 //   warp 1      TMEM allocator + MMA issuer (one thread)
-//   warps 2..9  epilogue (two per TMEM lane quadrant, columns split in
-//               groups of 64): tcgen05.ld 16 columns at a time; per column
+//   warps 2..    epilogue (two or four per TMEM lane quadrant by mode,
+//               columns split in groups of 64): tcgen05.ld 16 columns at a time; per column
 //               the max over the warp's rows and the lowest row reaching it
 //               (redux.sync on an order-preserving integer key); typical
 //               acceptance adds one exponential per element against that
@@ -43,8 +43,12 @@ namespace medusa {
 constexpr int VT_M = 128;       // vocab rows per MMA (M)
 constexpr int VT_SUB = 2;       // MMA halves per tile: a tile is VT_SUB * VT_M vocab rows
 constexpr int VT_BK = 64;       // K elements per stage (128 bytes of bf16)
-constexpr int VT_EPI_WARPS = 8;  // two warps per TMEM lane quadrant, each taking half the columns
-constexpr int VT_THREADS = 64 + 32 * VT_EPI_WARPS;
+// Epilogue warps per mode: 16 for greedy (four per TMEM lane quadrant, each
+// a quarter of the columns: 33B step 4547 -> 4426 us, the 7B step unchanged),
+// 8 for the typical and sampling epilogues (two per quadrant; with 16 they
+// measured no faster and the sampling epilogue spilled registers).
+__host__ __device__ constexpr int vt_epi_warps(int mode) { return mode == 0 ? 16 : 8; }
+__host__ __device__ constexpr int vt_threads(int mode) { return 64 + 32 * vt_epi_warps(mode); }
 constexpr uint32_t VT_TMEM_COLS = 512;
 constexpr uint64_t VT_WAIT_NS = 20ull * 1000 * 1000;  // 20 ms per wait
 
@@ -172,7 +176,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // MODE: 0 greedy, 1 typical, 2 sample, 3 typical with a sampled bonus (a
 // compile-time choice, so each instance carries only its own epilogue)
 template <int MODE>
-__global__ void __launch_bounds__(VT_THREADS, 1)
+__global__ void __launch_bounds__(vt_threads(MODE), 1)
     verify_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ VtcArgs a) {
   extern __shared__ uint8_t vt_smem_raw[];
@@ -194,6 +198,8 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr bool typical = MODE == 1 || MODE == 3;
+  constexpr int VT_EPI_WARPS = vt_epi_warps(MODE);
+  constexpr int VT_EPI_GROUPS = VT_EPI_WARPS / 4;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -322,12 +328,13 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       const uint32_t aph = tl & 1u;
       // one thread waits, the named barrier hands its verdict to all 128
       if (etid == 0) *ep_ok = wait_or_abort(&tfull[0], aph, abort_flag, a.ws) ? 1 : 0;
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * VT_EPI_WARPS) : "memory");
       if (!*ep_ok) break;
       tc::fence_after_sync();
-      // warps 2..5 take the even groups of 4 chunks, warps 6..9 the odd ones
-      const int half = (warp - 2) >> 2;
-      for (int ch0 = 4 * half; ch0 < a.BN / 16; ch0 += 8) {
+      // group g of the quadrant's warps (warps 2 + 4g .. 5 + 4g) takes every
+      // VT_EPI_GROUPS-th group of 4 chunks of 16 columns, starting at group g
+      const int grp = (warp - 2) >> 2;
+      for (int ch0 = 4 * grp; ch0 < a.BN / 16; ch0 += 4 * VT_EPI_GROUPS) {
         const int nch = min(4, a.BN / 16 - ch0);
         if constexpr (typical) {
           // typical: per column the max and argmax as in greedy (redux),
@@ -501,7 +508,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[0]);  // this warp is done with the accumulators
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * VT_EPI_WARPS) : "memory");
       for (int col = etid; col < a.BN; col += 32 * VT_EPI_WARPS) {
         const int n = nt * a.BN + col;
         if (n < a.N) {
@@ -518,7 +525,7 @@ __global__ void __launch_bounds__(VT_THREADS, 1)
           }
         }
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * VT_EPI_WARPS) : "memory");
     }
   }
 
@@ -769,7 +776,8 @@ int launch_verify_tc(const Plan& p, const void* attn_out, const void* lm_head, c
   cudaError_t ce = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ce != cudaSuccess) return (int)ce;
   const int grid = a.n_tiles < p.sm_count ? a.n_tiles : p.sm_count;
-  ce = launch_k(kern, dim3(grid), dim3(VT_THREADS), smem, st, true, tA, tB, a);
+  const int mode = p.sample_bonus ? 3 : (a.typical ? 1 : (a.sample ? 2 : 0));
+  ce = launch_k(kern, dim3(grid), dim3(vt_threads(mode)), smem, st, true, tA, tB, a);
   if (ce != cudaSuccess || part == VERIFY_GEMM) return (int)ce;
   if (a.typical) return (int)launch_k(verify_merge_kernel<true>, dim3(mgrid), dim3(256), 0, st, true, a);
   return (int)launch_k(verify_merge_kernel<false>, dim3(mgrid), dim3(256), 0, st, true, a);

@@ -226,7 +226,11 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     U.compare_step(s, res, ref)
 
 
-def _sample_nodes(s, plan, b, rng, extra=4):
+def _sample_nodes(s, plan, b, rng, extra=8):
+    """Every node of the first sequence; elsewhere the planted nodes and
+    `extra` seeded random ones."""
+    if b == 0:
+        return list(range(s.n_nodes))
     planted = [p[0] for p in plan["seqs"][b]["plant"]]
     rand = rng.choice(s.n_nodes, size=min(extra, s.n_nodes), replace=False).tolist()
     return sorted(set(planted) | set(rand))
