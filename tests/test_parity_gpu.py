@@ -290,17 +290,26 @@ def test_full_size_sampled(name, schedule):
             if i in planted or g == r:
                 assert g == r, (b, i)
             else:  # an unplanted node: the GPU's choice must tie the best within rounding
-                lg = float(o_st[j] @ O.decode(lm[g]))
-                # the bound scales with the best score; a sampled score adds
-                # Gumbel noise of order 1, so its best can sit near 0 while the
-                # rounding of the logit part does not shrink with it: there the
-                # scale is at least 1
+                wg, wr = O.decode(lm[g]), O.decode(lm[r])
+                lg = float(o_st[j] @ wg)
+                # Two sources of difference.  (1) The GPU scores its own stored
+                # attention output, which differs from the oracle's by the
+                # attention's rounding (checked above within its tolerance):
+                # a logit moves by at most |w| |o_gpu - o_oracle|, so the
+                # oracle's score of the GPU's choice may trail the best by
+                # (|w_g| + |w_r|) |o_gpu - o_oracle|.  (2) Accumulation
+                # rounding, bounded relative to the best score's magnitude
+                # (at least 1 for sampled scores: the Gumbel noise of order 1
+                # can put the best near 0 while the rounding of the logit
+                # part does not shrink with it).
+                drift = (np.linalg.norm(wg) + np.linalg.norm(wr)) * float(np.linalg.norm(got[j] - o_st[j]))
                 scale = abs(st["maxlogit"][j])
                 if sample:
                     lg = lg / s.temperature + float(O.gumbel_noise(s.sample_seed, s.sample_step, ids[j],
                                                                    s.vocab)[g])
+                    drift /= s.temperature
                     scale = max(1.0, scale)
-                assert st["maxlogit"][j] - lg <= 2e-3 * scale, (b, i, g, r)
+                assert st["maxlogit"][j] - lg <= 2e-3 * scale + drift, (b, i, g, r)
         if typical:
             U.assert_close(res["node_lse"][b, nodes].numpy(), st["lse"], s.dtype, "lse")
             U.assert_close(res["node_entropy"][b, nodes].numpy(), st["entropy"], s.dtype, "entropy")
