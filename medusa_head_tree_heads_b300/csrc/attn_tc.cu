@@ -51,6 +51,7 @@ constexpr uint32_t AT_KVCHUNK = AT_BK * 128;      // 8 KB: 64 keys x 64 dh
 constexpr uint32_t AT_KVTILE = 2 * AT_KVCHUNK;    // K or V: [64 keys][128 dh]
 constexpr uint32_t AT_TMEM_COLS = 512;            // per tile: S0, S1 (64 columns each; P over the first 32); then O of each tile (128)
 constexpr uint64_t AT_WAIT_NS = 20ull * 1000 * 1000;
+constexpr uint32_t AT_SLEEP_NS = 1000 * 1000;     // a waiting thread sleeps until its phase completes (<= 1 ms per poll)
 constexpr float AT_RESCALE_LOG2 = 8.f;            // raise the running max only past 2^8 growth
 
 struct AtArgs {
@@ -81,7 +82,7 @@ __device__ __forceinline__ uint32_t at_sw(int r, int unit) {  // byte offset of 
 __device__ __forceinline__ bool at_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint8_t* ws) {
   if (tc::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = tc::globaltimer_ns();
-  while (!tc::mbar_try_wait(bar, parity)) {
+  while (!tc::mbar_try_wait_sleep(bar, parity, AT_SLEEP_NS)) {
     if (*abort_flag) return false;
     if (tc::globaltimer_ns() - t0 > AT_WAIT_NS) {
       set_error(ws, MEDUSA_ERR_TIMEOUT);
@@ -108,6 +109,32 @@ __device__ __forceinline__ float at_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max of three (one instruction on sm_100 and later)
+__device__ __forceinline__ float at_max3(float x, float y, float z) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(x), "f"(y), "f"(z));
+  return d;
+}
+
+// (y0, y1) = (x0, x1) * s + c as one paired fp32 FMA (each lane rounds like fmaf)
+__device__ __forceinline__ void at_fma2(float& y0, float& y1, float x0, float x1, float s, float c) {
+  uint64_t x, sv, cv, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(sv) : "f"(s), "f"(s));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(cv) : "f"(c), "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(x), "l"(sv), "l"(cv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(y));
+}
+
+// (a0, a1) += (x0, x1) as one paired fp32 add
+__device__ __forceinline__ void at_add2(float& a0, float& a1, float x0, float x1) {
+  uint64_t av, xv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(av) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(xv) : "f"(x0), "f"(x1));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(av) : "l"(xv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(av));
 }
 
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
@@ -347,24 +374,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // the row's 64 scores into registers; the S buffer is released at once
       float v[AT_BK];
       if (warp_live) {
-        float v0[16], v1[16], v2[16], v3[16];
+        float(&va)[32] = *reinterpret_cast<float(*)[32]>(&v[0]);
+        float(&vb)[32] = *reinterpret_cast<float(*)[32]>(&v[32]);
         const uint32_t sb = sbase + buf * AT_BK;
-        tc::tmem_ld16_nowait(sb, v0);
-        tc::tmem_ld16_nowait(sb + 16, v1);
-        tc::tmem_ld16_nowait(sb + 32, v2);
-        tc::tmem_ld16_nowait(sb + 48, v3);
+        tc::tmem_ld32_nowait(sb, va);
+        tc::tmem_ld32_nowait(sb + 32, vb);
         tc::tmem_wait_ld();
-        tc::tmem_regs_ready(v0);
-        tc::tmem_regs_ready(v1);
-        tc::tmem_regs_ready(v2);
-        tc::tmem_regs_ready(v3);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          v[j] = v0[j];
-          v[16 + j] = v1[j];
-          v[32 + j] = v2[j];
-          v[48 + j] = v3[j];
-        }
+        tc::tmem_regs_ready32(va);
+        tc::tmem_regs_ready32(vb);
       }
       if (!warp_live) {  // no real row: nothing to compute, the handshake goes on
         __syncwarp();
@@ -382,14 +399,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           v[kk] = vis ? v[kk] : -INFINITY;
         }
       }
-      float tm[AT_BK / 2];
+      // row max of the block: a tree of three-input maxima (21 + 7 + 4)
+      static_assert(AT_BK == 64, "the max tree below is written for 64 keys");
+      float m1[22], m2[8];
 #pragma unroll
-      for (int j = 0; j < AT_BK / 2; ++j) tm[j] = fmaxf(v[2 * j], v[2 * j + 1]);
+      for (int j = 0; j < 21; ++j) m1[j] = at_max3(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+      m1[21] = v[63];
 #pragma unroll
-      for (int w = AT_BK / 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int j = 0; j < w; ++j) tm[j] = fmaxf(tm[j], tm[j + w]);
-      const float mx = tm[0] * a.qscale;  // the scale is positive; -inf stays -inf
+      for (int j = 0; j < 7; ++j) m2[j] = at_max3(m1[3 * j], m1[3 * j + 1], m1[3 * j + 2]);
+      m2[7] = m1[21];
+      const float bmax = at_max3(at_max3(m2[0], m2[1], m2[2]), at_max3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+      const float mx = bmax * a.qscale;  // the scale is positive; -inf stays -inf
       {
         const bool raise = mx > m + AT_RESCALE_LOG2 || (m == -INFINITY && mx > -INFINITY);
         const float mn = raise ? mx : m;
@@ -418,18 +438,22 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // P = exp2(s * scale - m) (a -inf score gives 0) as bf16 pairs (the
       // even key in the low half) over the first 32 columns of S(i) in TMEM
       const float nm = (m == -INFINITY) ? 0.f : -m;
-      float ls = 0.f;
-      float pk[2][16];
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      uint32_t pk[AT_BK / 2];
 #pragma unroll
-      for (int j = 0; j < AT_BK; j += 2) {
-        const float p0 = at_exp2(fmaf(v[j], a.qscale, nm)), p1 = at_exp2(fmaf(v[j + 1], a.qscale, nm));
-        ls += p0 + p1;
-        pk[j >> 5][(j >> 1) & 15] = __uint_as_float(pack2_bf16(p0, p1));
+      for (int j = 0; j < AT_BK; j += 4) {  // paired FMAs and adds around the exponentials
+        float x0, x1, x2, x3;
+        at_fma2(x0, x1, v[j], v[j + 1], a.qscale, nm);
+        at_fma2(x2, x3, v[j + 2], v[j + 3], a.qscale, nm);
+        const float p0 = at_exp2(x0), p1 = at_exp2(x1), p2 = at_exp2(x2), p3 = at_exp2(x3);
+        at_add2(s0, s1, p0, p1);
+        at_add2(s2, s3, p2, p3);
+        pk[j >> 1] = pack2_bf16(p0, p1);
+        pk[(j >> 1) + 1] = pack2_bf16(p2, p3);
       }
-      tc::tmem_st16(sbase + buf * AT_BK, pk[0]);
-      tc::tmem_st16(sbase + buf * AT_BK + 16, pk[1]);
+      tc::tmem_st32_nowait(sbase + buf * AT_BK, pk);
       tc::tmem_wait_st();
-      l += ls;
+      l += (s0 + s1) + (s2 + s3);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&p_full[2 * t + buf]);

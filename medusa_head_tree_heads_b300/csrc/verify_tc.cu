@@ -20,11 +20,11 @@
 //   warps 2..    epilogue (two or four per TMEM lane quadrant by mode,
 //               columns split in groups of 64): tcgen05.ld 16 columns at a time; per column
 //               the max over the warp's rows and the lowest row reaching it
-//               (redux.sync on an order-preserving integer key); typical
-//               acceptance adds one exponential per element against that
-//               max and a "transpose-reduce" of (sum e, sum e*t) across the
-//               lanes (each exchange round halves the columns a lane carries:
-//               16 rounds per 16 columns instead of 5 per column).  The warps
+//               by a "transpose-reduce" across the lanes (each exchange
+//               round halves the columns a lane carries: 15 pair exchanges
+//               per 16 columns instead of 5 dependent rounds per column);
+//               typical acceptance adds one exponential per element against
+//               that max and the same reduction of (sum e, sum e*t).  The warps
 //               combine in shared memory and write one partial (max, sum e,
 //               sum e*t, argmax) per (vocab tile, node).
 // A second small kernel merges the vocab-tile partials, one warp per node;
@@ -122,6 +122,37 @@ __device__ __forceinline__ Soft soft_join(const Soft& a, const Soft& b, bool typ
     r.s = 0.f;
   }
   return r;
+}
+
+// Best (value, id) of 16 columns over the warp's 32 lanes, each lane starting
+// from its own best of the column: four exchange rounds that each hand half
+// of the carried columns to the partner lane (8 + 4 + 2 + 1 pairs sent
+// instead of 5 dependent rounds per column), then one round within the lane
+// pair.  Lane l ends with column l >> 1 in bv[0], bi[0] (lanes l and l ^ 1
+// agree).  Ties go to the lower id, so the result does not depend on the
+// order of the merges.
+__device__ __forceinline__ void best_transpose16(float (&bv)[16], int (&bi)[16], int lane) {
+#pragma unroll
+  for (int step = 0; step < 4; ++step) {
+    const int o = 16 >> step, hh = 8 >> step;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < hh; ++k) {
+      const float sv = up ? bv[k] : bv[k + hh], kv = up ? bv[k + hh] : bv[k];
+      const int si = up ? bi[k] : bi[k + hh], ki = up ? bi[k + hh] : bi[k];
+      const float rv = __shfl_xor_sync(0xffffffffu, sv, o);
+      const int ri = __shfl_xor_sync(0xffffffffu, si, o);
+      const bool take = better(rv, ri, kv, ki);
+      bv[k] = take ? rv : kv;
+      bi[k] = take ? ri : ki;
+    }
+  }
+  const float rv = __shfl_xor_sync(0xffffffffu, bv[0], 1);
+  const int ri = __shfl_xor_sync(0xffffffffu, bi[0], 1);
+  if (better(rv, ri, bv[0], bi[0])) {
+    bv[0] = rv;
+    bi[0] = ri;
+  }
 }
 
 __device__ __forceinline__ Soft shfl_soft(const Soft& a, int o) {
@@ -337,9 +368,9 @@ __global__ void __launch_bounds__(vt_threads(MODE), 1)
       for (int ch0 = 4 * grp; ch0 < a.BN / 16; ch0 += 4 * VT_EPI_GROUPS) {
         const int nch = min(4, a.BN / 16 - ch0);
         if constexpr (typical) {
-          // typical: per column the max and argmax as in greedy (redux),
-          // then one exponential per element against that max and a plain
-          // additive transpose-reduce of (sum e, sum e*t) over the 64 rows
+          // typical: per column the max and argmax as in greedy, then one
+          // exponential per element against that max and a plain additive
+          // transpose-reduce of (sum e, sum e*t) over the 64 rows
           const int row0 = vt * VT_SUB * VT_M + q * 32 + lane;  // half 1 adds VT_M
           const bool ok0 = row0 < a.V, ok1 = row0 + VT_M < a.V;
 #pragma unroll 1
@@ -351,16 +382,20 @@ __global__ void __launch_bounds__(vt_threads(MODE), 1)
             tc::tmem_wait_ld();
 #pragma unroll
             for (int h = 0; h < VT_SUB; ++h) tc::tmem_regs_ready(v[h]);
-            float zs[16], ss[16];
-            float my_m = -INFINITY;
-            int my_i = INT_MAX;
-            float dr_m = -INFINITY;  // MODE 3: this lane's column (lane < 16) of the draw
-            int dr_i = INT_MAX;
+            // the column maxima and their rows first (transpose-reduce of
+            // each lane's better row), then every lane fetches the 16 maxima
+            float bv[16];
+            int bi[16];
+            float dv[16];  // MODE 3: the perturbed scores of the draw
             uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+            int di[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float x0 = ok0 ? v[0][j] : -INFINITY;
               const float x1 = ok1 ? v[1][j] : -INFINITY;
+              const bool one = x1 > x0;  // equal values keep half 0 (the lower row)
+              bv[j] = one ? x1 : x0;
+              bi[j] = ok0 ? a.id_off + (one ? row0 + VT_M : row0) : INT_MAX;
               if constexpr (MODE == 3) {
                 // the bonus draw: s / temperature + Gumbel noise, keyed as in the
                 // sampling mode (one Philox call per row and 4 node columns)
@@ -376,26 +411,21 @@ __global__ void __launch_bounds__(vt_threads(MODE), 1)
                 const float y0 = ok0 ? x0 * a.inv_temp + gumbel24(u0) : -INFINITY;
                 const float y1 = ok1 ? x1 * a.inv_temp + gumbel24(u1) : -INFINITY;
                 const bool one_d = y1 > y0;
-                const int dkey = order_key(one_d ? y1 : y0);
-                int dmax;
-                asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(dmax) : "r"(dkey));
-                const uint32_t dr = ok0 ? (uint32_t)(a.id_off + (one_d ? row0 + VT_M : row0)) : 0xffffffffu;
-                uint32_t drmin;
-                asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(drmin) : "r"(dkey == dmax ? dr : 0xffffffffu));
-                if (lane == j && drmin != 0xffffffffu) {
-                  dr_m = order_key_inv(dmax);
-                  dr_i = (int)drmin;
-                }
+                dv[j] = one_d ? y1 : y0;
+                di[j] = ok0 ? a.id_off + (one_d ? row0 + VT_M : row0) : INT_MAX;
               }
-              const bool one = x1 > x0;  // equal values keep half 0 (the lower row)
-              const int key = order_key(one ? x1 : x0);
-              int kmax;
-              asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(kmax) : "r"(key));
-              const uint32_t r = ok0 ? (uint32_t)(a.id_off + (one ? row0 + VT_M : row0)) : 0xffffffffu;
-              uint32_t rmin;
-              asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(rmin) : "r"(key == kmax ? r : 0xffffffffu));
-              const float mj = order_key_inv(kmax);
-              const bool any = rmin != 0xffffffffu;
+            }
+            best_transpose16(bv, bi, lane);
+            if constexpr (MODE == 3) best_transpose16(dv, di, lane);
+            const float colm = bv[0];  // column lane >> 1: max (-inf if no row is real) and its row
+            const int coli = bi[0];
+            float zs[16], ss[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float mj = __shfl_sync(0xffffffffu, colm, 2 * j);
+              const bool any = mj > -INFINITY;
+              const float x0 = ok0 ? v[0][j] : -INFINITY;
+              const float x1 = ok1 ? v[1][j] : -INFINITY;
               const float t0 = ok0 && any ? (x0 - mj) * a.inv_temp : 0.f;
               const float t1 = ok1 && any ? (x1 - mj) * a.inv_temp : 0.f;
               // one hardware exp2 per element (exp2f), t stays in natural units for the sums
@@ -403,10 +433,6 @@ __global__ void __launch_bounds__(vt_threads(MODE), 1)
               const float e1 = ok1 && any ? exp2f(t1 * 1.4426950408889634f) : 0.f;
               zs[j] = e0 + e1;
               ss[j] = e0 * t0 + e1 * t1;
-              if ((lane >> 1) == j) {  // this lane ends up holding column j
-                my_m = any ? mj : -INFINITY;
-                my_i = any ? (int)rmin : INT_MAX;
-              }
             }
             // after the four halving rounds lane l holds column l >> 1
 #pragma unroll
@@ -425,19 +451,17 @@ __global__ void __launch_bounds__(vt_threads(MODE), 1)
             ss[0] += __shfl_xor_sync(0xffffffffu, ss[0], 1);
             if ((lane & 1) == 0) {
               Soft o;
-              o.m = my_m;
-              o.i = my_i;
-              o.z = my_i == INT_MAX ? 0.f : zs[0];
-              o.s = my_i == INT_MAX ? 0.f : ss[0];
+              o.m = colm;
+              o.i = coli;
+              o.z = coli == INT_MAX ? 0.f : zs[0];
+              o.s = coli == INT_MAX ? 0.f : ss[0];
               red[q * a.BN + (ch0 + c) * 16 + (lane >> 1)] = o;
+              if constexpr (MODE == 3) red2[q * a.BN + (ch0 + c) * 16 + (lane >> 1)] = make_float2(dv[0], __int_as_float(di[0]));
             }
-            if (MODE == 3 && lane < 16) red2[q * a.BN + (ch0 + c) * 16 + lane] = make_float2(dr_m, __int_as_float(dr_i));
           }
         } else {
-          // greedy: per column, the best of this thread's two rows, then a
-          // warp max of an order-preserving integer key and a warp min of the
-          // rows that reach it (ties to the lowest row), both single
-          // instructions (redux.sync)
+          // greedy: per column, the best of this thread's two rows, then the
+          // warp's best by a transpose-reduce (ties to the lowest row)
           const int row0 = vt * VT_SUB * VT_M + q * 32 + lane;  // half 1 adds VT_M
           const bool ok0 = row0 < a.V, ok1 = row0 + VT_M < a.V;
 #pragma unroll
@@ -480,27 +504,23 @@ __global__ void __launch_bounds__(vt_threads(MODE), 1)
                   }
                 }
               }
+              float bv[16];
+              int bi[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const float x0 = ok0 ? v[0][c][j] : -INFINITY;
                 const float x1 = ok1 ? v[1][c][j] : -INFINITY;
                 const bool one = x1 > x0;  // equal values keep half 0 (the lower row)
-                const float x = one ? x1 : x0;
-                const uint32_t r = ok0 ? (uint32_t)(a.id_off + (one ? row0 + VT_M : row0)) : 0xffffffffu;
-                const int key = order_key(x);
-                int kmax;
-                asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(kmax) : "r"(key));
-                uint32_t rmin;
-                asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;"
-                             : "=r"(rmin)
-                             : "r"(key == kmax ? r : 0xffffffffu));
-                if (lane == j && rmin != 0xffffffffu) {
-                  mine.m = order_key_inv(kmax);
-                  mine.i = (int)rmin;
-                  mine.z = 1.f;
-                }
+                bv[j] = one ? x1 : x0;
+                bi[j] = ok0 ? a.id_off + (one ? row0 + VT_M : row0) : INT_MAX;
               }
-              if (lane < 16) red[q * a.BN + (ch0 + cp + c) * 16 + lane] = mine;
+              best_transpose16(bv, bi, lane);
+              if (bi[0] != INT_MAX) {
+                mine.m = bv[0];
+                mine.i = bi[0];
+                mine.z = 1.f;
+              }
+              if ((lane & 1) == 0) red[q * a.BN + (ch0 + cp + c) * 16 + (lane >> 1)] = mine;
             }
           }
         }

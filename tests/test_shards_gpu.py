@@ -73,3 +73,14 @@ def test_misordered_shards_set_the_device_error():
     steps[0].finish(io)
     torch.cuda.synchronize()
     assert M.medusa_get_device_error(steps[0].ws) == -5
+
+
+@pytest.mark.parametrize("name,S", [("7b-bf16", 2), ("gqa76-bf16", 4)])
+def test_sharded_full_size_matches_the_oracle(name, S):
+    """Full size, ragged shards: compared with the oracle the way the fused
+    full-size step is (heads, top-k, tree everywhere; planted acceptance bit
+    for bit; attention and the base model's choice on sampled nodes)."""
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for the gpu-marked tests")
+    s, inp, res = sharded_run(name, S)
+    U.compare_full_size(s, inp, res)

@@ -130,3 +130,90 @@ def compare_step(s, res: Dict, ref: Dict, check_all_nodes: bool = True) -> None:
         assert res["acc_nodes"][b, :n + 1].tolist() == ref["acc_nodes"][b], ("acc_nodes", b)
         assert (res["acc_nodes"][b, n + 1:] == -1).all()
         assert int(res["bonus"][b]) == ref["bonus"][b], ("bonus", b)
+
+
+def _sample_nodes(s, plan, b, rng, extra=8):
+    """Every node of the first sequence; elsewhere the planted nodes and
+    `extra` seeded random ones."""
+    if b == 0:
+        return list(range(s.n_nodes))
+    planted = [p[0] for p in plan["seqs"][b]["plant"]]
+    rand = rng.choice(s.n_nodes, size=min(extra, s.n_nodes), replace=False).tolist()
+    return sorted(set(planted) | set(rand))
+
+
+def compare_full_size(s, inp: Dict, res: Dict) -> None:
+    """A full-size step against the oracle: heads, top-k and tree everywhere;
+    the planted acceptance bit for bit; attention output and the base model's
+    choice on sampled nodes (an unplanted node's choice may trail the oracle's
+    best only by what rounding and the stored attention output allow)."""
+    from oracle import medusa_oracle as O
+    plan = plans()[s.name]
+    n = np_inputs(inp)
+    # heads and top-k: every sequence, every head
+    z = O.head_hidden(n["h"], n["W1"], n["b1"])
+    idx, val = O.topk_lists(O.head_logits(z, n["W2"]), list(s.topk))
+    np.testing.assert_array_equal(res["topk_idx"].numpy(), idx)
+    live = idx >= 0
+    assert_close(res["topk_val"].numpy()[live], val[live], s.dtype, "topk_val")
+    # the tree: everything
+    tree = O.Tree.for_shape(s)
+    np.testing.assert_array_equal(res["tree"]["token"].numpy(), tree.tokens(idx, n["root_token"]))
+    np.testing.assert_array_equal(res["tree"]["parent"].numpy(), tree.parent)
+    np.testing.assert_array_equal(res["tree"]["mask"].numpy().view(np.uint32), pack_mask(tree.mask))
+    np.testing.assert_array_equal(res["tree"]["paths"].numpy(), tree.paths)
+    # acceptance: the planted result, bit-exact
+    for b, sq in enumerate(plan["seqs"]):
+        assert int(res["accept_len"][b]) == sq["depth"], b
+        assert res["acc_tokens"][b, :sq["depth"]].tolist() == sq["tokens"], b
+        assert res["acc_nodes"][b, :sq["depth"] + 1].tolist() == sq["nodes"], b
+        assert int(res["bonus"][b]) == sq["bonus"], b
+    # sampled nodes: attention output and the base model's choice
+    rng = np.random.default_rng(s.seed)
+    bs = sorted({0, s.batch - 1} | set(rng.choice(s.batch, size=min(2, s.batch), replace=False).tolist()))
+    typical = s.accept == "typical"
+    for b in bs:
+        nodes = _sample_nodes(s, plan, b, rng)
+        o = O.tree_attention(n["q"], n["k_tree"], n["v_tree"], n["k_cache"], n["v_cache"], s.kv_len, tree.mask,
+                             nodes=nodes, batches=[b])
+        o_st = O.round_to_storage(o[b, nodes], s.dtype)
+        got = res["attn_out"][b, nodes].float().numpy()
+        assert_close(got, o_st, s.dtype, f"attn_out b={b}")
+        sample = s.accept == "sample"
+        ids = [b * s.n_nodes + i for i in nodes]
+        if sample:
+            st = O.sample_stats(o_st, n["lm_head"], s.temperature, s.sample_seed, s.sample_step, node_ids=ids)
+        else:
+            st = O.verify_stats(o_st, n["lm_head"], s.temperature if typical else None)
+        assert_close(res["node_maxlogit"][b, nodes].numpy(), st["maxlogit"], s.dtype, "maxlogit")
+        planted = {p[0] for p in plan["seqs"][b]["plant"]}
+        lm = n["lm_head"]
+        for j, i in enumerate(nodes):
+            g = int(res["node_argmax"][b, i])
+            r = int(st["argmax"][j])
+            if i in planted or g == r:
+                assert g == r, (b, i)
+            else:  # an unplanted node: the GPU's choice must tie the best within rounding
+                wg, wr = O.decode(lm[g]), O.decode(lm[r])
+                lg = float(o_st[j] @ wg)
+                # Two sources of difference.  (1) The GPU scores its own stored
+                # attention output, which differs from the oracle's by the
+                # attention's rounding (checked above within its tolerance):
+                # a logit moves by at most |w| |o_gpu - o_oracle|, so the
+                # oracle's score of the GPU's choice may trail the best by
+                # (|w_g| + |w_r|) |o_gpu - o_oracle|.  (2) Accumulation
+                # rounding, bounded relative to the best score's magnitude
+                # (at least 1 for sampled scores: the Gumbel noise of order 1
+                # can put the best near 0 while the rounding of the logit
+                # part does not shrink with it).
+                drift = (np.linalg.norm(wg) + np.linalg.norm(wr)) * float(np.linalg.norm(got[j] - o_st[j]))
+                scale = abs(st["maxlogit"][j])
+                if sample:
+                    lg = lg / s.temperature + float(O.gumbel_noise(s.sample_seed, s.sample_step, ids[j],
+                                                                   s.vocab)[g])
+                    drift /= s.temperature
+                    scale = max(1.0, scale)
+                assert st["maxlogit"][j] - lg <= 2e-3 * scale + drift, (b, i, g, r)
+        if typical:
+            assert_close(res["node_lse"][b, nodes].numpy(), st["lse"], s.dtype, "lse")
+            assert_close(res["node_entropy"][b, nodes].numpy(), st["entropy"], s.dtype, "entropy")
