@@ -8,7 +8,7 @@
 //   o = sum_j softmax_j(q . k_j / sqrt(Dh)) v_j,
 //   j over cache rows [0, L) and tree nodes j with bit j of the node's mask row.
 //
-// CUDA-core version: a CTA owns up to 16 query rows of one (b, g); its 8
+// CUDA-core version: a CTA owns up to 16 query rows (4 for small grids) of one (b, g); its 8
 // warps split the group's keys (cache tiles, then tree tiles masked by the
 // rows' mask words) between them, tile w, w + 8, ... for warp w, each warp
 // keeping an fp32 online softmax per row over its own tiles in registers and
@@ -21,6 +21,7 @@
 namespace medusa {
 
 constexpr int AF_ROWS = 16;   // query rows per CTA
+constexpr int AF_ROWS_FEW = 4;  // ... when 16 would leave most SMs idle
 constexpr int AF_WARPS = 8;
 
 struct AttnArgs {
@@ -35,29 +36,29 @@ struct AttnArgs {
 
 template <int DH>
 constexpr int af_keys() { return DH == 64 ? 32 : 16; }
-template <int DH>
+template <int DH, int ROWS>
 constexpr size_t af_smem_floats() {  // queries + per warp one K tile (padded rows) and one V tile
-  return (size_t)AF_ROWS * DH + (size_t)AF_WARPS * af_keys<DH>() * (2 * DH + 1);
+  return (size_t)ROWS * DH + (size_t)AF_WARPS * af_keys<DH>() * (2 * DH + 1);
 }
 
-template <typename TT, int DH>
+template <typename TT, int DH, int ROWS>
 __global__ void __launch_bounds__(AF_WARPS * 32) tree_attn_kernel(AttnArgs a) {
   constexpr int DPL = DH / 32;      // output dims per lane
   constexpr int KT = af_keys<DH>();  // keys per tile
   extern __shared__ float4 at_smem[];
-  float* qs = reinterpret_cast<float*>(at_smem);  // [AF_ROWS][DH]
+  float* qs = reinterpret_cast<float*>(at_smem);  // [ROWS][DH]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* ks = qs + AF_ROWS * DH + (size_t)warp * KT * (2 * DH + 1);  // this warp's [KT][DH + 1]
+  float* ks = qs + ROWS * DH + (size_t)warp * KT * (2 * DH + 1);  // this warp's [KT][DH + 1]
   float* vs = ks + KT * (DH + 1);                                     // this warp's [KT][DH]
   const int g = blockIdx.y, b = blockIdx.z;
-  const int row0 = blockIdx.x * AF_ROWS;
+  const int row0 = blockIdx.x * ROWS;
   const int nrows = a.T * a.G;
   const TT* Q = reinterpret_cast<const TT*>(a.q);
   pdl_trigger();
   pdl_wait();
 
   // queries of this CTA, pre-scaled so that exp2 gives the softmax weights
-  for (int e = threadIdx.x; e < AF_ROWS * DH; e += blockDim.x) {
+  for (int e = threadIdx.x; e < ROWS * DH; e += blockDim.x) {
     const int rr = e / DH, d = e - rr * DH;
     const int r = row0 + rr;
     float v = 0.f;
@@ -69,9 +70,9 @@ __global__ void __launch_bounds__(AF_WARPS * 32) tree_attn_kernel(AttnArgs a) {
   }
   __syncthreads();
 
-  float m[AF_ROWS], l[AF_ROWS], acc[AF_ROWS][DPL];
+  float m[ROWS], l[ROWS], acc[ROWS][DPL];
 #pragma unroll
-  for (int rr = 0; rr < AF_ROWS; ++rr) {
+  for (int rr = 0; rr < ROWS; ++rr) {
     m[rr] = -INFINITY;
     l[rr] = 0.f;
 #pragma unroll
@@ -87,21 +88,47 @@ __global__ void __launch_bounds__(AF_WARPS * 32) tree_attn_kernel(AttnArgs a) {
     const int k0 = is_tree ? (tile - n_cache_tiles) * KT : tile * KT;
     const int nk = is_tree ? min(KT, a.T - k0) : min(KT, Lb - k0);
     __syncwarp();
-    for (int e = lane; e < KT * DH; e += 32) {
-      const int j = e / DH, d = e - j * DH;
-      float kv = 0.f, vv = 0.f;
-      if (j < nk) {
-        const size_t o = is_tree ? (((size_t)b * a.T + k0 + j) * a.Hkv + g) * DH + d
-                                 : (((size_t)b * a.Lc + k0 + j) * a.Hkv + g) * DH + d;
-        kv = to_f32(reinterpret_cast<const TT*>(is_tree ? a.kt : a.kc)[o]);
-        vv = to_f32(reinterpret_cast<const TT*>(is_tree ? a.vt : a.vc)[o]);
+    // the tile's K and V rows with 16-byte loads, a batch of AF_LB per lane
+    // and array in flight before any is stored (keys past nk read as zero)
+    {
+      constexpr int VEC = 16 / (int)sizeof(TT);           // elements per 16-byte load
+      constexpr int NV = KT * DH / VEC / 32;              // loads per lane and array
+      constexpr int AF_LB = NV < 2 ? NV : 2;
+      const TT* kb = reinterpret_cast<const TT*>(is_tree ? a.kt : a.kc);
+      const TT* vb = reinterpret_cast<const TT*>(is_tree ? a.vt : a.vc);
+      const int rows = is_tree ? a.T : a.Lc;
+#pragma unroll
+      for (int u0 = 0; u0 < NV; u0 += AF_LB) {
+        uint4 kr[AF_LB], vr[AF_LB];
+#pragma unroll
+        for (int u = 0; u < AF_LB; ++u) {
+          const int e = ((u0 + u) * 32 + lane) * VEC;  // element of the [KT][DH] tile
+          const int j = e / DH, d = e - j * DH;
+          kr[u] = make_uint4(0u, 0u, 0u, 0u);
+          vr[u] = kr[u];
+          if (j < nk) {
+            const size_t o = (((size_t)b * rows + k0 + j) * a.Hkv + g) * DH + d;
+            kr[u] = *reinterpret_cast<const uint4*>(kb + o);
+            vr[u] = *reinterpret_cast<const uint4*>(vb + o);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < AF_LB; ++u) {
+          const int e = ((u0 + u) * 32 + lane) * VEC;
+          const int j = e / DH, d = e - j * DH;
+          const TT* kx = reinterpret_cast<const TT*>(&kr[u]);
+          const TT* vx = reinterpret_cast<const TT*>(&vr[u]);
+#pragma unroll
+          for (int x = 0; x < VEC; ++x) {
+            ks[j * (DH + 1) + d + x] = to_f32(kx[x]);
+            vs[j * DH + d + x] = to_f32(vx[x]);
+          }
+        }
       }
-      ks[j * (DH + 1) + d] = kv;
-      vs[j * DH + d] = vv;
     }
     __syncwarp();
 #pragma unroll
-    for (int rr = 0; rr < AF_ROWS; ++rr) {
+    for (int rr = 0; rr < ROWS; ++rr) {
       const int r = row0 + rr;
       if (r >= nrows) break;
       float s = 0.f;
@@ -130,33 +157,33 @@ __global__ void __launch_bounds__(AF_WARPS * 32) tree_attn_kernel(AttnArgs a) {
   // join the warps' states of every row: m* = max m_w,
   // o = sum_w 2^(m_w - m*) acc_w / sum_w 2^(m_w - m*) l_w
   __syncthreads();
-  float* pm = qs + AF_ROWS * DH;          // [AF_WARPS][AF_ROWS] (reuses the tiles' space)
-  float* pl = pm + AF_WARPS * AF_ROWS;    // [AF_WARPS][AF_ROWS]
-  float* pa = pl + AF_WARPS * AF_ROWS;    // [AF_WARPS][AF_ROWS][DH]
+  float* pm = qs + ROWS * DH;          // [AF_WARPS][ROWS] (reuses the tiles' space)
+  float* pl = pm + AF_WARPS * ROWS;    // [AF_WARPS][ROWS]
+  float* pa = pl + AF_WARPS * ROWS;    // [AF_WARPS][ROWS][DH]
 #pragma unroll
-  for (int rr = 0; rr < AF_ROWS; ++rr) {
+  for (int rr = 0; rr < ROWS; ++rr) {
     if (lane == 0) {
-      pm[warp * AF_ROWS + rr] = m[rr];
-      pl[warp * AF_ROWS + rr] = l[rr];
+      pm[warp * ROWS + rr] = m[rr];
+      pl[warp * ROWS + rr] = l[rr];
     }
 #pragma unroll
-    for (int t = 0; t < DPL; ++t) pa[((size_t)warp * AF_ROWS + rr) * DH + lane + 32 * t] = acc[rr][t];
+    for (int t = 0; t < DPL; ++t) pa[((size_t)warp * ROWS + rr) * DH + lane + 32 * t] = acc[rr][t];
   }
   __syncthreads();
   TT* O = reinterpret_cast<TT*>(a.out);
-  for (int e = threadIdx.x; e < AF_ROWS * DH; e += blockDim.x) {
+  for (int e = threadIdx.x; e < ROWS * DH; e += blockDim.x) {
     const int rr = e / DH, d = e - rr * DH;
     const int r = row0 + rr;
     if (r >= nrows) continue;
     float ms = -INFINITY;
-    for (int w = 0; w < AF_WARPS; ++w) ms = fmaxf(ms, pm[w * AF_ROWS + rr]);
+    for (int w = 0; w < AF_WARPS; ++w) ms = fmaxf(ms, pm[w * ROWS + rr]);
     float num = 0.f, den = 0.f;
     for (int w = 0; w < AF_WARPS; ++w) {
-      const float mw = pm[w * AF_ROWS + rr];
+      const float mw = pm[w * ROWS + rr];
       if (mw == -INFINITY) continue;  // this warp saw no visible key of the row
       const float f = exp2f(mw - ms);
-      num = fmaf(f, pa[((size_t)w * AF_ROWS + rr) * DH + d], num);
-      den = fmaf(f, pl[w * AF_ROWS + rr], den);
+      num = fmaf(f, pa[((size_t)w * ROWS + rr) * DH + d], num);
+      den = fmaf(f, pl[w * ROWS + rr], den);
     }
     const int i = r / a.G, h = g * a.G + (r - i * a.G);
     O[((size_t)b * a.T + i) * a.H + (size_t)h * DH + d] = from_f32<TT>(num / den);
@@ -189,14 +216,19 @@ int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* v
   a.qscale = 1.4426950408889634f / sqrtf((float)p.Dh);
   a.lens = lens;
   a.ws = ws;
-  dim3 grid((p.T * p.G + AF_ROWS - 1) / AF_ROWS, p.Hkv, p.B);
-  // the key tiles' space also holds the warps' final states ([8][16] m and l, [8][16][Dh] o)
-  const size_t tiles = p.Dh == 128 ? af_smem_floats<128>() : af_smem_floats<64>();
-  const size_t join = (size_t)AF_ROWS * p.Dh + 2 * AF_WARPS * AF_ROWS + (size_t)AF_WARPS * AF_ROWS * p.Dh;
+  // 16 query rows per CTA; 4 when that leaves most SMs idle (a small tree
+  // and batch): four times the CTAs, each warp's row loop a quarter as long
+  const bool few = (long long)((p.T * p.G + AF_ROWS - 1) / AF_ROWS) * p.Hkv * p.B < 148;
+  const int rows = few ? AF_ROWS_FEW : AF_ROWS;
+  dim3 grid((p.T * p.G + rows - 1) / rows, p.Hkv, p.B);
+  // the key tiles' space also holds the warps' final states ([8][rows] m and l, [8][rows][Dh] o)
+  const size_t tiles = few ? (p.Dh == 128 ? af_smem_floats<128, AF_ROWS_FEW>() : af_smem_floats<64, AF_ROWS_FEW>())
+                           : (p.Dh == 128 ? af_smem_floats<128, AF_ROWS>() : af_smem_floats<64, AF_ROWS>());
+  const size_t join = (size_t)rows * p.Dh + 2 * AF_WARPS * rows + (size_t)AF_WARPS * rows * p.Dh;
   const size_t smem = (tiles > join ? tiles : join) * sizeof(float);
   void (*k)(AttnArgs);
-  if (p.bf16) k = p.Dh == 128 ? tree_attn_kernel<__nv_bfloat16, 128> : tree_attn_kernel<__nv_bfloat16, 64>;
-  else k = p.Dh == 128 ? tree_attn_kernel<float, 128> : tree_attn_kernel<float, 64>;
+  if (few) k = p.Dh == 128 ? tree_attn_kernel<float, 128, AF_ROWS_FEW> : tree_attn_kernel<float, 64, AF_ROWS_FEW>;
+  else k = p.Dh == 128 ? tree_attn_kernel<float, 128, AF_ROWS> : tree_attn_kernel<float, 64, AF_ROWS>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
   return (int)launch_k(k, grid, dim3(AF_WARPS * 32), smem, st, true, a);

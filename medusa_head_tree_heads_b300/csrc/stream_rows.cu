@@ -424,11 +424,11 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(RowArgs a, int nctas) {
 // --------------------------------------------------------------- launchers --
 // rows per CTA so that a grid of `want` CTAs covers R rows with no CTA
 // spanning more than kMaxPieces segments of S rows
-static void partition(int R, int S, int want, int max_rows, int* ctas, int* rpc) {
+static void partition(int R, int S, int want, int max_rows, int min_rows, int* ctas, int* rpc) {
   if (want > kMaxStreamCtas) want = kMaxStreamCtas;
   if (want < 1) want = 1;
   int r = (R + want - 1) / want;
-  if (r < 1) r = 1;
+  if (r < min_rows) r = min_rows;
   if (r > max_rows) r = max_rows;
   const int cap = (kMaxPieces - 1) * S;
   if (r > cap) r = cap;
@@ -450,7 +450,10 @@ static int launch_nc(RowArgs a, int sm_count, int nc, int ctiles, cudaStream_t s
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, smem);       \
     if (e == cudaSuccess) {                                                                                 \
       int ctas = 0;                                                                                         \
-      partition(a.R, a.S, sm_count * (occ > 0 ? occ : 1), EPI == EPI_TOPK ? kRowBuf : (1 << 30), &ctas, &a.rpc); \
+      /* epilogues with a merge take at least four rows per warp: a small weight then */                   \
+      /* takes tens of CTAs instead of hundreds of one-row CTAs whose partials are merged one by one */   \
+      partition(a.R, a.S, sm_count * (occ > 0 ? occ : 1), EPI == EPI_TOPK ? kRowBuf : (1 << 30),           \
+                EPI == EPI_FC ? 1 : 4 * kWarps, &ctas, &a.rpc);                                             \
       if (ctas > kMaxStreamCtas) return (int)cudaErrorInvalidConfiguration;                                 \
       e = launch_k(k, dim3(ctas, ctiles), dim3(kThreads), smem, st, EPI != EPI_FC, a);                      \
       if (e == cudaSuccess && EPI == EPI_TOPK) {                                                            \
