@@ -13,6 +13,7 @@ instead (the only reference implementation of this path), on the host cores.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import json
 import os
 import statistics
@@ -250,6 +251,47 @@ def host_cores() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
 
+@contextlib.contextmanager
+def blas_one_thread():
+    """Holds the BLAS library numpy calls to one thread; yields how
+    ("threadpoolctl", "openblas") or None when neither way is available.
+    threadpoolctl is not installed on every host, so numpy's bundled OpenBLAS
+    is also reached directly through its exported thread setter."""
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        threadpool_limits = None
+    if threadpool_limits is not None:
+        with threadpool_limits(limits=1):
+            yield "threadpoolctl"
+        return
+    import ctypes
+    import glob
+    found = None
+    import numpy as np
+    for path in sorted(glob.glob(os.path.join(os.path.dirname(np.__file__), "..", "numpy.libs", "*openblas*.so*"))):
+        lib = ctypes.CDLL(path)
+        for name in ("scipy_openblas_{}_num_threads64_", "scipy_openblas_{}_num_threads", "openblas_{}_num_threads"):
+            setn = getattr(lib, name.format("set"), None)
+            getn = getattr(lib, name.format("get"), None)
+            if setn is not None and getn is not None:
+                found = (setn, getn)
+                break
+        if found:
+            break
+    if found is None:
+        yield None
+        return
+    setn, getn = found
+    getn.restype = ctypes.c_int
+    before = getn()
+    setn(ctypes.c_int(1))
+    try:
+        yield "openblas"
+    finally:
+        setn(ctypes.c_int(before))
+
+
 def time_oracle(s, inp, budget_s: float = 20.0, single_thread: bool = True) -> dict:
     """The oracle as it stands, on this host's cores: whole steps until the
     time budget is used (at least one), with the BLAS library on every core;
@@ -268,13 +310,15 @@ def time_oracle(s, inp, budget_s: float = 20.0, single_thread: bool = True) -> d
            "sample": f"{len(times)} whole step(s) of {s.name} (numpy float64, BLAS on all cores)",
            "seconds": sum(times), "cpu_model": cpu_model()}
     if single_thread:
-        from threadpoolctl import threadpool_limits
-        with threadpool_limits(limits=1):
-            t0 = time.perf_counter()
-            O.step(n, s)
-            dt = time.perf_counter() - t0
-        res["single_thread"] = {"value": 1.0 / dt, "unit": "steps/s", "cores": 1,
-                                "sample": f"1 whole step of {s.name} (BLAS held to one thread)"}
+        with blas_one_thread() as how:
+            if how is None:
+                res["single_thread"] = {"value": None, "unavailable": "no way to hold this host's BLAS to one thread"}
+            else:
+                t0 = time.perf_counter()
+                O.step(n, s)
+                dt = time.perf_counter() - t0
+                res["single_thread"] = {"value": 1.0 / dt, "unit": "steps/s", "cores": 1,
+                                        "sample": f"1 whole step of {s.name} (BLAS held to one thread by {how})"}
     return res
 
 

@@ -37,6 +37,41 @@ def test_cpu_baseline_reports_all_cores_and_one_thread():
     assert st["cores"] == 1 and st["value"] > 0 and st["unit"] == "steps/s"
 
 
+def test_one_thread_blas_without_threadpoolctl(monkeypatch):
+    """Hosts without threadpoolctl still hold numpy's bundled OpenBLAS to one
+    thread (through its own setter) and restore the thread count after."""
+    import builtins
+
+    import bench
+    real_import = builtins.__import__
+
+    def no_threadpoolctl(name, *args, **kw):
+        if name == "threadpoolctl":
+            raise ImportError("hidden for this test")
+        return real_import(name, *args, **kw)
+
+    monkeypatch.setattr(builtins, "__import__", no_threadpoolctl)
+    import ctypes
+    import glob
+    import os
+
+    import numpy as np
+    libs = glob.glob(os.path.join(os.path.dirname(np.__file__), "..", "numpy.libs", "*openblas*.so*"))
+    get = None
+    for path in libs:
+        lib = ctypes.CDLL(path)
+        get = getattr(lib, "scipy_openblas_get_num_threads64_", None)
+        if get is not None:
+            get.restype = ctypes.c_int
+            break
+    before = get() if get is not None else None
+    with bench.blas_one_thread() as how:
+        if get is not None:
+            assert how == "openblas" and get() == 1
+    if get is not None:
+        assert get() == before
+
+
 def test_reference_arm_prints_one_contract_line():
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny-fp32", "--steps", "2",
                         "--warmup", "0"], cwd=ROOT, capture_output=True, text=True, timeout=600)
