@@ -398,6 +398,34 @@ namespace medusa {
 
 // Validates every argument of the step, then launches its kernels in order,
 // recording events[2k] / events[2k+1] around kernel k when events != NULL.
+// A second stream of the calling host thread on the current device, with two
+// events, for the step's fork (created on first use; none if creation fails,
+// and the step then runs in one stream).  Per thread, so two host threads
+// never record into each other's fork.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool failed = false;
+};
+static SideStream* side_stream() {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream per_dev[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = per_dev[dev];
+  if (ss.failed) return nullptr;
+  if (!ss.s) {
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      ss.failed = true;
+      return nullptr;
+    }
+  }
+  return &ss;
+}
+
 static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
                     void* const* events, int n_events) {
   if (!io) return MEDUSA_ERR_INVALID_ARG;
@@ -437,6 +465,32 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
 #define MEDUSA_ATTN_STAGE                                                                                    \
   MEDUSA_STAGE(3, launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, \
                                    io->tree.mask, io->attn_out, ws, st))
+  // CUDA-core path without stage events: the tree attention (its ancestor
+  // masks built from the plan's parent table, not from the tree outputs) and
+  // the verification (the rows kernel's needs no tokens) read none of the
+  // heads' or the tree build's outputs, so they run on a second stream beside
+  // the head layer, projection and tree build, and the acceptance waits for
+  // both branches (inside a graph capture: two parallel branches)
+  SideStream* side = (!events && !p.bf16 && !p.late_tree) ? side_stream() : nullptr;
+  if (side) {
+    e = (int)cudaEventRecord(side->fork, st);
+    if (e == 0) e = (int)cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (e == 0)
+      e = launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, io->tree.mask,
+                           io->attn_out, ws, side->s);
+    if (e == 0)
+      e = launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit,
+                        io->node_lse, io->node_entropy, ws, side->s);
+    if (e == 0) e = (int)cudaEventRecord(side->join, side->s);
+    if (e == 0) e = launch_head_layer(p, io->h, io->W1, io->b1, ws, st);
+    if (e == 0) e = launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st);
+    if (e == 0) e = launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st);
+    if (e == 0) e = (int)cudaStreamWaitEvent(st, side->join, 0);
+    if (e == 0)
+      e = launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse, io->node_entropy,
+                        io->accept_len, io->acc_tokens, io->acc_nodes, io->bonus, ws, st);
+    return e ? cuda_status(e) : MEDUSA_OK;
+  }
   MEDUSA_STAGE(0, launch_head_layer(p, io->h, io->W1, io->b1, ws, st))
   if (p.late_tree) {
     // Tensor-core heads: the projection, the tree attention and the

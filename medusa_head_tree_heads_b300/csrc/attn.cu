@@ -26,7 +26,8 @@ constexpr int AF_WARPS = 8;
 
 struct AttnArgs {
   const void *q, *kt, *vt, *kc, *vc;
-  const uint32_t* mask;  // [T][W]
+  TreeDims td;           // the tree's parent table: each CTA builds its rows' ancestor masks from it
+  size_t smem_floats;    // the float area of dynamic shared memory; the rows' masks follow it
   void* out;             // [B][T][H]
   int B, T, W, Hq, Hkv, G, L, Lc, H;
   float qscale;  // log2(e) / sqrt(Dh)
@@ -54,9 +55,18 @@ __global__ void __launch_bounds__(AF_WARPS * 32) tree_attn_kernel(AttnArgs a) {
   const int row0 = blockIdx.x * ROWS;
   const int nrows = a.T * a.G;
   const TT* Q = reinterpret_cast<const TT*>(a.q);
+  uint32_t* mrow = reinterpret_cast<uint32_t*>(reinterpret_cast<float*>(at_smem) + a.smem_floats);  // [ROWS][W]
   pdl_trigger();
   pdl_wait();
 
+  // ancestor-or-self mask of each row's node (its chain of parents)
+  for (int rr = threadIdx.x; rr < ROWS; rr += blockDim.x) {
+    const int r = row0 + rr;
+    uint32_t* mw = mrow + (size_t)rr * a.W;
+    for (int w = 0; w < a.W; ++w) mw[w] = 0u;
+    if (r < nrows)
+      for (int j = r / a.G; j >= 0; j = a.td.parent[j]) mw[j >> 5] |= 1u << (j & 31);
+  }
   // queries of this CTA, pre-scaled so that exp2 gives the softmax weights
   for (int e = threadIdx.x; e < ROWS * DH; e += blockDim.x) {
     const int rr = e / DH, d = e - rr * DH;
@@ -135,7 +145,7 @@ __global__ void __launch_bounds__(AF_WARPS * 32) tree_attn_kernel(AttnArgs a) {
 #pragma unroll 16
       for (int d = 0; d < DH; ++d) s = fmaf(qs[rr * DH + d], ks[key * (DH + 1) + d], s);
       bool ok = lane < KT && key < nk;
-      if (is_tree) ok = ok && ((a.mask[(size_t)(r / a.G) * a.W + ((k0 + key) >> 5)] >> ((k0 + key) & 31)) & 1u);
+      if (is_tree) ok = ok && ((mrow[(size_t)rr * a.W + ((k0 + key) >> 5)] >> ((k0 + key) & 31)) & 1u);
       s = ok ? s : -INFINITY;
       const float mt = warp_max(s);
       if (mt == -INFINITY) continue;  // nothing visible in this tile
@@ -202,7 +212,7 @@ int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* v
   a.vt = vt;
   a.kc = kc;
   a.vc = vc;
-  a.mask = mask;
+  a.td = p.tree;
   a.out = out;
   a.B = p.B;
   a.T = p.T;
@@ -225,7 +235,8 @@ int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* v
   const size_t tiles = few ? (p.Dh == 128 ? af_smem_floats<128, AF_ROWS_FEW>() : af_smem_floats<64, AF_ROWS_FEW>())
                            : (p.Dh == 128 ? af_smem_floats<128, AF_ROWS>() : af_smem_floats<64, AF_ROWS>());
   const size_t join = (size_t)rows * p.Dh + 2 * AF_WARPS * rows + (size_t)AF_WARPS * rows * p.Dh;
-  const size_t smem = (tiles > join ? tiles : join) * sizeof(float);
+  a.smem_floats = tiles > join ? tiles : join;
+  const size_t smem = a.smem_floats * sizeof(float) + (size_t)rows * p.W * sizeof(uint32_t);
   void (*k)(AttnArgs);
   if (few) k = p.Dh == 128 ? tree_attn_kernel<float, 128, AF_ROWS_FEW> : tree_attn_kernel<float, 64, AF_ROWS_FEW>;
   else k = p.Dh == 128 ? tree_attn_kernel<float, 128, AF_ROWS> : tree_attn_kernel<float, 64, AF_ROWS>;
