@@ -133,6 +133,48 @@ def test_profiled_step_equals_step(name):
         U.assert_close(a[k].float().cpu().numpy(), b[k].float().cpu().numpy(), s.dtype, k)
 
 
+@pytest.mark.parametrize("name", ["tiny-fp32", "tiny-fp32-gqa", "k16-f32", "sparse-f32"])
+def test_forked_fp32_step_in_a_graph_equals_the_serial_step(name):
+    """The fp32 step runs its tree attention and verification on a second
+    stream beside the heads; captured in a CUDA graph (two branches) and
+    replayed, it gives the profiled step's results (one stream, stage order)
+    bit for bit: the same kernels with the same launch shapes."""
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs(name)
+    assert s.dtype == "f32"
+    d = U.to_device(inp)
+    cfg = M.make_config(s)
+    ws = M.alloc_workspace(cfg)
+    a, b = M.alloc_outputs(cfg), M.alloc_outputs(cfg)
+    io = M.step_io(d, a)
+    M.medusa_step(cfg, io, ws)  # eager once (creates the side stream outside the capture)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        M.medusa_step(cfg, io, ws)
+    def fill(outs):  # the same sentinel wherever a step leaves an output entry unwritten
+        for v in outs.values():
+            for t in (v.values() if isinstance(v, dict) else [v]):
+                t.fill_(-7)
+
+    for _ in range(3):
+        fill(a)
+        g.replay()
+    fill(b)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(M.STEP_KERNELS))]
+    for e in evs:
+        e.record()
+    M.medusa_step_profiled(cfg, M.step_io(d, b), ws, evs)
+    torch.cuda.synchronize()
+    assert M.medusa_get_device_error(ws) == 0
+    for k in a:
+        if k == "tree":
+            for t in a[k]:
+                assert torch.equal(a[k][t], b[k][t]), t
+        else:
+            assert torch.equal(a[k], b[k]), k
+
+
 @pytest.mark.parametrize("name", ["7b-mini", "gqa-mini"])
 def test_repeated_steps_are_identical(name):
     """The workspace tickets reset themselves: back-to-back steps agree bitwise."""
