@@ -17,8 +17,6 @@ int launch_head_layer(const Plan& p, const void* h, const void* W1, const void* 
   if (heads_tc_supported(p)) return launch_fc_tc(p, h, W1, b1, ws, st);
   return launch_fc(p, h, W1, b1, ws, st);
 }
-int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
-                     cudaStream_t st);
 int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
                      cudaStream_t st);
 
@@ -482,9 +480,12 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
       e = launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit,
                         io->node_lse, io->node_entropy, ws, side->s);
     if (e == 0) e = (int)cudaEventRecord(side->join, side->s);
+    // the heads branch: layer, projection, then one kernel for the top-k merge and the tree
+    int ctas = 0, rpc = 0;
     if (e == 0) e = launch_head_layer(p, io->h, io->W1, io->b1, ws, st);
-    if (e == 0) e = launch_head_proj(p, io->W2, io->topk_idx, io->topk_val, ws, st);
-    if (e == 0) e = launch_tree_build(p, io->topk_idx, io->root_token, io->tree, st);
+    if (e == 0) e = launch_proj_topk(p, io->W2, io->topk_idx, io->topk_val, ws, st, &ctas, &rpc);
+    if (e == 0)
+      e = launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, rpc, p.Vs, false, st);
     if (e == 0) e = (int)cudaStreamWaitEvent(st, side->join, 0);
     if (e == 0)
       e = launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse, io->node_entropy,

@@ -116,6 +116,10 @@ ShardRecord shard_record_layout(const Plan& p);
 // launchers (enqueue only; return cudaError_t as int)
 int launch_heads(const Plan& p, const void* h, const void* W1, const void* b1, const void* W2, int32_t* topk_idx,
                  float* topk_val, uint8_t* ws, cudaStream_t st);
+// head projection on the CUDA cores (streaming row kernel); with ctas / rpc
+// the per-CTA top-k candidates stay in the workspace for the caller's merge
+int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
+                     cudaStream_t st, int* ctas = nullptr, int* rpc = nullptr);
 int launch_tree_build(const Plan& p, const int32_t* topk_idx, const int32_t* root, const medusa_tree_t& t,
                       cudaStream_t st);
 int attn_tc_splits(int B, int T, int G, int Hkv, int L);

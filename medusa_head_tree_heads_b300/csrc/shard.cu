@@ -23,8 +23,6 @@
 
 namespace medusa {
 
-int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
-                     cudaStream_t st);
 int launch_topk_merge(const Plan& p, int32_t* topk_idx, float* topk_val, uint8_t* ws, int ctas, int rpc, int S,
                       cudaStream_t st);
 int launch_accept(const Plan& p, const void* attn_out, const void* lm_head, const medusa_tree_t& t,

@@ -439,7 +439,8 @@ static void partition(int R, int S, int want, int max_rows, int min_rows, int* c
 // Launches one persistent grid of (SM count x resident CTAs per SM) CTAs per
 // column tile; the grid size comes from the occupancy of the instance.
 template <typename TW, typename TX, int EPI>
-static int launch_nc(RowArgs a, int sm_count, int nc, int ctiles, cudaStream_t st) {
+static int launch_nc(RowArgs a, int sm_count, int nc, int ctiles, cudaStream_t st, int* ctas_out = nullptr,
+                     int* rpc_out = nullptr) {
   const size_t smem = (size_t)nc * a.H * sizeof(float) + (EPI == EPI_TOPK ? (size_t)nc * kRowBuf * sizeof(float) : 0);
   cudaError_t e = cudaSuccess;
 #define MEDUSA_LAUNCH_NC(N)                                                                                 \
@@ -456,7 +457,9 @@ static int launch_nc(RowArgs a, int sm_count, int nc, int ctiles, cudaStream_t s
                 EPI == EPI_FC ? 1 : 4 * kWarps, &ctas, &a.rpc);                                             \
       if (ctas > kMaxStreamCtas) return (int)cudaErrorInvalidConfiguration;                                 \
       e = launch_k(k, dim3(ctas, ctiles), dim3(kThreads), smem, st, EPI != EPI_FC, a);                      \
-      if (e == cudaSuccess && EPI == EPI_TOPK) {                                                            \
+      if (ctas_out) *ctas_out = ctas;                                                                       \
+      if (rpc_out) *rpc_out = a.rpc;                                                                        \
+      if (e == cudaSuccess && EPI == EPI_TOPK && !ctas_out) { /* else the caller merges */                  \
         const unsigned mg = (unsigned)((a.nseg * a.C + 7) / 8);                                             \
         if (a.kmax <= 4) e = launch_k(topk_merge_kernel<4>, dim3(mg), dim3(256), 0, st, true, a, ctas);     \
         else e = launch_k(topk_merge_kernel<KMAX>, dim3(mg), dim3(256), 0, st, true, a, ctas);              \
@@ -517,8 +520,11 @@ int launch_fc(const Plan& p, const void* h, const void* W1, const void* b1, uint
   return launch_nc<float, float, EPI_FC>(a, p.sm_count, p.fc_nc, p.fc_ctiles, st);
 }
 
+// ctas / rpc non-null: the candidates stay in the workspace for the caller's
+// merge (the grid and rows per CTA are reported); otherwise the top-k merge
+// is launched here
 int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* topk_val, uint8_t* ws,
-                     cudaStream_t st) {
+                     cudaStream_t st, int* ctas, int* rpc) {
   RowArgs a{};
   a.W = W2;
   a.x = ws + p.off_z;
@@ -539,8 +545,8 @@ int launch_proj_topk(const Plan& p, const void* W2, int32_t* topk_idx, float* to
   a.cand_seg = reinterpret_cast<int*>(ws + p.off_cand_seg);
   a.out_idx = topk_idx;
   a.out_val = topk_val;
-  if (p.bf16) return launch_nc<__nv_bfloat16, float, EPI_TOPK>(a, p.sm_count, p.pj_nc, p.pj_ctiles, st);
-  return launch_nc<float, float, EPI_TOPK>(a, p.sm_count, p.pj_nc, p.pj_ctiles, st);
+  if (p.bf16) return launch_nc<__nv_bfloat16, float, EPI_TOPK>(a, p.sm_count, p.pj_nc, p.pj_ctiles, st, ctas, rpc);
+  return launch_nc<float, float, EPI_TOPK>(a, p.sm_count, p.pj_nc, p.pj_ctiles, st, ctas, rpc);
 }
 
 int launch_verify_rows(const Plan& p, const void* attn_out, const void* lm_head, int32_t* node_argmax,
