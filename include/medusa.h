@@ -326,7 +326,9 @@ int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* wo
  * (+ split combine), 4 verification projection (+ partial merge),
  * 5 acceptance.  Under MEDUSA_SCHEDULE_OVERLAP stage 3 is issued before stage
  * 2 (the results are the same; its stage times may include overlap with the
- * projection). */
+ * projection).  With fp32 the profiled step does not fork (stages in order,
+ * in `stream`; the top-k merge and the tree build are then two launches, one
+ * in medusa_step), and its results equal medusa_step's bit for bit. */
 #define MEDUSA_STEP_KERNELS 6
 int medusa_step_profiled(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream,
                          void* const* events, int32_t n_events);

@@ -556,8 +556,9 @@ int medusa_step_launches(const medusa_config_t* cfg) {
   if (p.sharded) return MEDUSA_ERR_INVALID_ARG;
   finish_plan(&p);
   p.overlap = pick_overlap(p);
-  int n = 6;                        // one launch per stage
-  if (!heads_tc_supported(p)) n += 1;  // separate top-k merge (else fused with the tree)
+  int n = 6;                                     // one launch per stage
+  if (p.bf16 && !heads_tc_supported(p)) n += 1;  // separate top-k merge (else fused with the tree;
+                                                 // fp32 forks, with the merge and the tree in one kernel)
   if (p.bf16) {
     int NS, cb;
     attn_split_shape(p.B, p.T, p.G, p.Hkv, p.L, &NS, &cb);

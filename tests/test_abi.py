@@ -165,6 +165,7 @@ def test_schedule_launch_counts():
         return M.step_launches(M.make_config(synth.SHAPES[name], **over))
     assert n("7b-bf16", schedule=M.SERIAL) == 8   # 6 stages + attention combine + verification merge
     assert n("7b-bf16", schedule=M.OVERLAP) == 7
+    assert n("tiny-fp32") == 6  # two branches: layer, projection, merge + tree | attention, verification; acceptance
     for name in ("7b-bf16", "7b-sample", "7b-sparse64"):
         assert n(name) == n(name, schedule=M.OVERLAP), name
     for name in ("13b-bf16", "gqa128k-bf16", "33b-bf16", "tiny-fp32", "33b-b32-mini"):
