@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(HT_THREADS, 1)
             const bool in = (pass >> lane) & 1u;
             const int key = in ? order_key(v) : INT_MIN;
             int kmx;
-            kmx = __reduce_max_sync(0xffffffffu, key);
+            asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(kmx) : "r"(key));
             const unsigned top = __ballot_sync(0xffffffffu, in && key == kmx);
             const int w = __ffs(top) - 1;  // lowest lane = lowest row among equal values
             const float wv = __shfl_sync(0xffffffffu, v, w);
