@@ -399,19 +399,22 @@ namespace medusa {
 // A second stream of the calling host thread on the current device, with two
 // events, for the step's fork (created on first use; none if creation fails,
 // and the step then runs in one stream).  Per thread, so two host threads
-// never record into each other's fork.
+// never record into each other's fork.  Never created while `capturing` (a
+// stream or event creation could invalidate the caller's graph capture): that
+// call runs in one stream.
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   bool failed = false;
 };
-static SideStream* side_stream() {
+static SideStream* side_stream(bool capturing) {
   constexpr int kMaxDevices = 64;
   thread_local SideStream per_dev[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   SideStream& ss = per_dev[dev];
   if (ss.failed) return nullptr;
+  if (!ss.s && capturing) return nullptr;
   if (!ss.s) {
     if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
@@ -469,7 +472,12 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   // heads' or the tree build's outputs, so they run on a second stream beside
   // the head layer, projection and tree build, and the acceptance waits for
   // both branches (inside a graph capture: two parallel branches)
-  SideStream* side = (!events && !p.bf16 && !p.late_tree) ? side_stream() : nullptr;
+  SideStream* side = nullptr;
+  if (!events && !p.bf16 && !p.late_tree) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MEDUSA_ERR_CUDA;
+    side = side_stream(cs != cudaStreamCaptureStatusNone);
+  }
   if (side) {
     e = (int)cudaEventRecord(side->fork, st);
     if (e == 0) e = (int)cudaStreamWaitEvent(side->s, side->fork, 0);

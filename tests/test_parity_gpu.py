@@ -175,6 +175,50 @@ def test_forked_fp32_step_in_a_graph_equals_the_serial_step(name):
             assert torch.equal(a[k], b[k]), k
 
 
+def test_fp32_step_captured_on_a_threads_first_call():
+    """A host thread whose first fp32 step is inside a graph capture gets no
+    second stream (creating one could break the capture): the capture
+    succeeds, the step runs in one stream and matches the forked step."""
+    import threading
+
+    from medusa_head_tree_heads_b300 import medusa as M
+    s, inp = U.planned_inputs("tiny-fp32-gqa")
+    d = U.to_device(inp)
+    cfg = M.make_config(s)
+    ws = M.alloc_workspace(cfg)
+    a, b = M.alloc_outputs(cfg), M.alloc_outputs(cfg)
+    for outs in (a, b):  # the same sentinel wherever a step leaves an output entry unwritten
+        for v in outs.values():
+            for x in (v.values() if isinstance(v, dict) else [v]):
+                x.fill_(-7)
+    M.medusa_step(cfg, M.step_io(d, b), ws)  # this thread: forked
+    torch.cuda.synchronize()
+    err = []
+
+    def run():
+        try:
+            torch.cuda.set_device(d["h"].device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                M.medusa_step(cfg, M.step_io(d, a), ws)
+            g.replay()
+            torch.cuda.synchronize()
+        except Exception as e:  # reported below
+            err.append(e)
+
+    t = threading.Thread(target=run)
+    t.start()
+    t.join()
+    assert not err, err
+    assert M.medusa_get_device_error(ws) == 0
+    for k in a:
+        if k == "tree":
+            for x in a[k]:
+                assert torch.equal(a[k][x], b[k][x]), x
+        else:
+            assert torch.equal(a[k], b[k]), k
+
+
 @pytest.mark.parametrize("name", ["7b-mini", "gqa-mini"])
 def test_repeated_steps_are_identical(name):
     """The workspace tickets reset themselves: back-to-back steps agree bitwise."""
