@@ -309,8 +309,9 @@ int medusa_next_inputs(const medusa_config_t* cfg, const void* attn_out, const i
  * by later work: kernels of the step start early only beside other kernels of
  * the same step, and the first one waits for all earlier work.  With fp32
  * storage the tree attention and the verification run on a second stream of
- * the calling host thread (created on the first such call on each device;
- * the step runs in `stream` alone if that fails), forked from `stream` by an
+ * the calling host thread (created on the first such call on each device
+ * that is not inside a graph capture; until then, or if that fails, the step
+ * runs in `stream` alone), forked from `stream` by an
  * event and joined back before the acceptance, so the ordering above holds
  * unchanged; inside a graph capture of `stream` this gives two branches. */
 int medusa_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void* workspace, void* stream);
