@@ -17,7 +17,7 @@
 // (one per SM):
 //   warp 0      TMA producer (one thread), S-stage smem ring
 //   warp 1      TMEM allocator + MMA issuer (one thread)
-//   warps 2..    epilogue (two or four per TMEM lane quadrant by mode,
+//   warps 2..    epilogue (four or two per TMEM lane quadrant by mode,
 //               columns split in groups of 64): tcgen05.ld 16 columns at a time; per column
 //               the max over the warp's rows and the lowest row reaching it
 //               by a "transpose-reduce" across the lanes (each exchange
@@ -43,11 +43,11 @@ namespace medusa {
 constexpr int VT_M = 128;       // vocab rows per MMA (M)
 constexpr int VT_SUB = 2;       // MMA halves per tile: a tile is VT_SUB * VT_M vocab rows
 constexpr int VT_BK = 64;       // K elements per stage (128 bytes of bf16)
-// Epilogue warps per mode: 16 for greedy (four per TMEM lane quadrant, each
-// a quarter of the columns: 33B step 4547 -> 4426 us, the 7B step unchanged),
-// 8 for the typical and sampling epilogues (two per quadrant; with 16 they
-// measured no faster and the sampling epilogue spilled registers).
-__host__ __device__ constexpr int vt_epi_warps(int mode) { return mode == 0 ? 16 : 8; }
+// Epilogue warps per mode: 16 for greedy and typical (four per TMEM lane
+// quadrant, each a quarter of the columns: 33B step 4547 -> 4426 us; with the
+// transpose-reduce epilogue the GQA-shaped typical step 614 -> 599 us), 8 for
+// the sampling epilogues (two per quadrant: with 16 they spill registers).
+__host__ __device__ constexpr int vt_epi_warps(int mode) { return mode <= 1 ? 16 : 8; }
 __host__ __device__ constexpr int vt_threads(int mode) { return 64 + 32 * vt_epi_warps(mode); }
 constexpr uint32_t VT_TMEM_COLS = 512;
 constexpr uint64_t VT_WAIT_NS = 20ull * 1000 * 1000;  // 20 ms per wait
