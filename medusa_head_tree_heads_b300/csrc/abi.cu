@@ -480,21 +480,26 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   }
   if (side) {
     e = (int)cudaEventRecord(side->fork, st);
-    if (e == 0) e = (int)cudaStreamWaitEvent(side->s, side->fork, 0);
-    if (e == 0)
-      e = launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, io->tree.mask,
-                           io->attn_out, ws, side->s);
-    if (e == 0)
-      e = launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit,
-                        io->node_lse, io->node_entropy, ws, side->s);
-    if (e == 0) e = (int)cudaEventRecord(side->join, side->s);
+    if (e) return cuda_status(e);
+    int es = (int)cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (es == 0)
+      es = launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, io->tree.mask,
+                            io->attn_out, ws, side->s);
+    if (es == 0)
+      es = launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit,
+                         io->node_lse, io->node_entropy, ws, side->s);
+    // the join is recorded and waited on even after a failed launch, so that
+    // later work in `stream` never runs beside this step's second branch
+    const int ej = (int)cudaEventRecord(side->join, side->s);
     // the heads branch: layer, projection, then one kernel for the top-k merge and the tree
     int ctas = 0, rpc = 0;
-    if (e == 0) e = launch_head_layer(p, io->h, io->W1, io->b1, ws, st);
+    e = launch_head_layer(p, io->h, io->W1, io->b1, ws, st);
     if (e == 0) e = launch_proj_topk(p, io->W2, io->topk_idx, io->topk_val, ws, st, &ctas, &rpc);
     if (e == 0)
       e = launch_merge_tree(p, io->topk_idx, io->topk_val, io->root_token, io->tree, ws, ctas, rpc, p.Vs, false, st);
-    if (e == 0) e = (int)cudaStreamWaitEvent(st, side->join, 0);
+    const int ew = ej == 0 ? (int)cudaStreamWaitEvent(st, side->join, 0) : ej;
+    if (e == 0) e = es;
+    if (e == 0) e = ew;
     if (e == 0)
       e = launch_accept(p, io->attn_out, io->lm_head, io->tree, io->node_argmax, io->node_lse, io->node_entropy,
                         io->accept_len, io->acc_tokens, io->acc_nodes, io->bonus, ws, st);
