@@ -91,9 +91,9 @@ typedef enum {
  * OVERLAP: the tree attention runs beside the head projection, on the SMs the
  * projection's grid leaves free (the attention reads no head output); bf16,
  * head dim 128 and B <= 32 only, else MEDUSA_ERR_UNSUPPORTED.  AUTO takes
- * OVERLAP where it is supported and the attention is small next to the head
- * projection (an estimate from the shape: at the 7B shape the step measured
- * 301 us against 317 us), else SERIAL.  With the tensor-core heads (bf16,
+ * OVERLAP wherever it is supported (measured as fast or faster at every
+ * supported shape tried, e.g. the 7B-shaped step 293 us against 301 us),
+ * else SERIAL.  With the tensor-core heads (bf16,
  * B <= 32) both orders issue the verification projection before the
  * candidate merge and tree, which then run beside it.  Any other value is
  * MEDUSA_ERR_INVALID_ARG (every call validates the config). */

@@ -240,24 +240,19 @@ int launch_head_proj(const Plan& p, const void* W2, int32_t* topk_idx, float* to
 static bool aligned16(const void* x) { return x && ((uintptr_t)x & 15u) == 0; }
 
 // medusa_step's schedule (after finish_plan).  AUTO takes the overlap order
-// when the unsplit attention, on the SMs the projection's grid leaves free,
-// is estimated to need at most half the time of the projection's weight
-// stream; a CTA of the attention is modelled as 15 us plus 1.3 us per 64-key
-// block (measured beside the projection on the 7B shape), the stream at
-// 6 TB/s.  Measured: 7B 301 us per step in the overlap order against 317 us
-// in the serial one; 13B 481 against 484; the large-vocabulary GQA and the
-// 33B shapes 1% and 0.4% slower in the overlap order.
+// wherever it is supported and the projection's grid leaves SMs free.
+// Measured with the current kernels (first replays, before the power cap
+// lowers the clock): 7B 293 us per step in the overlap order against 301 us in
+// the serial one; 13B 478 against 482; GQA-76 1788 against 1811; the
+// large-vocabulary GQA 1930-2002 against 1960; 33B 4297-4415 against
+// 4438-4492.  (An earlier build had the last two 1% and 0.4% slower in the
+// overlap order, when AUTO estimated the attention's time beside the
+// projection and kept the serial order for them.)
 static bool pick_overlap(const Plan& p) {
   if (p.schedule == MEDUSA_SCHEDULE_SERIAL) return false;
   if (!heads_tc_supported(p) || !attn_tc_supported(p)) return false;
   if (p.schedule == MEDUSA_SCHEDULE_OVERLAP) return true;
-  const int free_sms = p.sm_count - heads_tc_proj_grid(p);
-  if (free_sms < 8) return false;
-  const long long ctas = attn_tc_unsplit_ctas(p);
-  const int nb = (p.L + 63) / 64 + (p.T + 63) / 64;
-  const double attn_us = (double)((ctas + free_sms - 1) / free_sms) * (15.0 + 1.3 * nb);
-  const double proj_us = (double)p.K * p.Vs * p.H * 2 / 6.0e6;
-  return attn_us <= 0.5 * proj_us;
+  return p.sm_count - heads_tc_proj_grid(p) >= 8;
 }
 
 static int cuda_status(int e) { return e == 0 ? MEDUSA_OK : MEDUSA_ERR_CUDA; }

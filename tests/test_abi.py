@@ -157,18 +157,17 @@ def test_noalloc_rejects_configs_beyond_its_scratch_on_the_host():
 
 def test_schedule_launch_counts():
     """The overlap schedule runs the attention unsplit (no combine launch).
-    AUTO (148 SMs assumed without a device) takes the overlap order where the
-    attention is small next to the head projection (the 7B shapes) and the
-    serial order for the larger attentions (13B, the GQA and 33B shapes) and
-    where the overlap order is unsupported (fp32, head dim 64)."""
+    AUTO (148 SMs assumed without a device) takes the overlap order wherever
+    it is supported (bf16, head dim 128, batch <= 32) and the serial order
+    elsewhere (fp32, head dim 64)."""
     def n(name, **over):
         return M.step_launches(M.make_config(synth.SHAPES[name], **over))
     assert n("7b-bf16", schedule=M.SERIAL) == 8   # 6 stages + attention combine + verification merge
     assert n("7b-bf16", schedule=M.OVERLAP) == 7
     assert n("tiny-fp32") == 6  # two branches: layer, projection, merge + tree | attention, verification; acceptance
-    for name in ("7b-bf16", "7b-sample", "7b-sparse64"):
+    for name in ("7b-bf16", "7b-sample", "7b-sparse64", "13b-bf16", "gqa128k-bf16", "33b-bf16", "b5-mini"):
         assert n(name) == n(name, schedule=M.OVERLAP), name
-    for name in ("13b-bf16", "gqa128k-bf16", "33b-bf16", "tiny-fp32", "33b-b32-mini"):
+    for name in ("tiny-fp32", "33b-b32-mini", "deep-bf16"):  # fp32; bf16 with head dim 64
         assert n(name) == n(name, schedule=M.SERIAL), name
 
 
