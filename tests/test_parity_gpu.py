@@ -312,11 +312,12 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     U.compare_step(s, res, ref)
 
 
-@pytest.mark.parametrize("name,schedule", [(n, "auto") for n in FULL] + [("7b-bf16", "serial")])
+@pytest.mark.parametrize("name,schedule", [(n, "auto") for n in FULL] +
+                         [(n, "serial") for n in ("7b-bf16", "13b-bf16", "gqa128k-bf16", "33b-bf16")])
 def test_full_size_sampled(name, schedule):
     """Full size in the launch configuration the benchmark times (AUTO: the
-    overlap order at the 7B shape, the serial order for the others), plus the
-    7B step in the serial order."""
+    overlap order wherever it is supported), plus the tensor-core shapes in
+    the serial order."""
     from medusa_head_tree_heads_b300 import medusa as M
     s, inp = U.planned_inputs(name)
     res = U.gpu_step(s, U.to_device(inp), schedule={"auto": M.AUTO, "serial": M.SERIAL, "overlap": M.OVERLAP}[schedule])
