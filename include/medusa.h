@@ -248,8 +248,10 @@ int medusa_heads_topk_noalloc(const medusa_config_t* cfg, const void* h, const v
  *   o = sum_j softmax_j(q.k_j / sqrt(Dh)) v_j
  * over the L cache rows and the tree nodes j with mask[i] bit j.
  * attn_out [B][T][H] holds o of q head h at columns h*Dh .. h*Dh+Dh-1, in the
- * config's dtype.  Only tree->mask is read (the bf16 kernels derive the same
- * ancestor-or-self relation from the config's tree). */
+ * config's dtype.  The ancestor-or-self relation (mask[i]) comes from the
+ * config's tree (the tree built by medusa_tree_build for this config has the
+ * same mask); the tree's device arrays are not read, tree->mask is only
+ * checked to be present. */
 int medusa_tree_attn(const medusa_config_t* cfg, const void* q, const void* k_tree, const void* v_tree,
                      const void* k_cache, const void* v_cache, const medusa_tree_t* tree, void* attn_out,
                      void* workspace, void* stream);

@@ -322,7 +322,7 @@ int medusa_tree_attn(const medusa_config_t* cfg, const void* q, const void* k_tr
     return MEDUSA_ERR_INVALID_ARG;
   if (p.L > 0 && (!aligned16(k_cache) || !aligned16(v_cache))) return MEDUSA_ERR_INVALID_ARG;
   finish_plan(&p);
-  return cuda_status(launch_tree_attn(p, q, k_tree, v_tree, k_cache, v_cache, nullptr, tree->mask, attn_out,
+  return cuda_status(launch_tree_attn(p, q, k_tree, v_tree, k_cache, v_cache, nullptr, attn_out,
                                       (uint8_t*)workspace, (cudaStream_t)stream));
 }
 
@@ -337,7 +337,7 @@ int medusa_tree_attn_lens(const medusa_config_t* cfg, const void* q, const void*
     return MEDUSA_ERR_INVALID_ARG;
   if (p.Lc > 0 && (!aligned16(k_cache) || !aligned16(v_cache))) return MEDUSA_ERR_INVALID_ARG;
   finish_plan(&p);
-  return cuda_status(launch_tree_attn(p, q, k_tree, v_tree, k_cache, v_cache, kv_lens, tree->mask, attn_out,
+  return cuda_status(launch_tree_attn(p, q, k_tree, v_tree, k_cache, v_cache, kv_lens, attn_out,
                                       (uint8_t*)workspace, (cudaStream_t)stream));
 }
 
@@ -460,7 +460,7 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
   if (e) return cuda_status(e);
 #define MEDUSA_ATTN_STAGE                                                                                    \
   MEDUSA_STAGE(3, launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, \
-                                   io->tree.mask, io->attn_out, ws, st))
+                                   io->attn_out, ws, st))
   // CUDA-core path without stage events: the tree attention (its ancestor
   // masks built from the plan's parent table, not from the tree outputs) and
   // the verification (the rows kernel's needs no tokens) read none of the
@@ -478,8 +478,8 @@ static int run_step(const medusa_config_t* cfg, const medusa_step_io_t* io, void
     if (e) return cuda_status(e);
     int es = (int)cudaStreamWaitEvent(side->s, side->fork, 0);
     if (es == 0)
-      es = launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, io->tree.mask,
-                            io->attn_out, ws, side->s);
+      es = launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, io->attn_out,
+                            ws, side->s);
     if (es == 0)
       es = launch_verify(p, io->attn_out, io->lm_head, io->tree.token, io->node_argmax, io->node_maxlogit,
                          io->node_lse, io->node_entropy, ws, side->s);

@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(AF_WARPS * 32) tree_attn_kernel(AttnArgs a) {
 // bf16, head dim 128: tcgen05 kernel (attn_tc.cu); other bf16: mma.sync kernel
 // (attn_mma.cu); fp32: this CUDA-core kernel (no TF32)
 int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                     const int32_t* lens, const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st) {
+                     const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st) {
   if (attn_tc_supported(p)) return launch_tree_attn_tc(p, q, kt, vt, kc, vc, lens, out, ws, st);
   if (p.bf16) return launch_tree_attn_mma(p, q, kt, vt, kc, vc, lens, out, ws, st);
   AttnArgs a;

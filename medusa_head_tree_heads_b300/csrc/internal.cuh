@@ -131,7 +131,7 @@ int launch_tree_attn_tc(const Plan& p, const void* q, const void* kt, const void
 int launch_tree_attn_mma(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
                          const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st);
 int launch_tree_attn(const Plan& p, const void* q, const void* kt, const void* vt, const void* kc, const void* vc,
-                     const int32_t* lens, const uint32_t* mask, void* out, uint8_t* ws, cudaStream_t st);
+                     const int32_t* lens, void* out, uint8_t* ws, cudaStream_t st);
 int launch_kv_commit(const Plan& p, const int32_t* acc_nodes, const int32_t* accept_len, const void* kt,
                      const void* vt, void* kc, void* vc, int32_t* lens, uint8_t* ws, cudaStream_t st);
 int launch_next_inputs(const Plan& p, const void* attn_out, const int32_t* acc_nodes, const int32_t* accept_len,

@@ -354,8 +354,8 @@ int medusa_shard_partial(const medusa_config_t* cfg, const medusa_step_io_t* io,
   // the mask), then the attention over every node, then the verification over
   // this shard's rows, its per-node states into the record
   if (!e) e = launch_tree_build(p, nullptr, nullptr, t, st);
-  if (!e) e = launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, t.mask,
-                               io->attn_out, ws, st);
+  if (!e) e = launch_tree_attn(p, io->q, io->k_tree, io->v_tree, io->k_cache, io->v_cache, io->kv_lens, io->attn_out,
+                               ws, st);
   float4* node = reinterpret_cast<float4*>(rec + lay.off_node);
   if (!e) {
     if (p.bf16) {
