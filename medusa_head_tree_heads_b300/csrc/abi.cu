@@ -401,6 +401,11 @@ struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   bool failed = false;
+  ~SideStream() {  // at thread exit (errors ignored: the runtime may already be unloading)
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (s) cudaStreamDestroy(s);
+  }
 };
 static SideStream* side_stream(bool capturing) {
   constexpr int kMaxDevices = 64;
